@@ -1,0 +1,140 @@
+"""fp64 CPU oracle for scaled dot-product and multi-head attention.
+
+TEST INFRASTRUCTURE ONLY: imported by the tests, by the package smoke check
+and by the benchmark's CPU-baseline leg, never by the product path.  It shares
+no code with the CUDA library; the only module both sides use is the seeded
+input generator.
+
+The arithmetic lives in ``mha_oracle.c`` (plain C, fp64, libm ``exp``); this
+module only marshals numpy arrays through ctypes.  See that file's header for
+what is computed and which passage of the pages each step follows.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING, MASK_CAUSAL_KEY_PADDING = 0, 1, 2, 3
+
+_lib = None
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        # A test that plants a mistake in a copy of the oracle points this
+        # variable at the planted build; nothing else sets it.
+        path = os.environ.get("MHA_ORACLE_LIB") or _build.build()
+        lib = ctypes.CDLL(path)
+        dp = ctypes.POINTER(ctypes.c_double)
+        ip = ctypes.POINTER(ctypes.c_int32)
+        lp = ctypes.POINTER(ctypes.c_int64)
+        ci, cd, cl = ctypes.c_int, ctypes.c_double, ctypes.c_long
+        lib.oracle_sdpa.argtypes = [dp, dp, dp, dp, dp, ci, ci, ci, ci, ci, ci, cd, ci, ip]
+        lib.oracle_sdpa.restype = ci
+        lib.oracle_sdpa_rows.argtypes = [dp, dp, dp, dp, lp, cl, ci, ci, ci, ci, ci, ci, cd,
+                                         ci, ip]
+        lib.oracle_sdpa_rows.restype = ci
+        lib.oracle_mha.argtypes = [dp, dp, dp, dp, dp, dp, dp, ci, ci, ci, ci, ci, ci, ci, cd,
+                                   ci, ip, lp, cl]
+        lib.oracle_mha.restype = ci
+        lib.oracle_num_threads.argtypes = []
+        lib.oracle_num_threads.restype = ci
+        _lib = lib
+    return _lib
+
+
+def _d(a):
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _p(a, t=ctypes.c_double):
+    return None if a is None else a.ctypes.data_as(ctypes.POINTER(t))
+
+
+def _lens(key_lens, B):
+    if key_lens is None:
+        return None
+    kl = np.ascontiguousarray(key_lens, dtype=np.int32)
+    if kl.shape != (B,):
+        raise ValueError("key_lens must have B entries")
+    return kl
+
+
+def num_threads() -> int:
+    return int(_load().oracle_num_threads())
+
+
+def sdpa(q, k, v, scale=None, mask=MASK_NONE, key_lens=None, return_weights=False):
+    """softmax(scale * q k^T + mask) v for q (B,H,Tq,dk), k (B,H,Tk,dk),
+    v (B,H,Tk,dv).  Returns o (B,H,Tq,dv) [and weights (B,H,Tq,Tk)]."""
+    q, k, v = _d(q), _d(k), _d(v)
+    B, H, Tq, dk = q.shape
+    Tk, dv = k.shape[2], v.shape[3]
+    if k.shape != (B, H, Tk, dk) or v.shape != (B, H, Tk, dv):
+        raise ValueError("shape mismatch")
+    if scale is None:
+        scale = 1.0 / np.sqrt(dk)
+    kl = _lens(key_lens, B)
+    o = np.empty((B, H, Tq, dv))
+    w = np.empty((B, H, Tq, Tk)) if return_weights else None
+    rc = _load().oracle_sdpa(_p(q), _p(k), _p(v), _p(o), _p(w), B, H, Tq, Tk, dk, dv,
+                             float(scale), int(mask), _p(kl, ctypes.c_int32))
+    if rc:
+        raise RuntimeError("oracle_sdpa failed")
+    return (o, w) if return_weights else o
+
+
+def sdpa_rows(q, k, v, rows, scale=None, mask=MASK_NONE, key_lens=None):
+    """Output rows only: rows are flat indices (b*H + h)*Tq + i.  Returns
+    (len(rows), dv)."""
+    q, k, v = _d(q), _d(k), _d(v)
+    B, H, Tq, dk = q.shape
+    Tk, dv = k.shape[2], v.shape[3]
+    if scale is None:
+        scale = 1.0 / np.sqrt(dk)
+    r = np.ascontiguousarray(rows, dtype=np.int64)
+    kl = _lens(key_lens, B)
+    o = np.empty((len(r), dv))
+    rc = _load().oracle_sdpa_rows(_p(q), _p(k), _p(v), _p(o), _p(r, ctypes.c_int64), len(r),
+                                  B, H, Tq, Tk, dk, dv, float(scale), int(mask),
+                                  _p(kl, ctypes.c_int32))
+    if rc:
+        raise RuntimeError("oracle_sdpa_rows failed")
+    return o
+
+
+def mha(x_q, x_kv, w_q, w_k, w_v, w_o, h, scale=None, mask=MASK_NONE, key_lens=None,
+        query_rows=None):
+    """Concat_i(softmax(scale (x_q W_i^Q)(x_kv W_i^K)^T + mask) x_kv W_i^V) W^O.
+    x_q (B,Tq,D), x_kv (B,Tk,D), W^Q/W^K (D,h*dk), W^V (D,h*dv), W^O (h*dv,D).
+    Returns (B,Tq,D), or (len(query_rows), D) for flat query rows b*Tq + i."""
+    x_q, x_kv = _d(x_q), _d(x_kv)
+    w_q, w_k, w_v, w_o = _d(w_q), _d(w_k), _d(w_v), _d(w_o)
+    B, Tq, D = x_q.shape
+    Tk = x_kv.shape[1]
+    dk = w_q.shape[1] // h
+    dv = w_v.shape[1] // h
+    if (x_kv.shape != (B, Tk, D) or w_q.shape != (D, h * dk) or w_k.shape != (D, h * dk)
+            or w_v.shape != (D, h * dv) or w_o.shape != (h * dv, D)):
+        raise ValueError("shape mismatch")
+    if scale is None:
+        scale = 1.0 / np.sqrt(dk)
+    kl = _lens(key_lens, B)
+    if query_rows is None:
+        out = np.empty((B, Tq, D))
+        qr, n = None, 0
+    else:
+        qr = np.ascontiguousarray(query_rows, dtype=np.int64)
+        n = len(qr)
+        out = np.empty((n, D))
+    rc = _load().oracle_mha(_p(x_q), _p(x_kv), _p(w_q), _p(w_k), _p(w_v), _p(w_o), _p(out),
+                            B, h, Tq, Tk, D, dk, dv, float(scale), int(mask),
+                            _p(kl, ctypes.c_int32), _p(qr, ctypes.c_int64), n)
+    if rc:
+        raise RuntimeError("oracle_mha failed")
+    return out
