@@ -1,0 +1,136 @@
+/*
+ * mha.h -- C ABI of the GB300 (sm_103a) multi-head scaled dot-product
+ * attention forward library (libmha.so).
+ *
+ * The operation (cited by page title and section):
+ *
+ *   Attention(Q, K, V) = softmax(Q K^T / sqrt(d_k) + mask) V
+ *     "Attention Is All You Need" (azimuth.plus), "The idea: every word
+ *     queries every word"; "The Transformer: Attention Is All You Need"
+ *     (cuijiawei.cn), "The core idea: scaled dot-product attention" and its
+ *     scaled_dot_product_attention(q, k, v, mask) with masked_fill(-inf).
+ *
+ *   MultiHead = Concat(head_1, ..., head_h) W^O,
+ *   head_i = Attention(X_q W_i^Q, X_kv W_i^K, X_kv W_i^V)
+ *     "Attention Is All You Need: The Research Paper That Changed AI"
+ *     (muhitai.com), "Multi-Head Attention Formula"; notebook chapter
+ *     "Attention is All You Need", "Multi-Head Self-Attention" and "The
+ *     Decoder's Cross-Attention" (queries from the decoder, keys and values
+ *     from the encoder output).
+ *
+ *   Masks: causal -- query i sees key j only if j <= i (notebook chapter,
+ *   "Masked Attention in the Decoder"; muhitai.com "What Is Masked
+ *   Attention?"); key padding -- keys j >= key_lens[b] get weight zero.
+ *
+ * Conventions shared by every entry point:
+ *   - All tensor pointers are DEVICE pointers to caller-owned memory,
+ *     row-major and contiguous.  The library never allocates, frees or
+ *     synchronises; every launch is enqueued on `stream` (0 = legacy default
+ *     stream) and the call returns immediately.
+ *   - Argument errors are detected on the host before anything is enqueued
+ *     and returned synchronously (nothing is launched).  A failed launch
+ *     returns MHA_ERR_CUDA.
+ *   - `status_dev` (optional, may be NULL) is a device int the caller zeroes
+ *     before the call.  Every wait inside the kernels is bounded; a wait that
+ *     runs out stores MHA_ERR_TIMEOUT there and the kernel returns early
+ *     (its outputs are then undefined).  Read it after synchronising.
+ *   - `key_lens` is a DEVICE int32 array of B entries, used only with a
+ *     key-padding mask (NULL otherwise).  Values are clamped to [0, T_k].  A
+ *     query row that sees no key at all (key_lens[b] == 0) outputs zeros.
+ *   - Causal visibility is top-left aligned: key j is visible to query i iff
+ *     j <= i, also when T_q != T_k.
+ *   - The bf16 paths accumulate in fp32 (tensor memory), keep the softmax in
+ *     fp32, round the probabilities to bf16 for the P.V product and round
+ *     every stored tensor to bf16 (round to nearest even).
+ */
+#ifndef MHA_H
+#define MHA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MHA_OK = 0,
+    MHA_ERR_INVALID_ARG = 1, /* null pointer, negative size, bad enum, missing key_lens */
+    MHA_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. bf16 with d_k != 64) */
+    MHA_ERR_WORKSPACE = 3,   /* workspace NULL or smaller than mha_workspace_bytes() */
+    MHA_ERR_MISALIGNED = 4,  /* a bf16 pointer is not 16-byte aligned (TMA rule) */
+    MHA_ERR_CUDA = 5,        /* a CUDA runtime/driver call or a launch failed */
+    MHA_ERR_TIMEOUT = 6      /* written to *status_dev by a kernel whose wait ran out */
+} mha_status;
+
+typedef enum {
+    MHA_MASK_NONE = 0,
+    MHA_MASK_CAUSAL = 1,
+    MHA_MASK_KEY_PADDING = 2,
+    MHA_MASK_CAUSAL_KEY_PADDING = 3
+} mha_mask;
+
+typedef enum { MHA_F32 = 0, MHA_BF16 = 1 } mha_dtype;
+
+/*
+ * Scaled dot-product attention, o = softmax(scale * q k^T + mask) v.
+ *
+ *   q (B, h, T_q, d_k), k (B, h, T_k, d_k), v (B, h, T_k, d_v),
+ *   o (B, h, T_q, d_v): element type `dt` (fp32 or bf16).
+ *   scale: usually 1/sqrt(d_k) (aiany.app, Step 5: "divide by 8" for 64).
+ *
+ * MHA_F32: fp32 SIMT kernel (FFMA + expf), d_k, d_v <= 128.
+ * MHA_BF16: fused tcgen05 kernel (TMA tiles, QK^T and PV on the tensor cores
+ *   with fp32 accumulators in tensor memory, online softmax in registers; the
+ *   T_q x T_k score matrix never reaches global memory).  Requires
+ *   d_k == d_v == 64 and 16-byte aligned q, k, v, o.
+ * B, h, T_q, T_k >= 0 (a zero extent is a no-op; T_k == 0 with T_q > 0
+ * outputs zeros); B * h < 2^31.
+ */
+mha_status sdpa_forward(mha_dtype dt, const void *q, const void *k, const void *v, void *o,
+                        int B, int h, int T_q, int T_k, int d_k, int d_v, float scale,
+                        mha_mask mask, const int32_t *key_lens, int *status_dev,
+                        cudaStream_t stream);
+
+/*
+ * Bytes of device workspace mha_forward needs: the projected Q, K, V in
+ * head-split layout (B, h, T, d) and the merged attention output
+ * (B, T_q, h * d_v), all bf16, each region 256-byte aligned.
+ * Returns 0 for negative sizes.
+ */
+size_t mha_workspace_bytes(int B, int h, int T_q, int T_k, int d_k, int d_v);
+
+/*
+ * Multi-head attention forward, bf16 only:
+ *   out = Concat_i(softmax(scale * (x_q W_i^Q)(x_kv W_i^K)^T + mask)
+ *                  (x_kv W_i^V)) W^O
+ *
+ *   x_q (B, T_q, d_model); x_kv (B, T_k, d_model), may equal x_q for
+ *   self-attention; W^Q, W^K (d_model, h*d_k); W^V (d_model, h*d_v);
+ *   W^O (h*d_v, d_model); out (B, T_q, d_model).  Row-vector convention
+ *   y = x W (notebook chapter: W^Q in R^{d_model x d_k}); head i owns
+ *   columns [i*d_k, (i+1)*d_k) of W^Q/W^K/W^V; no bias.
+ *   workspace: device buffer of at least mha_workspace_bytes() bytes,
+ *   256-byte aligned, owned by the caller, not read before it is written.
+ *
+ * Three launches on `stream`: one grouped projection GEMM (Q, K, V with a
+ * head-split epilogue), the fused attention kernel (writing the merged
+ * (B, T_q, h*d_v) layout directly), and the W^O GEMM.
+ * Requires d_k == d_v == 64, d_model % 8 == 0 and 16-byte aligned pointers.
+ */
+mha_status mha_forward(mha_dtype dt, const void *x_q, const void *x_kv, const void *w_q,
+                       const void *w_k, const void *w_v, const void *w_o, void *out,
+                       void *workspace, size_t workspace_bytes, int B, int h, int T_q, int T_k,
+                       int d_model, int d_k, int d_v, float scale, mha_mask mask,
+                       const int32_t *key_lens, int *status_dev, cudaStream_t stream);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char *mha_status_string(mha_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MHA_H */

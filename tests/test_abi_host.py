@@ -1,0 +1,106 @@
+"""The C-ABI library loads without a GPU, exports every symbol include/mha.h
+declares, and rejects bad arguments on the host before launching anything."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from transformer_scaled_dot_softmax_gb300 import build
+    build.build()
+    from transformer_scaled_dot_softmax_gb300 import _native
+    return _native
+
+
+def declared_functions():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", h)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\*?\s*([a-z_][a-z0-9_]*)\s*\(",
+                                text, flags=re.M)
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert {"sdpa_forward", "mha_forward", "mha_workspace_bytes", "mha_status_string"} <= set(names)
+    raw = ctypes.CDLL(lib.LIB_PATH)
+    for n in names:
+        assert hasattr(raw, n), n
+        assert n in lib.SIGNATURES, n
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        s = lib.lib.mha_status_string(code)
+        assert s and s != b"unknown status"
+    assert lib.lib.mha_status_string(99) == b"unknown status"
+
+
+def test_workspace_bytes(lib):
+    ws = lib.lib.mha_workspace_bytes
+    assert ws(2, 16, 8192, 8192, 64, 64) == 4 * 2 * 16 * 8192 * 64 * 2
+    assert ws(1, 1, 3, 5, 64, 64) == 512 + 768 + 768 + 512  # regions rounded to 256 bytes
+    assert ws(-1, 1, 1, 1, 64, 64) == 0
+
+
+FAKE = 1 << 20  # never dereferenced: every case below fails validation first
+
+
+def sdpa(lib, dt=1, q=FAKE, k=FAKE, v=FAKE, o=FAKE, B=1, h=1, Tq=8, Tk=8, dk=64, dv=64,
+         scale=0.125, mask=0, lens=None):
+    return lib.lib.sdpa_forward(dt, q, k, v, o, B, h, Tq, Tk, dk, dv, scale, mask, lens, None, None)
+
+
+def test_sdpa_rejects_bad_arguments(lib):
+    assert sdpa(lib, q=None) == lib.MHA_ERR_INVALID_ARG
+    assert sdpa(lib, o=None) == lib.MHA_ERR_INVALID_ARG
+    assert sdpa(lib, B=-1) == lib.MHA_ERR_INVALID_ARG
+    assert sdpa(lib, dk=0) == lib.MHA_ERR_INVALID_ARG
+    assert sdpa(lib, mask=7) == lib.MHA_ERR_INVALID_ARG
+    assert sdpa(lib, mask=2, lens=None) == lib.MHA_ERR_INVALID_ARG
+    assert sdpa(lib, scale=float("nan")) == lib.MHA_ERR_INVALID_ARG
+    assert sdpa(lib, dt=5) == lib.MHA_ERR_INVALID_ARG
+    assert sdpa(lib, dk=32, dv=32) == lib.MHA_ERR_UNSUPPORTED
+    assert sdpa(lib, dt=0, dk=256) == lib.MHA_ERR_UNSUPPORTED
+    assert sdpa(lib, q=FAKE + 8) == lib.MHA_ERR_MISALIGNED
+    assert sdpa(lib, o=FAKE + 2) == lib.MHA_ERR_MISALIGNED
+
+
+def test_empty_problems_are_no_ops(lib):
+    assert sdpa(lib, B=0) == lib.MHA_OK
+    assert sdpa(lib, Tq=0) == lib.MHA_OK
+    assert sdpa(lib, h=0, q=None) == lib.MHA_OK
+
+
+def mha(lib, dt=1, x=FAKE, ws=FAKE, ws_bytes=1 << 40, B=1, h=2, Tq=8, Tk=8, D=128, dk=64,
+        mask=0, lens=None, w=FAKE):
+    return lib.lib.mha_forward(dt, x, x, w, w, w, w, FAKE, ws, ws_bytes, B, h, Tq, Tk, D, dk,
+                               dk, 0.125, mask, lens, None, None)
+
+
+def test_mha_rejects_bad_arguments(lib):
+    assert mha(lib, x=None) == lib.MHA_ERR_INVALID_ARG
+    assert mha(lib, h=0) == lib.MHA_ERR_INVALID_ARG
+    assert mha(lib, mask=3, lens=None) == lib.MHA_ERR_INVALID_ARG
+    assert mha(lib, dt=0) == lib.MHA_ERR_UNSUPPORTED
+    assert mha(lib, dk=128) == lib.MHA_ERR_UNSUPPORTED
+    assert mha(lib, D=100) == lib.MHA_ERR_UNSUPPORTED
+    assert mha(lib, ws=None) == lib.MHA_ERR_WORKSPACE
+    assert mha(lib, ws_bytes=100) == lib.MHA_ERR_WORKSPACE
+    assert mha(lib, ws=FAKE + 16) == lib.MHA_ERR_MISALIGNED
+    assert mha(lib, w=FAKE + 4) == lib.MHA_ERR_MISALIGNED
+    assert mha(lib, B=0) == lib.MHA_OK
+
+
+def test_python_binding_imports_without_gpu():
+    import transformer_scaled_dot_softmax_gb300 as m
+    assert m.status_string(6) == "kernel wait timed out"
+    assert m.MASKS["causal"] == 1

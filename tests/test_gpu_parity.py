@@ -1,0 +1,247 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle.
+
+Tolerances: fp32 path max-abs <= 1e-5; bf16 path max-abs <= 2e-2 and
+mean-abs <= 2e-3, over every compared output element.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import seeded_inputs as si
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+F32_MAX = 1e-5
+BF16_MAX, BF16_MEAN = 2e-2, 2e-3
+MASK_NAMES = {si.MASK_NONE: "none", si.MASK_CAUSAL: "causal",
+              si.MASK_KEY_PADDING: "key_padding", si.MASK_CAUSAL_KEY_PADDING: "causal_key_padding"}
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import transformer_scaled_dot_softmax_gb300 as m
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return m
+
+
+def dev():
+    return torch.device("cuda:0")
+
+
+def bf16_dev(bits):
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev()).view(torch.bfloat16)
+
+
+def f32_dev(x):
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(dev())
+
+
+def host(t):
+    return t.float().cpu().numpy().astype(np.float64)
+
+
+def check_bf16(got, ref, what=""):
+    assert np.all(np.isfinite(got)), what + ": non-finite output"
+    err = np.abs(got - ref)
+    assert err.max() <= BF16_MAX and err.mean() <= BF16_MEAN, (
+        "%s: max %.4g mean %.4g" % (what, err.max(), err.mean()))
+
+
+def lens_dev(x):
+    return None if x["key_lens"] is None else torch.from_numpy(x["key_lens"]).to(dev())
+
+
+def run_sdpa_bf16(lib, w, x, q=None, k=None, v=None, poison=True):
+    q = bf16_dev(x["q_bits"]) if q is None else q
+    k = bf16_dev(x["k_bits"]) if k is None else k
+    v = bf16_dev(x["v_bits"]) if v is None else v
+    out = torch.empty((w.B, w.h, w.T_q, w.d_v), dtype=torch.bfloat16, device=dev())
+    if poison:
+        out.fill_(float("nan"))
+    status = torch.zeros(1, dtype=torch.int32, device=dev())
+    lib.sdpa_forward(q, k, v, out, scale=w.scale, mask=w.mask, key_lens=lens_dev(x),
+                     status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return out
+
+
+# ----------------------------------------------------------------- fp32 path
+def test_config1_fp32_full(lib):
+    w = si.WORKLOADS[0]
+    x = si.make_inputs(w)
+    out = lib.sdpa_forward(f32_dev(x["q"]), f32_dev(x["k"]), f32_dev(x["v"]), scale=w.scale)
+    torch.cuda.synchronize()
+    ref = oracle.sdpa(x["q"], x["k"], x["v"], scale=w.scale)
+    assert np.abs(host(out) - ref).max() <= F32_MAX
+
+
+@pytest.mark.parametrize("mask", list(MASK_NAMES))
+@pytest.mark.parametrize("T_q,T_k,d", [(37, 53, 64), (16, 16, 32), (5, 200, 128), (130, 7, 64)])
+def test_fp32_masks_and_ragged(lib, mask, T_q, T_k, d):
+    w = si.WORKLOADS[0].replace(B=2, h=3, T_q=T_q, T_k=T_k, d_k=d, d_v=d, mask=mask, len_lo=1,
+                                len_hi=T_k, seed=11)
+    x = si.make_inputs(w)
+    out = lib.sdpa_forward(f32_dev(x["q"]), f32_dev(x["k"]), f32_dev(x["v"]), scale=w.scale,
+                           mask=mask, key_lens=lens_dev(x))
+    torch.cuda.synchronize()
+    ref = oracle.sdpa(x["q"], x["k"], x["v"], scale=w.scale, mask=mask, key_lens=x["key_lens"])
+    assert np.abs(host(out) - ref).max() <= F32_MAX
+
+
+# ----------------------------------------------------------------- bf16 SDPA
+BF16_SHAPES = [
+    (1, 1, 128, 128, si.MASK_NONE),
+    (1, 2, 1, 1, si.MASK_NONE),
+    (2, 2, 255, 257, si.MASK_NONE),
+    (1, 2, 256, 256, si.MASK_CAUSAL),
+    (1, 2, 300, 300, si.MASK_CAUSAL),
+    (2, 1, 513, 700, si.MASK_KEY_PADDING),
+    (2, 2, 384, 384, si.MASK_CAUSAL_KEY_PADDING),
+    (1, 1, 64, 1000, si.MASK_NONE),
+    (1, 1, 1000, 64, si.MASK_CAUSAL),
+    (3, 1, 129, 1025, si.MASK_KEY_PADDING),
+    (1, 3, 777, 777, si.MASK_CAUSAL),
+]
+
+
+@pytest.mark.parametrize("B,h,T_q,T_k,mask", BF16_SHAPES)
+def test_bf16_sdpa_vs_oracle(lib, B, h, T_q, T_k, mask):
+    w = si.WORKLOADS[4].replace(B=B, h=h, T_q=T_q, T_k=T_k, mask=mask, len_lo=1, len_hi=T_k,
+                                seed=21)
+    x = si.make_inputs(w)
+    out = run_sdpa_bf16(lib, w, x)
+    ref = oracle.sdpa(x["q"], x["k"], x["v"], scale=w.scale, mask=mask, key_lens=x["key_lens"])
+    check_bf16(host(out), ref, "B%d h%d Tq%d Tk%d mask%d" % (B, h, T_q, T_k, mask))
+
+
+def test_config5_full_size_sampled_rows(lib):
+    w = si.WORKLOADS[4]
+    x = si.make_inputs(w)
+    out = run_sdpa_bf16(lib, w, x)
+    got = host(out)
+    assert np.all(np.isfinite(got))
+    rng = np.random.default_rng(5)
+    rows_t = np.unique(np.concatenate([[0, 1, 127, 128, 255, 256, 257, 4095, 4096, 8190, 8191],
+                                       rng.integers(0, w.T_q, 200)]))
+    flat = []
+    for bh in range(w.B * w.h):
+        for t in rows_t[bh % 3::3]:
+            flat.append(bh * w.T_q + int(t))
+    flat = np.array(flat, dtype=np.int64)
+    ref = oracle.sdpa_rows(x["q"], x["k"], x["v"], flat, scale=w.scale, mask=w.mask)
+    check_bf16(got.reshape(-1, w.d_v)[flat], ref, "config 5 sampled rows")
+
+
+def test_bf16_padding_rows_bitwise_independent_of_masked_keys(lib):
+    w = si.WORKLOADS[4].replace(B=3, h=2, T_q=200, T_k=600, mask=si.MASK_KEY_PADDING,
+                                len_lo=100, len_hi=500, seed=31)
+    x = si.make_inputs(w)
+    a = run_sdpa_bf16(lib, w, x)
+    k = bf16_dev(x["k_bits"]).clone()
+    v = bf16_dev(x["v_bits"]).clone()
+    for b, L in enumerate(x["key_lens"]):
+        k[b, :, L:] = torch.randn_like(k[b, :, L:].float()).mul(30).bfloat16()
+        v[b, :, L:] = torch.randn_like(v[b, :, L:].float()).mul(30).bfloat16()
+    b2 = run_sdpa_bf16(lib, w, x, k=k, v=v)
+    assert torch.equal(a.view(torch.int16), b2.view(torch.int16))
+
+
+def test_bf16_causal_rows_bitwise_independent_of_future_keys(lib):
+    w = si.WORKLOADS[4].replace(B=1, h=2, T_q=400, T_k=400, mask=si.MASK_CAUSAL, seed=32)
+    x = si.make_inputs(w)
+    a = run_sdpa_bf16(lib, w, x)
+    k = bf16_dev(x["k_bits"]).clone()
+    v = bf16_dev(x["v_bits"]).clone()
+    cut = 250
+    k[:, :, cut:] = 7.0
+    v[:, :, cut:] = -9.0
+    b2 = run_sdpa_bf16(lib, w, x, k=k, v=v)
+    assert torch.equal(a[:, :, :cut].view(torch.int16), b2[:, :, :cut].view(torch.int16))
+    # causal row 0 sees key 0 only: output = V_0 (exactly representable)
+    assert torch.equal(a[:, :, 0], bf16_dev(x["v_bits"])[:, :, 0])
+
+
+def test_bf16_constant_values(lib):
+    w = si.WORKLOADS[4].replace(B=1, h=2, T_q=300, T_k=900, mask=si.MASK_NONE, seed=33)
+    x = si.make_inputs(w)
+    v = torch.full((w.B, w.h, w.T_k, w.d_v), 1.5, dtype=torch.bfloat16, device=dev())
+    out = run_sdpa_bf16(lib, w, x, v=v)
+    # P is rounded to bf16 but l is summed in fp32: within a few bf16 ulps
+    np.testing.assert_allclose(host(out), 1.5, rtol=0, atol=1.5 * 2 ** -7)
+
+
+def test_bf16_zero_length_rows_are_zero(lib):
+    w = si.WORKLOADS[4].replace(B=2, h=1, T_q=130, T_k=300, mask=si.MASK_KEY_PADDING, seed=34)
+    x = si.make_inputs(w)
+    x["key_lens"] = np.array([0, 123], dtype=np.int32)
+    out = run_sdpa_bf16(lib, w, x)
+    assert torch.all(out[0] == 0)
+    ref = oracle.sdpa(x["q"], x["k"], x["v"], scale=w.scale, mask=w.mask, key_lens=x["key_lens"])
+    check_bf16(host(out), ref, "zero-length rows")
+
+
+def test_bf16_on_side_stream(lib):
+    w = si.WORKLOADS[4].replace(B=1, h=2, T_q=256, T_k=256, mask=si.MASK_CAUSAL, seed=35)
+    x = si.make_inputs(w)
+    s = torch.cuda.Stream()
+    q, k, v = bf16_dev(x["q_bits"]), bf16_dev(x["k_bits"]), bf16_dev(x["v_bits"])
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        out = lib.sdpa_forward(q, k, v, scale=w.scale, mask="causal")
+    s.synchronize()
+    ref = oracle.sdpa(x["q"], x["k"], x["v"], scale=w.scale, mask=w.mask)
+    check_bf16(host(out), ref, "side stream")
+
+
+# ------------------------------------------------------------------ bf16 MHA
+def run_mha(lib, w, x):
+    xq = bf16_dev(x["x_q_bits"])
+    xkv = bf16_dev(x["x_kv_bits"]) if w.cross else xq
+    out = torch.full((w.B, w.T_q, w.d_model), float("nan"), dtype=torch.bfloat16, device=dev())
+    status = torch.zeros(1, dtype=torch.int32, device=dev())
+    lib.mha_forward(xq, xkv, bf16_dev(x["w_q_bits"]), bf16_dev(x["w_k_bits"]),
+                    bf16_dev(x["w_v_bits"]), bf16_dev(x["w_o_bits"]), h=w.h, out=out,
+                    scale=w.scale, mask=w.mask, key_lens=lens_dev(x), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return host(out)
+
+
+def oracle_mha(w, x, query_rows=None):
+    x_kv = x["x_kv"] if w.cross else x["x_q"]
+    return oracle.mha(x["x_q"], x_kv, x["w_q"], x["w_k"], x["w_v"], x["w_o"], h=w.h,
+                      scale=w.scale, mask=w.mask, key_lens=x["key_lens"], query_rows=query_rows)
+
+
+MHA_SMALL = [
+    # B, T_q, T_k, D, h, mask, cross
+    (2, 130, 130, 128, 2, si.MASK_KEY_PADDING, False),
+    (1, 300, 300, 192, 3, si.MASK_CAUSAL, False),
+    (2, 70, 333, 128, 2, si.MASK_KEY_PADDING, True),
+    (1, 257, 129, 256, 4, si.MASK_NONE, True),
+    (2, 64, 64, 64, 1, si.MASK_CAUSAL_KEY_PADDING, False),
+]
+
+
+@pytest.mark.parametrize("B,T_q,T_k,D,h,mask,cross", MHA_SMALL)
+def test_mha_small_vs_oracle(lib, B, T_q, T_k, D, h, mask, cross):
+    w = si.WORKLOADS[3].replace(B=B, T_q=T_q, T_k=T_k, d_model=D, h=h, mask=mask, cross=cross,
+                                len_lo=1, len_hi=T_k, seed=41)
+    x = si.make_inputs(w)
+    check_bf16(run_mha(lib, w, x), oracle_mha(w, x), "mha small")
+
+
+@pytest.mark.parametrize("idx", [1, 2])
+def test_mha_configs_full(lib, idx):
+    w = si.WORKLOADS[idx]
+    x = si.make_inputs(w)
+    check_bf16(run_mha(lib, w, x), oracle_mha(w, x), w.name)
+
+
+def test_mha_config4_full(lib):
+    w = si.WORKLOADS[3]
+    x = si.make_inputs(w)
+    check_bf16(run_mha(lib, w, x), oracle_mha(w, x), w.name)

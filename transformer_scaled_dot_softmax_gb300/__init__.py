@@ -1,0 +1,133 @@
+"""GB300 (sm_103a) multi-head scaled dot-product attention forward.
+
+A thin binding over the C ABI of libmha.so (include/mha.h): these functions
+only marshal arguments -- every step of the computation runs in the
+library's CUDA kernels.  PyTorch supplies device memory and the stream.
+
+    out = sdpa_forward(q, k, v, mask="causal")            # (B, h, T, 64) bf16
+    out = mha_forward(x_q, x_kv, w_q, w_k, w_v, w_o, h=8)  # (B, T, d_model) bf16
+"""
+from __future__ import annotations
+
+import math
+
+from . import _native
+from ._native import (MHA_BF16, MHA_F32, MHA_MASK_CAUSAL, MHA_MASK_CAUSAL_KEY_PADDING,
+                      MHA_MASK_KEY_PADDING, MHA_MASK_NONE, MHA_OK, lib)
+
+__all__ = ["sdpa_forward", "mha_forward", "mha_workspace_bytes", "status_string", "MhaError",
+           "MASKS", "lib"]
+
+MASKS = {"none": MHA_MASK_NONE, "causal": MHA_MASK_CAUSAL, "key_padding": MHA_MASK_KEY_PADDING,
+         "causal_key_padding": MHA_MASK_CAUSAL_KEY_PADDING}
+
+
+class MhaError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__("%s: %s (status %d)" % (what, status_string(code), code))
+        self.code = code
+
+
+def status_string(code: int) -> str:
+    return lib.mha_status_string(int(code)).decode()
+
+
+def _mask_code(mask) -> int:
+    if isinstance(mask, str):
+        return MASKS[mask]
+    return int(mask)
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_handle(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _check_dev(name, t, dtype=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError("%s must be %s" % (name, dtype))
+
+
+def sdpa_forward(q, k, v, out=None, *, scale=None, mask="none", key_lens=None, status=None,
+                 stream=None):
+    """softmax(scale * q k^T + mask) v for q (B,h,T_q,d_k), k (B,h,T_k,d_k),
+    v (B,h,T_k,d_v); fp32 or bf16 CUDA tensors.  Returns out (B,h,T_q,d_v)."""
+    torch = _torch()
+    dtype = q.dtype
+    if dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("q must be float32 or bfloat16")
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _check_dev(n, t, dtype)
+    B, h, T_q, d_k = q.shape
+    T_k, d_v = k.shape[2], v.shape[3]
+    if out is None:
+        out = torch.empty((B, h, T_q, d_v), dtype=dtype, device=q.device)
+    _check_dev("out", out, dtype)
+    if key_lens is not None:
+        _check_dev("key_lens", key_lens, torch.int32)
+    if status is not None:
+        _check_dev("status", status, torch.int32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_k)
+    rc = lib.sdpa_forward(MHA_F32 if dtype == torch.float32 else MHA_BF16, _ptr(q), _ptr(k),
+                          _ptr(v), _ptr(out), B, h, T_q, T_k, d_k, d_v, float(scale),
+                          _mask_code(mask), _ptr(key_lens), _ptr(status), _stream_handle(stream))
+    if rc != MHA_OK:
+        raise MhaError(rc, "sdpa_forward")
+    return out
+
+
+def mha_workspace_bytes(B, h, T_q, T_k, d_k=64, d_v=64) -> int:
+    return int(lib.mha_workspace_bytes(B, h, T_q, T_k, d_k, d_v))
+
+
+def mha_forward(x_q, x_kv, w_q, w_k, w_v, w_o, h, out=None, workspace=None, *, scale=None,
+                mask="none", key_lens=None, status=None, stream=None):
+    """Concat_i(softmax(scale (x_q W_i^Q)(x_kv W_i^K)^T + mask)(x_kv W_i^V)) W^O
+    for bf16 CUDA tensors x_q (B,T_q,D), x_kv (B,T_k,D) (may be x_q),
+    W^Q/W^K/W^V (D, h*64), W^O (h*64, D).  Returns out (B,T_q,D)."""
+    torch = _torch()
+    bf = torch.bfloat16
+    for n, t in (("x_q", x_q), ("x_kv", x_kv), ("w_q", w_q), ("w_k", w_k), ("w_v", w_v),
+                 ("w_o", w_o)):
+        _check_dev(n, t, bf)
+    B, T_q, D = x_q.shape
+    T_k = x_kv.shape[1]
+    d_k = w_q.shape[1] // h
+    d_v = w_v.shape[1] // h
+    if out is None:
+        out = torch.empty((B, T_q, D), dtype=bf, device=x_q.device)
+    _check_dev("out", out, bf)
+    need = mha_workspace_bytes(B, h, T_q, T_k, d_k, d_v)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x_q.device)
+    _check_dev("workspace", workspace)
+    if key_lens is not None:
+        _check_dev("key_lens", key_lens, torch.int32)
+    if status is not None:
+        _check_dev("status", status, torch.int32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_k)
+    rc = lib.mha_forward(MHA_BF16, _ptr(x_q), _ptr(x_kv), _ptr(w_q), _ptr(w_k), _ptr(w_v),
+                         _ptr(w_o), _ptr(out), _ptr(workspace),
+                         workspace.numel() * workspace.element_size(), B, h, T_q, T_k, D, d_k,
+                         d_v, float(scale), _mask_code(mask), _ptr(key_lens), _ptr(status),
+                         _stream_handle(stream))
+    if rc != MHA_OK:
+        raise MhaError(rc, "mha_forward")
+    return out

@@ -1,0 +1,43 @@
+"""ctypes view of libmha.so (the C ABI in include/mha.h).
+
+Loading never touches the GPU.  If the library has not been built the import
+fails loudly: there is no fallback implementation."""
+from __future__ import annotations
+
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libmha.so")
+
+MHA_OK, MHA_ERR_INVALID_ARG, MHA_ERR_UNSUPPORTED, MHA_ERR_WORKSPACE = 0, 1, 2, 3
+MHA_ERR_MISALIGNED, MHA_ERR_CUDA, MHA_ERR_TIMEOUT = 4, 5, 6
+MHA_F32, MHA_BF16 = 0, 1
+MHA_MASK_NONE, MHA_MASK_CAUSAL, MHA_MASK_KEY_PADDING, MHA_MASK_CAUSAL_KEY_PADDING = 0, 1, 2, 3
+
+# Every symbol include/mha.h declares, with its ctypes signature.
+_vp, _ci, _cf, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+SIGNATURES = {
+    "sdpa_forward": (_ci, [_ci, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _ci, _cf, _ci, _vp,
+                           _vp, _vp]),
+    "mha_workspace_bytes": (_sz, [_ci, _ci, _ci, _ci, _ci, _ci]),
+    "mha_forward": (_ci, [_ci, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _ci, _ci, _ci, _ci,
+                          _ci, _ci, _ci, _cf, _ci, _vp, _vp, _vp]),
+    "mha_status_string": (ctypes.c_char_p, [_ci]),
+}
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(
+            "libmha.so is not built (%s); run transformer_scaled_dot_softmax_gb300.build.build() "
+            "or __graft_entry__.build() -- there is no CPU fallback" % LIB_PATH)
+    lib = ctypes.CDLL(LIB_PATH)
+    for name, (res, args) in SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+lib = _load()

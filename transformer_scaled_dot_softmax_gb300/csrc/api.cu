@@ -1,0 +1,275 @@
+// api.cu -- the C ABI declared in include/mha.h: argument checks, TMA
+// tensor-map encoding and kernel launches on the caller's stream.  Nothing
+// here allocates, frees or synchronises.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "../../include/mha.h"
+#include "kernels.h"
+
+#define MHA_EXPORT extern "C" __attribute__((visibility("default")))
+
+namespace {
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, looked up once through the runtime so the
+// library does not link libcuda directly.
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// bf16 tensor map with 128-byte swizzling.  dims/strides are innermost first;
+// strides are in bytes for dims 1..rank-1.
+mha_status encode_bf16(CUtensorMap *m, const void *base, int rank, const uint64_t *dims,
+                       const uint64_t *strides_bytes, const uint32_t *box) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return MHA_ERR_CUDA;
+    cuuint64_t d[5], s[4];
+    cuuint32_t bx[5], es[5];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        bx[i] = box[i];
+        es[i] = 1;
+        if (i + 1 < rank) s[i] = strides_bytes[i];
+    }
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, static_cast<cuuint32_t>(rank),
+                    const_cast<void *>(base), d, s, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? MHA_OK : MHA_ERR_CUDA;
+}
+
+// (B*H, T, 64) head-split bf16 tensor, 128-row boxes.
+mha_status encode_heads(CUtensorMap *m, const void *base, long long BH, int T) {
+    const uint64_t dims[3] = {64, static_cast<uint64_t>(T), static_cast<uint64_t>(BH)};
+    const uint64_t strides[2] = {128, static_cast<uint64_t>(T) * 128};
+    const uint32_t box[3] = {64, 128, 1};
+    return encode_bf16(m, base, 3, dims, strides, box);
+}
+
+// Activation (M rows x K) row-major: box 64 (K) x 128 (rows).
+mha_status encode_act(CUtensorMap *m, const void *base, long long M, int K) {
+    const uint64_t dims[2] = {static_cast<uint64_t>(K), static_cast<uint64_t>(M)};
+    const uint64_t strides[1] = {static_cast<uint64_t>(K) * 2};
+    const uint32_t box[2] = {64, 128};
+    return encode_bf16(m, base, 2, dims, strides, box);
+}
+
+// Weight (K rows x N) row-major viewed as (64, K, N/64): box (64, 64, 2).
+mha_status encode_weight(CUtensorMap *m, const void *base, int K, int N) {
+    const uint64_t dims[3] = {64, static_cast<uint64_t>(K), static_cast<uint64_t>(N / 64)};
+    const uint64_t strides[2] = {static_cast<uint64_t>(N) * 2, 128};
+    const uint32_t box[3] = {64, 64, 2};
+    return encode_bf16(m, base, 3, dims, strides, box);
+}
+
+bool valid_mask(int mask) { return mask >= MHA_MASK_NONE && mask <= MHA_MASK_CAUSAL_KEY_PADDING; }
+
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+mha_status launch_status(cudaError_t e) { return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA; }
+
+mha_status run_attention_bf16(const void *q, const void *k, const void *v, void *o,
+                              long long o_sb, long long o_sh, long long o_st, int B, int h,
+                              int T_q, int T_k, float scale, int mask, const int32_t *key_lens,
+                              int *status_dev, cudaStream_t stream) {
+    CUtensorMap tq, tk, tv;
+    const long long BH = static_cast<long long>(B) * h;
+    mha_status s;
+    // T_k == 0: keys do not exist; the kernel then writes zeros.  A TMA map
+    // needs every extent >= 1, so describe a one-row tensor it never loads.
+    const int Tk_map = T_k > 0 ? T_k : 1;
+    if ((s = encode_heads(&tq, q, BH, T_q)) != MHA_OK) return s;
+    if ((s = encode_heads(&tk, k, BH, Tk_map)) != MHA_OK) return s;
+    if ((s = encode_heads(&tv, v, BH, Tk_map)) != MHA_OK) return s;
+    mha::AttnParams p;
+    p.B = B;
+    p.H = h;
+    p.Tq = T_q;
+    p.Tk = T_k;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.mask = mask;
+    p.key_lens = key_lens;
+    p.o = static_cast<__nv_bfloat16 *>(o);
+    p.o_stride_b = o_sb;
+    p.o_stride_h = o_sh;
+    p.o_stride_t = o_st;
+    p.num_qblocks = (T_q + mha::kAttnRowsPerCta - 1) / mha::kAttnRowsPerCta;
+    p.status = status_dev;
+    return launch_status(mha::launch_attn_bf16(tq, tk, tv, p, stream));
+}
+
+}  // namespace
+
+MHA_EXPORT const char *mha_status_string(mha_status status) {
+    switch (status) {
+        case MHA_OK: return "ok";
+        case MHA_ERR_INVALID_ARG: return "invalid argument";
+        case MHA_ERR_UNSUPPORTED: return "unsupported configuration";
+        case MHA_ERR_WORKSPACE: return "workspace missing or too small";
+        case MHA_ERR_MISALIGNED: return "pointer not 16-byte aligned";
+        case MHA_ERR_CUDA: return "CUDA error";
+        case MHA_ERR_TIMEOUT: return "kernel wait timed out";
+    }
+    return "unknown status";
+}
+
+MHA_EXPORT mha_status sdpa_forward(mha_dtype dt, const void *q, const void *k, const void *v,
+                                   void *o, int B, int h, int T_q, int T_k, int d_k, int d_v,
+                                   float scale, mha_mask mask, const int32_t *key_lens,
+                                   int *status_dev, cudaStream_t stream) {
+    if (B < 0 || h < 0 || T_q < 0 || T_k < 0 || d_k <= 0 || d_v <= 0) return MHA_ERR_INVALID_ARG;
+    if (!valid_mask(mask) || !isfinite(scale)) return MHA_ERR_INVALID_ARG;
+    if ((mask & MHA_MASK_KEY_PADDING) && !key_lens) return MHA_ERR_INVALID_ARG;
+    if (static_cast<long long>(B) * h >= (1ll << 31)) return MHA_ERR_UNSUPPORTED;
+    if (B == 0 || h == 0 || T_q == 0) return MHA_OK;
+    if (!q || !o || (T_k > 0 && (!k || !v))) return MHA_ERR_INVALID_ARG;
+    if (dt == MHA_F32) {
+        if (d_k > 128 || d_v > 128) return MHA_ERR_UNSUPPORTED;
+        if ((T_q + 3) / 4 > 65535) return MHA_ERR_UNSUPPORTED;
+        return launch_status(mha::launch_sdpa_f32(
+            static_cast<const float *>(q), static_cast<const float *>(k),
+            static_cast<const float *>(v), static_cast<float *>(o), B, h, T_q, T_k, d_k, d_v,
+            scale, mask, key_lens, stream));
+    }
+    if (dt != MHA_BF16) return MHA_ERR_INVALID_ARG;
+    if (d_k != 64 || d_v != 64) return MHA_ERR_UNSUPPORTED;
+    if ((T_q + mha::kAttnRowsPerCta - 1) / mha::kAttnRowsPerCta > 65535) return MHA_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(o) || (T_k > 0 && (!aligned16(k) || !aligned16(v))))
+        return MHA_ERR_MISALIGNED;
+    const long long so_t = 64, so_h = static_cast<long long>(T_q) * 64, so_b = so_h * h;
+    return run_attention_bf16(q, T_k > 0 ? k : q, T_k > 0 ? v : q, o, so_b, so_h, so_t, B, h,
+                              T_q, T_k, scale, mask, key_lens, status_dev, stream);
+}
+
+MHA_EXPORT size_t mha_workspace_bytes(int B, int h, int T_q, int T_k, int d_k, int d_v) {
+    if (B < 0 || h < 0 || T_q < 0 || T_k < 0 || d_k < 0 || d_v < 0) return 0;
+    const size_t bh = static_cast<size_t>(B) * h;
+    return round256(bh * T_q * d_k * 2) + round256(bh * T_k * d_k * 2) +
+           round256(bh * T_k * d_v * 2) + round256(bh * T_q * d_v * 2);
+}
+
+MHA_EXPORT mha_status mha_forward(mha_dtype dt, const void *x_q, const void *x_kv,
+                                  const void *w_q, const void *w_k, const void *w_v,
+                                  const void *w_o, void *out, void *workspace,
+                                  size_t workspace_bytes, int B, int h, int T_q, int T_k,
+                                  int d_model, int d_k, int d_v, float scale, mha_mask mask,
+                                  const int32_t *key_lens, int *status_dev, cudaStream_t stream) {
+    if (B < 0 || h <= 0 || T_q < 0 || T_k < 0 || d_model <= 0 || d_k <= 0 || d_v <= 0)
+        return MHA_ERR_INVALID_ARG;
+    if (!valid_mask(mask) || !isfinite(scale)) return MHA_ERR_INVALID_ARG;
+    if ((mask & MHA_MASK_KEY_PADDING) && !key_lens) return MHA_ERR_INVALID_ARG;
+    if (dt != MHA_BF16) return dt == MHA_F32 ? MHA_ERR_UNSUPPORTED : MHA_ERR_INVALID_ARG;
+    if (d_k != 64 || d_v != 64) return MHA_ERR_UNSUPPORTED;
+    if (d_model % 64 != 0) return MHA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(B) * h >= (1ll << 31) ||
+        static_cast<long long>(B) * (T_q > T_k ? T_q : T_k) >= (1ll << 31))
+        return MHA_ERR_UNSUPPORTED;
+    if ((T_q + mha::kAttnRowsPerCta - 1) / mha::kAttnRowsPerCta > 65535) return MHA_ERR_UNSUPPORTED;
+    if (B == 0 || T_q == 0) return MHA_OK;
+    if (!x_q || !out || !w_q || !w_o || (T_k > 0 && (!x_kv || !w_k || !w_v)))
+        return MHA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < mha_workspace_bytes(B, h, T_q, T_k, d_k, d_v))
+        return MHA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MHA_ERR_MISALIGNED;
+    if (!aligned16(x_q) || !aligned16(out) || !aligned16(w_q) || !aligned16(w_o) ||
+        (T_k > 0 && (!aligned16(x_kv) || !aligned16(w_k) || !aligned16(w_v))))
+        return MHA_ERR_MISALIGNED;
+
+    const int hd = h * 64;
+    const size_t bh = static_cast<size_t>(B) * h;
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    void *qh = ws;
+    void *kh = ws + round256(bh * T_q * 128);
+    void *vh = static_cast<uint8_t *>(kh) + round256(bh * T_k * 128);
+    void *om = static_cast<uint8_t *>(vh) + round256(bh * T_k * 128);
+    const long long Mq = static_cast<long long>(B) * T_q, Mk = static_cast<long long>(B) * T_k;
+
+    // 1. Q, K, V projections with the head split folded into the epilogue.
+    CUtensorMap ta[mha::kGemmMaxProblems], tb[mha::kGemmMaxProblems];
+    mha::GemmParams gp{};
+    gp.status = status_dev;
+    mha_status s;
+    struct In {
+        const void *x, *w;
+        void *out;
+        long long M;
+        int T;
+    } ins[3] = {{x_q, w_q, qh, Mq, T_q}, {x_kv, w_k, kh, Mk, T_k}, {x_kv, w_v, vh, Mk, T_k}};
+    int np = 0, tiles = 0;
+    for (int i = 0; i < 3; ++i) {
+        if (ins[i].M == 0) continue;
+        if ((s = encode_act(&ta[np], ins[i].x, ins[i].M, d_model)) != MHA_OK) return s;
+        if ((s = encode_weight(&tb[np], ins[i].w, d_model, hd)) != MHA_OK) return s;
+        mha::GemmProblem &pr = gp.prob[np];
+        pr.M = static_cast<int>(ins[i].M);
+        pr.N = hd;
+        pr.K = d_model;
+        pr.tiles_n = (hd + mha::kGemmBN - 1) / mha::kGemmBN;
+        pr.tile_start = tiles;
+        pr.tile_count = pr.tiles_n * static_cast<int>((ins[i].M + mha::kGemmBM - 1) / mha::kGemmBM);
+        pr.out = static_cast<__nv_bfloat16 *>(ins[i].out);
+        pr.out_mode = mha::kOutHeadSplit;
+        pr.T = ins[i].T;
+        pr.H = h;
+        tiles += pr.tile_count;
+        ++np;
+    }
+    for (int i = np; i < mha::kGemmMaxProblems; ++i) {
+        ta[i] = ta[0];
+        tb[i] = tb[0];
+    }
+    gp.num_problems = np;
+    gp.total_tiles = tiles;
+    if ((s = launch_status(mha::launch_gemm_bf16(ta, tb, gp, stream))) != MHA_OK) return s;
+
+    // 2. Fused attention, writing the merged (B, T_q, h*64) layout directly.
+    if ((s = run_attention_bf16(qh, T_k > 0 ? kh : qh, T_k > 0 ? vh : qh, om,
+                                static_cast<long long>(T_q) * hd, 64, hd, B, h, T_q, T_k, scale,
+                                mask, key_lens, status_dev, stream)) != MHA_OK)
+        return s;
+
+    // 3. Output projection Concat(heads) W^O.
+    mha::GemmParams go{};
+    go.status = status_dev;
+    if ((s = encode_act(&ta[0], om, Mq, hd)) != MHA_OK) return s;
+    if ((s = encode_weight(&tb[0], w_o, hd, d_model)) != MHA_OK) return s;
+    for (int i = 1; i < mha::kGemmMaxProblems; ++i) {
+        ta[i] = ta[0];
+        tb[i] = tb[0];
+    }
+    mha::GemmProblem &pr = go.prob[0];
+    pr.M = static_cast<int>(Mq);
+    pr.N = d_model;
+    pr.K = hd;
+    pr.tiles_n = (d_model + mha::kGemmBN - 1) / mha::kGemmBN;
+    pr.tile_start = 0;
+    pr.tile_count = pr.tiles_n * static_cast<int>((Mq + mha::kGemmBM - 1) / mha::kGemmBM);
+    pr.out = static_cast<__nv_bfloat16 *>(out);
+    pr.out_mode = mha::kOutRowMajor;
+    pr.T = T_q;
+    pr.H = h;
+    go.num_problems = 1;
+    go.total_tiles = pr.tile_count;
+    return launch_status(mha::launch_gemm_bf16(ta, tb, go, stream));
+}

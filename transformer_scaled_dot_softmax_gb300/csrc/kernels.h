@@ -1,0 +1,63 @@
+// kernels.h -- launch interfaces between the C ABI (api.cu) and the kernels.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace mha {
+
+constexpr int kMaskCausalBit = 1;
+constexpr int kMaskPaddingBit = 2;
+
+// ------------------------------------------------ fused bf16 attention
+struct AttnParams {
+    int B, H, Tq, Tk;
+    float scale_log2;  // scale * log2(e): scores are exponentiated with ex2
+    int mask;          // kMaskCausalBit | kMaskPaddingBit
+    const int32_t *key_lens;
+    __nv_bfloat16 *o;  // output; element (b, h, t, c) at o + b*sb + h*sh + t*st + c
+    long long o_stride_b, o_stride_h, o_stride_t;
+    int num_qblocks;   // ceil(Tq / rows per CTA)
+    int *status;
+};
+constexpr int kAttnRowsPerCta = 256;  // two 128-row query tiles per CTA
+constexpr int kAttnHeadDim = 64;
+
+// q, k, v: head-split (B, H, T, 64) bf16 tensors described by 3-D TMA maps
+// over (64, T, B*H) with 128-byte swizzling and 128-row boxes.
+cudaError_t launch_attn_bf16(const CUtensorMap &tq, const CUtensorMap &tk,
+                             const CUtensorMap &tv, const AttnParams &p, cudaStream_t stream);
+
+// ------------------------------------------------ fp32 SIMT attention
+cudaError_t launch_sdpa_f32(const float *q, const float *k, const float *v, float *o, int B,
+                            int H, int Tq, int Tk, int dk, int dv, float scale, int mask,
+                            const int32_t *key_lens, cudaStream_t stream);
+
+// ------------------------------------------------ bf16 projection GEMM
+constexpr int kGemmMaxProblems = 3;
+enum GemmOutMode { kOutRowMajor = 0, kOutHeadSplit = 1 };
+struct GemmProblem {
+    int M, N, K;
+    int tiles_n, tile_start, tile_count;
+    __nv_bfloat16 *out;
+    int out_mode;  // kOutRowMajor: out (M, N); kOutHeadSplit: row m = b*T + t,
+                   // column n = head*64 + c -> out ((b*H + head)*T + t)*64 + c
+    int T, H;
+};
+struct GemmParams {
+    int num_problems;
+    int total_tiles;
+    GemmProblem prob[kGemmMaxProblems];
+    int *status;
+};
+constexpr int kGemmBM = 128, kGemmBN = 128, kGemmBK = 64;
+
+// a[i]: 2-D TMA map over the activation (K inner, M rows), box (64, 128).
+// b[i]: 3-D TMA map over the weight viewed as (64, K, N/64), box (64, 64, 2).
+cudaError_t launch_gemm_bf16(const CUtensorMap (&a)[kGemmMaxProblems],
+                             const CUtensorMap (&b)[kGemmMaxProblems], const GemmParams &p,
+                             cudaStream_t stream);
+
+}  // namespace mha
