@@ -118,7 +118,7 @@ size_t mha_workspace_bytes(int B, int h, int T_q, int T_k, int d_k, int d_v);
  * Three launches on `stream`: one grouped projection GEMM (Q, K, V with a
  * head-split epilogue), the fused attention kernel (writing the merged
  * (B, T_q, h*d_v) layout directly), and the W^O GEMM.
- * Requires d_k == d_v == 64, d_model % 8 == 0 and 16-byte aligned pointers.
+ * Requires d_k == d_v == 64, d_model % 64 == 0 and 16-byte aligned pointers.
  */
 mha_status mha_forward(mha_dtype dt, const void *x_q, const void *x_kv, const void *w_q,
                        const void *w_k, const void *w_v, const void *w_o, void *out,
@@ -128,6 +128,11 @@ mha_status mha_forward(mha_dtype dt, const void *x_q, const void *x_kv, const vo
 
 /* Static, human-readable name of a status code (never NULL). */
 const char *mha_status_string(mha_status status);
+
+/* Detail of the most recent MHA_ERR_CUDA returned on the calling thread
+ * (which step failed and the CUDA error name), or "" if none.  The string is
+ * owned by the library and stays valid until the thread's next call. */
+const char *mha_last_error(void);
 
 #ifdef __cplusplus
 }

@@ -11,8 +11,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 @pytest.fixture(scope="module")
 def lib():
-    from transformer_scaled_dot_softmax_gb300 import build
-    build.build()
+    import __graft_entry__
+    __graft_entry__.build()
     from transformer_scaled_dot_softmax_gb300 import _native
     return _native
 

@@ -24,7 +24,9 @@ MASKS = {"none": MHA_MASK_NONE, "causal": MHA_MASK_CAUSAL, "key_padding": MHA_MA
 
 class MhaError(RuntimeError):
     def __init__(self, code: int, what: str):
-        super().__init__("%s: %s (status %d)" % (what, status_string(code), code))
+        detail = lib.mha_last_error().decode() if code == _native.MHA_ERR_CUDA else ""
+        super().__init__("%s: %s (status %d)%s" % (what, status_string(code), code,
+                                                   " -- " + detail if detail else ""))
         self.code = code
 
 

@@ -24,6 +24,7 @@ SIGNATURES = {
     "mha_forward": (_ci, [_ci, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _ci, _ci, _ci, _ci,
                           _ci, _ci, _ci, _cf, _ci, _vp, _vp, _vp]),
     "mha_status_string": (ctypes.c_char_p, [_ci]),
+    "mha_last_error": (ctypes.c_char_p, []),
 }
 
 

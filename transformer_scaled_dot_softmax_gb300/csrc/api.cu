@@ -6,6 +6,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <stdio.h>
+
 #include <mutex>
 
 #include "../../include/mha.h"
@@ -36,6 +38,13 @@ EncodeTiledFn encode_fn() {
     return fn;
 }
 
+thread_local char g_last_error[256] = "";
+
+mha_status cuda_fail(const char *what, const char *detail) {
+    snprintf(g_last_error, sizeof(g_last_error), "%s: %s", what, detail);
+    return MHA_ERR_CUDA;
+}
+
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // bf16 tensor map with 128-byte swizzling.  dims/strides are innermost first;
@@ -43,7 +52,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 mha_status encode_bf16(CUtensorMap *m, const void *base, int rank, const uint64_t *dims,
                        const uint64_t *strides_bytes, const uint32_t *box) {
     EncodeTiledFn fn = encode_fn();
-    if (!fn) return MHA_ERR_CUDA;
+    if (!fn) return cuda_fail("cuTensorMapEncodeTiled", "driver entry point not found");
     cuuint64_t d[5], s[4];
     cuuint32_t bx[5], es[5];
     for (int i = 0; i < rank; ++i) {
@@ -56,7 +65,14 @@ mha_status encode_bf16(CUtensorMap *m, const void *base, int rank, const uint64_
                     const_cast<void *>(base), d, s, bx, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? MHA_OK : MHA_ERR_CUDA;
+    if (r != CUDA_SUCCESS) {
+        char buf[96];
+        snprintf(buf, sizeof(buf), "CUresult %d (rank %d, dims %llu x %llu x %llu)", (int)r, rank,
+                 (unsigned long long)d[0], (unsigned long long)(rank > 1 ? d[1] : 0),
+                 (unsigned long long)(rank > 2 ? d[2] : 0));
+        return cuda_fail("cuTensorMapEncodeTiled", buf);
+    }
+    return MHA_OK;
 }
 
 // (B*H, T, 64) head-split bf16 tensor, 128-row boxes.
@@ -87,7 +103,10 @@ bool valid_mask(int mask) { return mask >= MHA_MASK_NONE && mask <= MHA_MASK_CAU
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
-mha_status launch_status(cudaError_t e) { return e == cudaSuccess ? MHA_OK : MHA_ERR_CUDA; }
+mha_status launch_status(cudaError_t e, const char *what) {
+    if (e == cudaSuccess) return MHA_OK;
+    return cuda_fail(what, cudaGetErrorName(e));
+}
 
 mha_status run_attention_bf16(const void *q, const void *k, const void *v, void *o,
                               long long o_sb, long long o_sh, long long o_st, int B, int h,
@@ -116,7 +135,7 @@ mha_status run_attention_bf16(const void *q, const void *k, const void *v, void 
     p.o_stride_t = o_st;
     p.num_qblocks = (T_q + mha::kAttnRowsPerCta - 1) / mha::kAttnRowsPerCta;
     p.status = status_dev;
-    return launch_status(mha::launch_attn_bf16(tq, tk, tv, p, stream));
+    return launch_status(mha::launch_attn_bf16(tq, tk, tv, p, stream), "attention launch");
 }
 
 }  // namespace
@@ -134,6 +153,8 @@ MHA_EXPORT const char *mha_status_string(mha_status status) {
     return "unknown status";
 }
 
+MHA_EXPORT const char *mha_last_error(void) { return g_last_error; }
+
 MHA_EXPORT mha_status sdpa_forward(mha_dtype dt, const void *q, const void *k, const void *v,
                                    void *o, int B, int h, int T_q, int T_k, int d_k, int d_v,
                                    float scale, mha_mask mask, const int32_t *key_lens,
@@ -150,7 +171,7 @@ MHA_EXPORT mha_status sdpa_forward(mha_dtype dt, const void *q, const void *k, c
         return launch_status(mha::launch_sdpa_f32(
             static_cast<const float *>(q), static_cast<const float *>(k),
             static_cast<const float *>(v), static_cast<float *>(o), B, h, T_q, T_k, d_k, d_v,
-            scale, mask, key_lens, stream));
+            scale, mask, key_lens, stream), "fp32 attention launch");
     }
     if (dt != MHA_BF16) return MHA_ERR_INVALID_ARG;
     if (d_k != 64 || d_v != 64) return MHA_ERR_UNSUPPORTED;
@@ -241,7 +262,9 @@ MHA_EXPORT mha_status mha_forward(mha_dtype dt, const void *x_q, const void *x_k
     }
     gp.num_problems = np;
     gp.total_tiles = tiles;
-    if ((s = launch_status(mha::launch_gemm_bf16(ta, tb, gp, stream))) != MHA_OK) return s;
+    if ((s = launch_status(mha::launch_gemm_bf16(ta, tb, gp, stream), "projection GEMM launch")) !=
+        MHA_OK)
+        return s;
 
     // 2. Fused attention, writing the merged (B, T_q, h*64) layout directly.
     if ((s = run_attention_bf16(qh, T_k > 0 ? kh : qh, T_k > 0 ? vh : qh, om,
@@ -271,5 +294,5 @@ MHA_EXPORT mha_status mha_forward(mha_dtype dt, const void *x_q, const void *x_k
     pr.H = h;
     go.num_problems = 1;
     go.total_tiles = pr.tile_count;
-    return launch_status(mha::launch_gemm_bf16(ta, tb, go, stream));
+    return launch_status(mha::launch_gemm_bf16(ta, tb, go, stream), "output GEMM launch");
 }

@@ -76,7 +76,7 @@ struct __align__(1024) SmemAttn {
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
 
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q,
                          const __grid_constant__ CUtensorMap tmap_k,
                          const __grid_constant__ CUtensorMap tmap_v, const AttnParams p) {
@@ -246,80 +246,84 @@ __global__ void __maxnreg__(200)
             ok = __all_sync(0xffffffffu, mbar_wait(&sm.s_full[t], j & 1, ab));
             if (!ok) break;
             tc_fence_after_sync();
-            uint32_t s0[32], s1[32], s2[32], s3[32];
-            tmem_ld32(ts + 0, s0);
-            tmem_ld32(ts + 32, s1);
-            tmem_ld32(ts + 64, s2);
-            tmem_ld32(ts + 96, s3);
-            tmem_ld_wait(s0);
-            reg_fence32(s1);
-            reg_fence32(s2);
-            reg_fence32(s3);
 
             // In-tile mask: only tiles that reach past the padding length or
-            // the diagonal need it (tile-uniform branch).
+            // the diagonal need it (tile-uniform branch).  Keys with index
+            // >= row_lim get -inf, i.e. weight exactly zero.
             const int k0 = j * BN;
             const bool need_mask =
                 (k0 + BN > kv_len) || (causal && k0 + BN - 1 > tile_row_lo);
-            if (need_mask) {
-                const int lim = row_lim - k0;
-#pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    if (c >= lim) s0[c] = f2u(-INFINITY);
-                    if (c + 32 >= lim) s1[c] = f2u(-INFINITY);
-                    if (c + 64 >= lim) s2[c] = f2u(-INFINITY);
-                    if (c + 96 >= lim) s3[c] = f2u(-INFINITY);
-                }
-            }
+            const int lim = row_lim - k0;
+
+            // Pass 1: row maximum over the 128 scores, read as two halves.
             float mx = -INFINITY;
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+                uint32_t a[32], b2[32];
+                tmem_ld32(ts + half * 64, a);
+                tmem_ld32(ts + half * 64 + 32, b2);
+                tmem_ld_wait(a);
+                reg_fence32(b2);
+                if (need_mask) {
 #pragma unroll
-            for (int c = 0; c < 32; ++c)
-                mx = fmaxf(fmaxf(mx, fmaxf(u2f(s0[c]), u2f(s1[c]))), fmaxf(u2f(s2[c]), u2f(s3[c])));
+                    for (int c = 0; c < 32; ++c) {
+                        if (half * 64 + c >= lim) a[c] = f2u(-INFINITY);
+                        if (half * 64 + 32 + c >= lim) b2[c] = f2u(-INFINITY);
+                    }
+                }
+#pragma unroll
+                for (int c = 0; c < 32; ++c) mx = fmaxf(mx, fmaxf(u2f(a[c]), u2f(b2[c])));
+            }
 
             // Running maximum: keep the stale one unless it grew by > 2^8.
+            // The decision is per row, so a row's result never depends on
+            // another row's scores; the warp only shares the tensor-memory
+            // access (rows that keep their maximum scale O by exactly 1).
             const float m_new = fmaxf(m_run, mx);
-            bool rescale = false;
+            const bool grow = j > 0 && (m_new - m_run) * C > kRescaleThreshold;
+            const bool rescale = __any_sync(0xffffffffu, grow);
             float alpha = 1.f;
             if (j == 0) {
                 m_run = m_new;
-            } else if (__any_sync(0xffffffffu, (m_new - m_run) * C > kRescaleThreshold)) {
-                rescale = true;
+            } else if (grow) {
                 alpha = ex2_approx((m_run - m_new) * C);
                 l_run *= alpha;
                 m_run = m_new;
             }
             const float mc = m_run * C;
+
+            // Pass 2: P = 2^(s*c - m*c) in bf16, written over the scores: half
+            // h reads score columns [64h, 64h+64) and writes P columns
+            // [32h, 32h+32) (column c holds keys 2c and 2c+1), which only
+            // overwrites scores already consumed.
             float sum0 = 0.f, sum1 = 0.f;
-            {
-                uint32_t pa[32];
+#pragma unroll 1
+            for (int half = 0; half < 2; ++half) {
+                uint32_t a[32], b2[32];
+                tmem_ld32(ts + half * 64, a);
+                tmem_ld32(ts + half * 64 + 32, b2);
+                tmem_ld_wait(a);
+                reg_fence32(b2);
+                if (need_mask) {
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        if (half * 64 + c >= lim) a[c] = f2u(-INFINITY);
+                        if (half * 64 + 32 + c >= lim) b2[c] = f2u(-INFINITY);
+                    }
+                }
+                uint32_t pk[32];
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
-                    const float e0 = ex2_approx(fmaf(u2f(s0[2 * c]), C, -mc));
-                    const float e1 = ex2_approx(fmaf(u2f(s0[2 * c + 1]), C, -mc));
-                    const float e2 = ex2_approx(fmaf(u2f(s1[2 * c]), C, -mc));
-                    const float e3 = ex2_approx(fmaf(u2f(s1[2 * c + 1]), C, -mc));
+                    const float e0 = ex2_approx(fmaf(u2f(a[2 * c]), C, -mc));
+                    const float e1 = ex2_approx(fmaf(u2f(a[2 * c + 1]), C, -mc));
+                    const float e2 = ex2_approx(fmaf(u2f(b2[2 * c]), C, -mc));
+                    const float e3 = ex2_approx(fmaf(u2f(b2[2 * c + 1]), C, -mc));
                     sum0 += e0 + e1;
                     sum1 += e2 + e3;
-                    pa[c] = pack_bf16x2(e0, e1);
-                    pa[c + 16] = pack_bf16x2(e2, e3);
+                    pk[c] = pack_bf16x2(e0, e1);
+                    pk[c + 16] = pack_bf16x2(e2, e3);
                 }
-                // P_t over the first 64 columns of S_t: column c holds keys 2c, 2c+1.
-                tmem_st32(ts + 0, pa);
-            }
-            {
-                uint32_t pb[32];
-#pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const float e0 = ex2_approx(fmaf(u2f(s2[2 * c]), C, -mc));
-                    const float e1 = ex2_approx(fmaf(u2f(s2[2 * c + 1]), C, -mc));
-                    const float e2 = ex2_approx(fmaf(u2f(s3[2 * c]), C, -mc));
-                    const float e3 = ex2_approx(fmaf(u2f(s3[2 * c + 1]), C, -mc));
-                    sum0 += e0 + e1;
-                    sum1 += e2 + e3;
-                    pb[c] = pack_bf16x2(e0, e1);
-                    pb[c + 16] = pack_bf16x2(e2, e3);
-                }
-                tmem_st32(ts + 32, pb);
+                tmem_st32(ts + half * 32, pk);
             }
             l_run += sum0 + sum1;
             if (rescale) {
