@@ -274,6 +274,20 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> int:
 
     # End to end through the public API with host buffers: pinned host Q/K/V
     # -> device, attention, output -> pinned host, every step.
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, q, k, v, out, w, stream, dev, dist, flops, world)
+
+    if rank == 0:
+        emit(args, w, x, ms, ms_mean, value, flops, world, clocks, e2e)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, q, k, v, out, w, stream, dev, dist, flops, world):
+    import torch
+    import transformer_scaled_dot_softmax_gb300 as tsds
     hq, hk, hv = (t.cpu().pin_memory() for t in (q, k, v))
     hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     e2e_steps = max(3, min(args.steps, 20))
@@ -300,42 +314,41 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> int:
     e2e_value = whole_job_value(flops, world, e2e_ms)
     h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv))
     d2h = hout.numel() * hout.element_size()
+    return {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
-    if rank == 0:
-        peaks, peak_src = load_peaks()
-        peak = float(peaks["bf16_tflops"])
-        achieved = flops / (float(ms.mean()) * 1e-3) / 1e12
-        cpu = None
-        if world == 1 and not args.no_cpu_baseline:
-            cv, cdt, cn, cores = time_oracle(x, w, args.oracle_stride)
-            cpu = {"value": cv, "unit": UNIT, "cores": cores, "kind": "oracle",
-                   "sample": "all %d (batch, head) pairs x every %d-th query row of the causal "
-                             "T=8192 triangle (%d rows, %.1f s), fp64"
-                             % (w.B * w.h, args.oracle_stride, cn, cdt)}
-        line = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_mean,
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic", "config": workload_config(w),
-            "pct_of_dense_bf16_peak": {
-                "measured_%.1f" % peak: 100.0 * achieved / peak,
-                "nominal_%.0f" % NOMINAL_BF16_TFLOPS: 100.0 * achieved / NOMINAL_BF16_TFLOPS,
-                "datasheet_%.0f" % DATASHEET_BF16_TFLOPS: 100.0 * achieved / DATASHEET_BF16_TFLOPS},
-            "roofline": {"kernel": "attn_fwd_bf16_kernel", "bound": "tensor",
-                         "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "peak_source": peak_src + " burst bf16",
-                         "flops_per_launch": flops, "traffic": measured_traffic()},
-            "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-            "gpu_launches": args.steps,
-            "clocks": clocks.summary(),
-            "ms_min": float(ms.min()), "ms_median": float(np.median(ms)),
-        }
-        print(json.dumps(line), flush=True)
-    if dist is not None:
-        dist.destroy_process_group()
-    return 0
+
+def emit(args, w, x, ms, ms_mean, value, flops, world, clocks, e2e):
+    peaks, peak_src = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    achieved = flops / (float(ms.mean()) * 1e-3) / 1e12
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cv, cdt, cn, cores = time_oracle(x, w, args.oracle_stride)
+        cpu = {"value": cv, "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": "all %d (batch, head) pairs x every %d-th query row of the causal "
+                         "T=8192 triangle (%d rows, %.1f s), fp64"
+                         % (w.B * w.h, args.oracle_stride, cn, cdt)}
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_mean,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": workload_config(w),
+        "pct_of_dense_bf16_peak": {
+            "measured_%.1f" % peak: 100.0 * achieved / peak,
+            "nominal_%.0f" % NOMINAL_BF16_TFLOPS: 100.0 * achieved / NOMINAL_BF16_TFLOPS,
+            "datasheet_%.0f" % DATASHEET_BF16_TFLOPS: 100.0 * achieved / DATASHEET_BF16_TFLOPS},
+        "roofline": {"kernel": "attn_fwd_bf16_kernel", "bound": "tensor",
+                     "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "peak_source": peak_src + " burst bf16",
+                     "flops_per_launch": flops, "traffic": measured_traffic()},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clocks.summary(),
+        "ms_min": float(ms.min()), "ms_median": float(np.median(ms)),
+    }
+    print(json.dumps(line), flush=True)
 
 
 def parse(argv=None):
@@ -347,6 +360,10 @@ def parse(argv=None):
     ap.add_argument("--oracle-stride", type=int, default=1,
                     help="CPU baseline: time every n-th query row of every head")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--shape", default=None,
+                    help="B,h,T override of the causal workload (profiling and sweeps only; "
+                         "the reported line then names the changed workload)")
     return ap.parse_args(argv)
 
 
@@ -359,6 +376,11 @@ def main(argv=None) -> int:
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if world != args.gpus and world != 1:
         raise SystemExit("--gpus %d does not match WORLD_SIZE %d" % (args.gpus, world))
+    global WORKLOAD
+    if args.shape:
+        B, h, T = (int(v) for v in args.shape.split(","))
+        WORKLOAD = WORKLOAD.replace(B=B, h=h, T_q=T, T_k=T,
+                                    name="sdpa_causal_bf16_B%d_h%d_T%d_d64" % (B, h, T))
     if args.impl == "reference":
         return run_reference(args, rank, world)
     return run_gpu(args, rank, world, local_rank)
