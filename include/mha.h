@@ -126,6 +126,39 @@ mha_status mha_forward(mha_dtype dt, const void *x_q, const void *x_kv, const vo
                        int d_model, int d_k, int d_v, float scale, mha_mask mask,
                        const int32_t *key_lens, int *status_dev, cudaStream_t stream);
 
+/*
+ * Multi-head attention forward exactly as mha_forward, but with no workspace
+ * argument: the scratch lives in a device array inside the library, so the
+ * call allocates nothing.  (The pages have no counterpart: this is a
+ * deployment convenience, not part of the method.)
+ *
+ * For callers that cannot call cudaMalloc or reach any device allocator --
+ * for example a plugin hosted by a framework that owns all device memory and
+ * exposes no allocation hook, or a serving loop whose memory plan forbids
+ * allocation after start-up.
+ *
+ * Limit: the problem's mha_workspace_bytes(B, h, T_q, T_k, d_k, d_v) must not
+ * exceed MHA_STATIC_WORKSPACE_BYTES (32 MiB); larger problems return
+ * MHA_ERR_WORKSPACE and launch nothing.  Every GPU that loads the library
+ * holds those 32 MiB until the process exits.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that
+ * first call before any stream capture.  A failure there returns
+ * MHA_ERR_CUDA.  All calls on a device share the one array and it keeps the
+ * previous call's contents (every byte read is written earlier in the same
+ * call, so nothing needs clearing): calls that overlap on the GPU -- on
+ * different streams, or from different host threads -- race on it and must
+ * be serialised by the caller.  Other arguments and errors as mha_forward.
+ */
+#define MHA_STATIC_WORKSPACE_BYTES (32u << 20)
+mha_status mha_forward_static_workspace(mha_dtype dt, const void *x_q, const void *x_kv,
+                                        const void *w_q, const void *w_k, const void *w_v,
+                                        const void *w_o, void *out, int B, int h, int T_q,
+                                        int T_k, int d_model, int d_k, int d_v, float scale,
+                                        mha_mask mask, const int32_t *key_lens,
+                                        int *status_dev, cudaStream_t stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char *mha_status_string(mha_status status);
 

@@ -13,6 +13,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libmha.so")
 MHA_OK, MHA_ERR_INVALID_ARG, MHA_ERR_UNSUPPORTED, MHA_ERR_WORKSPACE = 0, 1, 2, 3
 MHA_ERR_MISALIGNED, MHA_ERR_CUDA, MHA_ERR_TIMEOUT = 4, 5, 6
 MHA_F32, MHA_BF16 = 0, 1
+MHA_STATIC_WORKSPACE_BYTES = 32 << 20
 MHA_MASK_NONE, MHA_MASK_CAUSAL, MHA_MASK_KEY_PADDING, MHA_MASK_CAUSAL_KEY_PADDING = 0, 1, 2, 3
 
 # Every symbol include/mha.h declares, with its ctypes signature.
@@ -23,6 +24,8 @@ SIGNATURES = {
     "mha_workspace_bytes": (_sz, [_ci, _ci, _ci, _ci, _ci, _ci]),
     "mha_forward": (_ci, [_ci, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _ci, _ci, _ci, _ci,
                           _ci, _ci, _ci, _cf, _ci, _vp, _vp, _vp]),
+    "mha_forward_static_workspace": (_ci, [_ci, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci,
+                                           _ci, _ci, _ci, _ci, _cf, _ci, _vp, _vp, _vp]),
     "mha_status_string": (ctypes.c_char_p, [_ci]),
     "mha_last_error": (ctypes.c_char_p, []),
 }
