@@ -11,7 +11,8 @@
 // One CTA owns 256 query rows of one (b, h) as two 128-row tiles Q0, Q1 and
 // streams the visible K/V tiles through shared memory:
 //
-//   warp 8      TMA producer: Q0, Q1 once; K_j, V_j into a 3-stage ring.
+//   warp 8      TMA producer: Q0, Q1 once; K_j and V_j together into a
+//               4-stage ring (one barrier per stage for both tiles).
 //   warp 9      MMA issuer (one thread): S_t = Q_t K_j^T and O_t += P_t V_j
 //               on the tensor cores (tcgen05.mma kind::f16, fp32 accumulators
 //               in tensor memory).  P_t is read straight from tensor memory.
@@ -23,17 +24,28 @@
 //               updates m and l, writes P = bf16(2^(s*c - m*c)) back over its
 //               scores, and finally normalises O by 1/l and stores it.
 //
-// The MMA warp issues PV_0(j), S_0(j+1), PV_1(j), S_1(j+1), ... so that while
-// one softmax warpgroup works on its tile the tensor cores run the other
-// group's two products (ping-pong).  A tcgen05.commit arrives once every
-// earlier MMA of the issuing thread has completed, so "S_t(j+1) is full"
-// also means "PV_t(j) is done": the softmax group may then rescale O_t in
-// tensor memory without another barrier.  O_t is only rescaled when the row
-// maximum has grown by more than 2^8 (otherwise the stale maximum is kept;
-// the probabilities then stay below 256, exact in fp32 and fine in bf16).
+// Score tiles rotate through three tensor-memory buffers (S_t(j) uses buffer
+// (2j + t) mod 3), so the MMA warp can compute the next score tile of a
+// query tile before the current P.V product of that tile has been issued:
+// it issues S_0(j+1), PV_0(j), S_1(j+1), PV_1(j), ...  While one softmax
+// group works on S_t(j+1) the tensor cores still hold PV_t(j), S_u(j+1),
+// PV_u(j) and S_t(j+2) of queued work.  Every M=128 MMA costs at least ~64
+// cycles whatever its N, so PV (N = 64) runs at half rate; the queue depth is
+// what keeps the pipe busy.
 //
-// Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 [256,320),
-// O1 [320,384).  P_t (bf16 pairs) overwrites the first 64 columns of S_t.
+// Handshakes are per score buffer: "S in buffer b is ready" and "P in buffer
+// b is ready".  A buffer's next use needs the MMA warp to have consumed the
+// current one, so neither barrier can run two phases ahead of its waiter.
+//
+// The running maximum is rescaled in O_t only when it grows by more than 2^8
+// (otherwise the stale maximum is kept; the probabilities then stay below
+// 256, exact in fp32 and fine in bf16), decided per row.  A rescale at tile j
+// needs PV_t(j-1) complete: it waits for the release of tile j-1's K/V stage,
+// which is committed after both products of that tile.
+//
+// Tensor memory (512 columns): S buffers [0,128), [128,256), [256,384);
+// O0 [384,448), O1 [448,512).  P overwrites the first 64 columns of its S
+// buffer.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -46,27 +58,33 @@ constexpr int BM = 128;        // query rows per tile
 constexpr int BN = 128;        // keys per tile
 constexpr int HD = kAttnHeadDim;
 constexpr int NQ = 2;          // query tiles per CTA
-constexpr int STAGES = 3;      // K/V ring depth
+constexpr int STAGES = 4;      // K/V ring depth
 constexpr int kThreads = 320;  // 8 softmax warps + load warp + MMA warp
 constexpr int kLoadWarp = 8;
 constexpr int kMmaWarp = 9;
 constexpr uint32_t kTileBytes = BM * HD * 2;  // 16 KiB, one 128 x 64 bf16 tile
 constexpr uint32_t kTmemCols = 512;
+constexpr int kSBufs = 3;                    // score buffers in tensor memory
 constexpr float kRescaleThreshold = 8.0f;    // log2 units
 
-__device__ __forceinline__ uint32_t s_col(int t) { return t == 0 ? 0u : 128u; }
-__device__ __forceinline__ uint32_t o_col(int t) { return t == 0 ? 256u : 320u; }
+// Score slots are numbered in issue order over the (tile j, query tile t)
+// pairs that exist (query tile t has n_t key tiles): slot u uses buffer
+// u mod 3 (128 columns each) for the (u / 3)-th time.
+__device__ __forceinline__ int score_slot(int j, int t, int n0, int n1) {
+    return min(j, n0) + min(j, n1) + ((t == 1 && j < n0) ? 1 : 0);
+}
+__device__ __forceinline__ uint32_t s_col(int u) { return 128u * static_cast<uint32_t>(u % kSBufs); }
+__device__ __forceinline__ uint32_t o_col(int t) { return 384u + 64u * static_cast<uint32_t>(t); }
 
 struct __align__(1024) SmemAttn {
     uint8_t q[NQ][kTileBytes];
     uint8_t k[STAGES][kTileBytes];
     uint8_t v[STAGES][kTileBytes];
     uint64_t q_full;
-    uint64_t k_full[STAGES];
-    uint64_t v_full[STAGES];
+    uint64_t kv_full[STAGES];
     uint64_t kv_empty[STAGES];
-    uint64_t s_full[NQ];
-    uint64_t p_full[NQ];
+    uint64_t s_full[kSBufs];
+    uint64_t p_full[kSBufs];
     uint64_t o_final[NQ];
     uint64_t drain;
     uint32_t tmem_base;
@@ -110,15 +128,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         mbar_init(&sm.q_full, 1);
         for (int i = 0; i < STAGES; ++i) {
-            mbar_init(&sm.k_full[i], 1);
-            mbar_init(&sm.v_full[i], 1);
+            mbar_init(&sm.kv_full[i], 1);
             mbar_init(&sm.kv_empty[i], 1);
         }
-        for (int t = 0; t < NQ; ++t) {
-            mbar_init(&sm.s_full[t], 1);
-            mbar_init(&sm.p_full[t], BM);
-            mbar_init(&sm.o_final[t], 1);
+        for (int b = 0; b < kSBufs; ++b) {
+            mbar_init(&sm.s_full[b], 1);
+            mbar_init(&sm.p_full[b], BM / 32);  // one arrival per softmax warp
         }
+        for (int t = 0; t < NQ; ++t) mbar_init(&sm.o_final[t], 1);
         mbar_init(&sm.drain, 1);
         sm.abort_flag = 0;
         fence_barrier_init();
@@ -147,20 +164,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < n_kv; ++j) {
                 const int st = j % STAGES;
                 if (j >= STAGES && !mbar_wait(&sm.kv_empty[st], ((j / STAGES) - 1) & 1, ab)) break;
-                mbar_arrive_expect_tx(&sm.k_full[st], kTileBytes);
-                tma_load_3d(&tmap_k, &sm.k_full[st], sm.k[st], 0, j * BN, bh);
-                mbar_arrive_expect_tx(&sm.v_full[st], kTileBytes);
-                tma_load_3d(&tmap_v, &sm.v_full[st], sm.v[st], 0, j * BN, bh);
+                mbar_arrive_expect_tx(&sm.kv_full[st], 2 * kTileBytes);
+                tma_load_3d(&tmap_k, &sm.kv_full[st], sm.k[st], 0, j * BN, bh);
+                tma_load_3d(&tmap_v, &sm.kv_full[st], sm.v[st], 0, j * BN, bh);
                 issued = j + 1;
             }
-            if (sm.abort_flag) {
-                // Let every copy still in flight land before the CTA exits.
-                mbar_wait_drain(&sm.q_full, 0);
-                for (int j = max(0, issued - STAGES); j < issued; ++j) {
-                    mbar_wait_drain(&sm.k_full[j % STAGES], (j / STAGES) & 1);
-                    mbar_wait_drain(&sm.v_full[j % STAGES], (j / STAGES) & 1);
-                }
-            }
+            // Let every copy still in flight land before the CTA exits (on the
+            // normal path these phases completed long ago).
+            mbar_wait_drain(&sm.q_full, 0);
+            for (int j = max(0, issued - STAGES); j < issued; ++j)
+                mbar_wait_drain(&sm.kv_full[j % STAGES], (j / STAGES) & 1);
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------- MMA issuer
@@ -168,63 +181,91 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, false, false);
             constexpr uint32_t idesc_o = idesc_bf16_f32(BM, HD, false, true);
             const int n0 = n_tiles[0], n1 = n_tiles[1];
-            // S_t = Q_t K^T: A = Q_t (K-major), B = K tile (K-major), K dim 64 = 4 x 16.
-            auto issue_s = [&](int t, int st) {
-                const uint32_t qa = smem_u32(sm.q[t]);
-                const uint32_t ka = smem_u32(sm.k[st]);
+            // Shared-memory descriptors, built once.  Tiles of one kind are
+            // contiguous, so stage st adds st * 16 KiB (>> 4 = 1024) to the
+            // start-address field; a K step of 16 adds 32 bytes (2) within a
+            // K-major row and 16 V rows (2 KiB, 128) for the MN-major V tile.
+            const uint64_t q_desc0 = smem_desc_sw128(smem_u32(sm.q[0]), 16, 1024);
+            const uint64_t k_desc0 = smem_desc_sw128(smem_u32(sm.k[0]), 16, 1024);
+            const uint64_t v_desc0 = smem_desc_sw128(smem_u32(sm.v[0]), 1024, 1024);
+            constexpr uint64_t kTileDesc = kTileBytes >> 4;
+
+            // One group per query tile t: S_t(j_s) (if has_s) and PV_t(j_pv)
+            // (if has_pv), interleaved so the PV chain (one accumulator) and
+            // the S chain overlap in the tensor pipe.  The group opens with
+            // two PV MMAs: the S it carries overwrites a buffer the previous
+            // group's PV read, and the gap keeps that reuse off the critical
+            // path.  The S-ready commit follows the last S MMA (it also
+            // covers the PV MMAs issued before it).
+            auto issue_group = [&](int t, bool has_s, int st_s, int j_s, bool has_pv, int st_pv,
+                                   int j_pv) {
+                const int us = has_s ? score_slot(j_s, t, n0, n1) : 0;
+                const int up = has_pv ? score_slot(j_pv, t, n0, n1) : 0;
+                const uint32_t d_s = tmem + s_col(us);
+                const uint32_t a_p = tmem + s_col(up);
+                const uint32_t d_o = tmem + o_col(t);
+                const uint64_t qd = q_desc0 + static_cast<uint64_t>(t) * kTileDesc;
+                const uint64_t kd = k_desc0 + static_cast<uint64_t>(st_s) * kTileDesc;
+                const uint64_t vd = v_desc0 + static_cast<uint64_t>(st_pv) * kTileDesc;
+                const uint32_t acc0 = j_pv > 0 ? 1u : 0u;
+                // schedule: PV0 PV1 S0 PV2 S1 PV3 S2 PV4 S3 [commit] PV5 PV6 PV7
 #pragma unroll
-                for (int kk = 0; kk < HD / 16; ++kk)
-                    mma_bf16_ss(tmem + s_col(t), smem_desc_sw128(qa + kk * 32, 16, 1024),
-                                smem_desc_sw128(ka + kk * 32, 16, 1024), idesc_s, kk > 0);
-                mma_commit(&sm.s_full[t]);
+                for (int step = 0; step < 13; ++step) {
+                    constexpr int kind_tab[13] = {0, 0, 1, 0, 1, 0, 1, 0, 1, 2, 0, 0, 0};
+                    constexpr int idx_tab[13] = {0, 1, 0, 2, 1, 3, 2, 4, 3, 0, 5, 6, 7};
+                    const int kind = kind_tab[step], i = idx_tab[step];
+                    if (kind == 0 && has_pv)
+                        mma_bf16_ts(d_o, a_p + 8 * i, vd + 128 * i, idesc_o, (i > 0) ? 1u : acc0);
+                    else if (kind == 1 && has_s)
+                        mma_bf16_ss(d_s, qd + 2 * i, kd + 2 * i, idesc_s, i > 0 ? 1u : 0u);
+                    else if (kind == 2 && has_s)
+                        mma_commit(&sm.s_full[us % kSBufs]);
+                }
             };
-            // O_t (+)= P_t V: A = P_t in tensor memory (8 columns per 16 keys),
-            // B = V tile (keys x 64, MN-major: 16 keys = 2 swizzle atoms = 2 KiB).
-            auto issue_o = [&](int t, int st, int j) {
-                const uint32_t va = smem_u32(sm.v[st]);
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-                    mma_bf16_ts(tmem + o_col(t), tmem + s_col(t) + kk * 8,
-                                smem_desc_sw128(va + kk * 2048, kTileBytes, 1024), idesc_o,
-                                (j > 0 || kk > 0) ? 1u : 0u);
+            // P of query tile t, key tile j is ready.
+            auto wait_p = [&](int t, int j) {
+                const int u = score_slot(j, t, n0, n1);
+                return mbar_wait(&sm.p_full[u % kSBufs], (u / kSBufs) & 1, ab);
             };
-            bool ok = mbar_wait(&sm.q_full, 0, ab) && mbar_wait(&sm.k_full[0], 0, ab);
+            // Each wait sits right after an MMA group has been issued, so the
+            // tensor pipe has queued work while this thread polls.
+            auto wait_kv = [&](int j) {
+                return mbar_wait(&sm.kv_full[j % STAGES], (j / STAGES) & 1, ab);
+            };
+            bool ok = mbar_wait(&sm.q_full, 0, ab) && wait_kv(0);
             if (ok) {
                 tc_fence_after_sync();
-                if (n0 > 0) issue_s(0, 0);
-                if (n1 > 0) issue_s(1, 0);
+                if (n0 > 0) issue_group(0, true, 0, 0, false, 0, 0);
+                if (n1 > 0) issue_group(1, true, 0, 0, false, 0, 0);
+                if (n_kv > 1) ok = wait_kv(1);
             }
             for (int j = 0; ok && j < n_kv; ++j) {
                 const int st = j % STAGES;
-                const bool has_next = j + 1 < n_kv;
                 const int st1 = (j + 1) % STAGES;
-                if (!(ok = mbar_wait(&sm.v_full[st], (j / STAGES) & 1, ab))) break;
-                if (j < n0) {
-                    if (!(ok = mbar_wait(&sm.p_full[0], j & 1, ab))) break;
-                    tc_fence_after_sync();
-                    issue_o(0, st, j);
-                    if (j == n0 - 1) mma_commit(&sm.o_final[0]);
-                }
-                if (has_next) {
-                    if (!(ok = mbar_wait(&sm.k_full[st1], ((j + 1) / STAGES) & 1, ab))) break;
-                    tc_fence_after_sync();
-                    if (j + 1 < n0) issue_s(0, st1);
-                }
-                if (j < n1) {
-                    if (!(ok = mbar_wait(&sm.p_full[1], j & 1, ab))) break;
-                    tc_fence_after_sync();
-                    issue_o(1, st, j);
-                    if (j == n1 - 1) mma_commit(&sm.o_final[1]);
-                }
+                const bool next0 = j + 1 < n0, next1 = j + 1 < n1;
+                const bool pv0 = j < n0, pv1 = j < n1;
+                // K/V of tiles j and j+1 are resident (waited one group ago).
+                // Tile 0: S_0(j+1) looks ahead into the buffer PV_1(j-1) has
+                // already consumed; PV_0(j) needs P_0(j).
+                if (pv0 && !(ok = wait_p(0, j))) break;
+                tc_fence_after_sync();
+                issue_group(0, next0, st1, j + 1, pv0, st, j);
+                if (pv0 && j == n0 - 1) mma_commit(&sm.o_final[0]);
+                // Tile 1: S_1(j+1) reuses the buffer of P_0(j), read by the
+                // group just issued (tensor-core operations of one thread run
+                // in order).
+                if (pv1 && !(ok = wait_p(1, j))) break;
+                tc_fence_after_sync();
+                issue_group(1, next1, st1, j + 1, pv1, st, j);
+                if (pv1 && j == n1 - 1) mma_commit(&sm.o_final[1]);
                 mma_commit(&sm.kv_empty[st]);
-                if (has_next && j + 1 < n1) issue_s(1, st1);
+                if (j + 2 < n_kv && !(ok = wait_kv(j + 2))) break;
             }
-            if (!ok) {
-                // Wait (bounded) for the MMAs already issued before tensor
-                // memory is released.
-                mma_commit(&sm.drain);
-                mbar_wait_drain(&sm.drain, 0);
-            }
+            // Always wait (time-bounded, whatever the abort state) until every
+            // MMA this thread issued has completed: tensor memory is released
+            // and the CTA exits only after that.
+            mma_commit(&sm.drain);
+            mbar_wait_drain(&sm.drain, 0);
         }
     } else {
         // --------------------------------------------------------- softmax
@@ -232,8 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = static_cast<uint32_t>(warp & 3) * 32;
         const int r = static_cast<int>(lane_base) + lane;  // row in tile = TMEM lane
         const int row = q0 + t * BM + r;                   // query index
-        const uint32_t ts = tmem_addr(tmem, lane_base, s_col(t));
-        const uint32_t to = tmem_addr(tmem, lane_base, o_col(t));
+        const uint32_t tl = tmem_addr(tmem, lane_base, 0);
+        const uint32_t to = tl + o_col(t);
         const int nt = t == 0 ? n_tiles[0] : n_tiles[1];
         const float C = p.scale_log2;
         const int row_lim = causal ? min(kv_len, row + 1) : kv_len;  // keys < row_lim visible
@@ -243,43 +284,66 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
 
         for (int j = 0; j < nt; ++j) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&sm.s_full[t], j & 1, ab));
+            const int u = score_slot(j, t, n_tiles[0], n_tiles[1]);
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(&sm.s_full[u % kSBufs], (u / kSBufs) & 1, ab));
             if (!ok) break;
             tc_fence_after_sync();
+            const uint32_t ts = tl + s_col(u);
+            uint32_t s0[32], s1[32], s2[32], s3[32];
+            tmem_ld32(ts + 0, s0);
+            tmem_ld32(ts + 32, s1);
+            tmem_ld32(ts + 64, s2);
+            tmem_ld32(ts + 96, s3);
+            tmem_ld_wait(s0);
+            reg_fence32(s1);
+            reg_fence32(s2);
+            reg_fence32(s3);
 
             // In-tile mask: only tiles that reach past the padding length or
             // the diagonal need it (tile-uniform branch).  Keys with index
             // >= row_lim get -inf, i.e. weight exactly zero.
             const int k0 = j * BN;
-            const bool need_mask =
-                (k0 + BN > kv_len) || (causal && k0 + BN - 1 > tile_row_lo);
-            const int lim = row_lim - k0;
-
-            // Pass 1: row maximum over the 128 scores, read as two halves.
-            float mx = -INFINITY;
-#pragma unroll 1
-            for (int half = 0; half < 2; ++half) {
-                uint32_t a[32], b2[32];
-                tmem_ld32(ts + half * 64, a);
-                tmem_ld32(ts + half * 64 + 32, b2);
-                tmem_ld_wait(a);
-                reg_fence32(b2);
-                if (need_mask) {
+            if ((k0 + BN > kv_len) || (causal && k0 + BN - 1 > tile_row_lo)) {
+                const int lim = row_lim - k0;
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        if (half * 64 + c >= lim) a[c] = f2u(-INFINITY);
-                        if (half * 64 + 32 + c >= lim) b2[c] = f2u(-INFINITY);
-                    }
+                for (int c = 0; c < 32; ++c) {
+                    if (c >= lim) s0[c] = f2u(-INFINITY);
+                    if (c + 32 >= lim) s1[c] = f2u(-INFINITY);
+                    if (c + 64 >= lim) s2[c] = f2u(-INFINITY);
+                    if (c + 96 >= lim) s3[c] = f2u(-INFINITY);
                 }
-#pragma unroll
-                for (int c = 0; c < 32; ++c) mx = fmaxf(mx, fmaxf(u2f(a[c]), u2f(b2[c])));
             }
+
+            // Row maximum of the tile: eight independent chains of three-input
+            // maxima, then a small tree.
+            float tm[8];
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                tm[i] = fmaxf(u2f(s0[i]), u2f(s0[i + 2]));
+                tm[2 + i] = fmaxf(u2f(s1[i]), u2f(s1[i + 2]));
+                tm[4 + i] = fmaxf(u2f(s2[i]), u2f(s2[i + 2]));
+                tm[6 + i] = fmaxf(u2f(s3[i]), u2f(s3[i + 2]));
+            }
+#pragma unroll
+            for (int c = 4; c < 32; c += 4) {
+#pragma unroll
+                for (int i = 0; i < 2; ++i) {
+                    tm[i] = fmax3(tm[i], u2f(s0[c + i]), u2f(s0[c + i + 2]));
+                    tm[2 + i] = fmax3(tm[2 + i], u2f(s1[c + i]), u2f(s1[c + i + 2]));
+                    tm[4 + i] = fmax3(tm[4 + i], u2f(s2[c + i]), u2f(s2[c + i + 2]));
+                    tm[6 + i] = fmax3(tm[6 + i], u2f(s3[c + i]), u2f(s3[c + i + 2]));
+                }
+            }
+            tm[0] = fmax3(tm[0], tm[1], tm[2]);
+            tm[3] = fmax3(tm[3], tm[4], tm[5]);
+            tm[0] = fmax3(tm[0], tm[3], fmaxf(tm[6], tm[7]));
 
             // Running maximum: keep the stale one unless it grew by > 2^8.
             // The decision is per row, so a row's result never depends on
             // another row's scores; the warp only shares the tensor-memory
             // access (rows that keep their maximum scale O by exactly 1).
-            const float m_new = fmaxf(m_run, mx);
+            const float m_new = fmaxf(m_run, tm[0]);
             const bool grow = j > 0 && (m_new - m_run) * C > kRescaleThreshold;
             const bool rescale = __any_sync(0xffffffffu, grow);
             float alpha = 1.f;
@@ -292,43 +356,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             const float mc = m_run * C;
 
-            // Pass 2: P = 2^(s*c - m*c) in bf16, written over the scores: half
-            // h reads score columns [64h, 64h+64) and writes P columns
-            // [32h, 32h+32) (column c holds keys 2c and 2c+1), which only
-            // overwrites scores already consumed.
-            float sum0 = 0.f, sum1 = 0.f;
-#pragma unroll 1
-            for (int half = 0; half < 2; ++half) {
-                uint32_t a[32], b2[32];
-                tmem_ld32(ts + half * 64, a);
-                tmem_ld32(ts + half * 64 + 32, b2);
-                tmem_ld_wait(a);
-                reg_fence32(b2);
-                if (need_mask) {
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        if (half * 64 + c >= lim) a[c] = f2u(-INFINITY);
-                        if (half * 64 + 32 + c >= lim) b2[c] = f2u(-INFINITY);
-                    }
-                }
-                uint32_t pk[32];
-#pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const float e0 = ex2_approx(fmaf(u2f(a[2 * c]), C, -mc));
-                    const float e1 = ex2_approx(fmaf(u2f(a[2 * c + 1]), C, -mc));
-                    const float e2 = ex2_approx(fmaf(u2f(b2[2 * c]), C, -mc));
-                    const float e3 = ex2_approx(fmaf(u2f(b2[2 * c + 1]), C, -mc));
-                    sum0 += e0 + e1;
-                    sum1 += e2 + e3;
-                    pk[c] = pack_bf16x2(e0, e1);
-                    pk[c + 16] = pack_bf16x2(e2, e3);
-                }
-                tmem_st32(ts + half * 32, pk);
+            // P = 2^(s*c - m*c) in bf16 over the first 64 columns of the
+            // buffer (column c holds keys 2c, 2c+1; chunk q of 32 scores
+            // becomes P columns [16q, 16q+16), all already read).
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#define MHA_EXP_CHUNK(SRC, COL)                                               \
+            {                                                                 \
+                uint32_t pk[16];                                              \
+                _Pragma("unroll") for (int c = 0; c < 16; ++c) {              \
+                    const float e0 = ex2_approx(fmaf(u2f(SRC[2 * c]), C, -mc));     \
+                    const float e1 = ex2_approx(fmaf(u2f(SRC[2 * c + 1]), C, -mc)); \
+                    acc[(2 * c) & 7] += e0;                                   \
+                    acc[(2 * c + 1) & 7] += e1;                               \
+                    pk[c] = pack_bf16x2(e0, e1);                              \
+                }                                                             \
+                tmem_st16(ts + (COL), pk);                                    \
             }
-            l_run += sum0 + sum1;
+            MHA_EXP_CHUNK(s0, 0)
+            MHA_EXP_CHUNK(s1, 16)
+            MHA_EXP_CHUNK(s2, 32)
+            MHA_EXP_CHUNK(s3, 48)
+#undef MHA_EXP_CHUNK
+            l_run += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+
             if (rescale) {
-                // O_t holds sum_{j' < j} P V; all those MMAs are complete
-                // (the commit that signalled S_t(j) covers them).
+                // O_t must hold exactly sum_{j' < j} P V: wait for the
+                // release of tile j-1's stage (committed after PV_0(j-1) and
+                // PV_1(j-1)).  Its next release needs P_t(j), which this
+                // thread has not yet published, so the parity cannot alias.
+                ok = __all_sync(0xffffffffu, mbar_wait(&sm.kv_empty[(j - 1) % STAGES],
+                                                       ((j - 1) / STAGES) & 1, ab));
+                if (!ok) {
+                    tmem_st_wait();  // no tensor-memory store may outlive the CTA
+                    break;
+                }
+                tc_fence_after_sync();
                 uint32_t o0[32], o1[32];
                 tmem_ld32(to, o0);
                 tmem_ld32(to + 32, o1);
@@ -344,7 +406,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tmem_st_wait();
             tc_fence_before_sync();
-            mbar_arrive(&sm.p_full[t]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.p_full[u % kSBufs]);
         }
 
         // ----------------------------------------------------------- epilogue

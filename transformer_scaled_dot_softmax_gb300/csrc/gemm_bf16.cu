@@ -102,10 +102,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_3d(tb, &sm.full[st], sm.b[st], 0, kb * BK, tn * (BN / 64));
                 issued = kb + 1;
             }
-            if (sm.abort_flag) {
-                for (int kb = max(0, issued - STAGES); kb < issued; ++kb)
-                    mbar_wait_drain(&sm.full[kb % STAGES], (kb / STAGES) & 1);
-            }
+            // Let every copy still in flight land before the CTA exits.
+            for (int kb = max(0, issued - STAGES); kb < issued; ++kb)
+                mbar_wait_drain(&sm.full[kb % STAGES], (kb / STAGES) & 1);
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -124,12 +123,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 (kb > 0 || kk > 0) ? 1u : 0u);
                 mma_commit(&sm.empty[st]);
             }
-            if (ok) {
-                mma_commit(&sm.acc_full);
-            } else {
-                mma_commit(&sm.drain);
-                mbar_wait_drain(&sm.drain, 0);
-            }
+            if (ok) mma_commit(&sm.acc_full);
+            // Always wait (time-bounded, whatever the abort state) until every
+            // MMA this thread issued has completed before tensor memory is
+            // released.
+            mma_commit(&sm.drain);
+            mbar_wait_drain(&sm.drain, 0);
         }
     } else {
         // Epilogue: warp w reads tensor-memory lanes 32*(w%4) .. +31.

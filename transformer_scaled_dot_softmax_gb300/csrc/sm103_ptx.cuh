@@ -17,6 +17,9 @@ namespace mha {
 constexpr int kStatusTimeout = 6;  // == MHA_ERR_TIMEOUT
 // A wait that has not completed after this long is treated as a hang.
 constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
+// Longest single hardware suspension inside a wait (the thread resumes as soon
+// as the phase completes; the limit only bounds how often the timer is read).
+constexpr uint32_t kSuspendNs = 20u * 1000u * 1000u;  // 20 ms
 
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -61,6 +64,22 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// As mbar_try_wait, but lets the hardware suspend the thread for up to
+// `suspend_ns` while the phase is incomplete (it resumes when the phase
+// completes), so a waiting warp does not keep polling shared memory.
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t *bar, uint32_t parity,
+                                                      uint32_t suspend_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(suspend_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Per-CTA abort state shared by all waits of one kernel instance.
 struct AbortState {
     volatile int *cta_flag;  // shared memory
@@ -81,14 +100,12 @@ __device__ __forceinline__ bool should_abort(const AbortState &ab) {
     return false;
 }
 
-// Waits for the phase with the given parity to complete.  Returns false if
-// the wait ran out (and raises the abort) or another thread aborted.
-static __device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, AbortState ab) {
-    if (mbar_try_wait(bar, parity)) return true;
+// Slow path of mbar_wait: polls with a time limit.
+static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, AbortState ab) {
     const unsigned long long t0 = global_timer_ns();
     for (uint32_t it = 1;; ++it) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((it & 31u) == 0) {
+        if (mbar_try_wait_suspend(bar, parity, kSuspendNs)) return true;
+        if ((it & 3u) == 0) {
             if (should_abort(ab)) return false;
             if (global_timer_ns() - t0 > kWaitLimitNs) {
                 raise_abort(ab);
@@ -96,6 +113,15 @@ static __device__ __noinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, Ab
             }
         }
     }
+}
+
+// Waits for the phase with the given parity to complete.  Returns false if
+// the wait ran out (and raises the abort) or another thread aborted.  The
+// common case -- the phase is already complete or completes within one
+// try_wait -- stays inline.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, const AbortState &ab) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity, ab);
 }
 
 // Drain-time wait: bounded, never raises (used while already aborting).
@@ -213,6 +239,16 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         : "memory");
 }
 
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -285,6 +321,13 @@ __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// Maximum of three fp32 values (one instruction on sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float m;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(m) : "f"(a), "f"(b), "f"(c));
+    return m;
 }
 
 // Packs two fp32 values into bf16x2 (round to nearest even): `lo` goes to
