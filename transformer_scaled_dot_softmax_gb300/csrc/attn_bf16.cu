@@ -8,44 +8,56 @@
 // sum l, rescaling the partial output when m grows), which reaches the same
 // result up to rounding order.
 //
-// One CTA owns 256 query rows of one (b, h) as two 128-row tiles Q0, Q1 and
-// streams the visible K/V tiles through shared memory:
+// One CTA owns one 128-row query tile of one (b, h) and streams the visible
+// K/V tiles through shared memory.  Warp roles:
 //
-//   warp 8      TMA producer: Q0, Q1 once; K_j and V_j together into a
-//               4-stage ring (one barrier per stage for both tiles).
-//   warp 9      MMA issuer (one thread): S_t = Q_t K_j^T and O_t += P_t V_j
-//               on the tensor cores (tcgen05.mma kind::f16, fp32 accumulators
-//               in tensor memory).  P_t is read straight from tensor memory.
-//   warps 0-3   softmax for Q0, warps 4-7 softmax for Q1: one thread per
-//               query row (= tensor-memory lane).  Each thread loads its
-//               128 scores, applies the causal / key-padding mask in-tile
-//               (masked score = -inf, i.e. exactly zero weight: aiany.app
-//               Step 10; notebook chapter "Masked Attention in the Decoder"),
-//               updates m and l, writes P = bf16(2^(s*c - m*c)) back over its
-//               scores, and finally normalises O by 1/l and stores it.
+//   warp 8      TMA producer: Q once; K_j and V_j together into a 4-stage
+//               ring (one barrier per stage for both tiles).
+//   warp 9      issues S_j = Q K_j^T (tcgen05.mma kind::f16, M=128 N=128,
+//               fp32 accumulator in tensor memory).
+//   warps 10,11 issue O_A += P_A,j V_j and O_B += P_B,j V_j for key halves
+//               A = [0, 64) and B = [64, 128) of every tile (N = 64, A
+//               operand P read straight from tensor memory).
+//   warps 0-3   softmax over key half A, warps 4-7 over key half B: one
+//               thread per (query row = tensor-memory lane, half).  Each
+//               thread loads its 64 scores, applies the causal / key-padding
+//               mask in-tile (masked score = -inf, i.e. exactly zero weight:
+//               aiany.app Step 10; notebook chapter "Masked Attention in the
+//               Decoder"), keeps its own running maximum m_h and sum l_h, and
+//               writes P_h = bf16(2^(s*c - m_h*c)) back over its scores.
 //
-// Score tiles rotate through three tensor-memory buffers (S_t(j) uses buffer
-// (2j + t) mod 3), so the MMA warp can compute the next score tile of a
-// query tile before the current P.V product of that tile has been issued:
-// it issues S_0(j+1), PV_0(j), S_1(j+1), PV_1(j), ...  While one softmax
-// group works on S_t(j+1) the tensor cores still hold PV_t(j), S_u(j+1),
-// PV_u(j) and S_t(j+2) of queued work.  Every M=128 MMA costs at least ~64
-// cycles whatever its N, so PV (N = 64) runs at half rate; the queue depth is
-// what keeps the pipe busy.
+// Splitting the row over two halves with their own maxima, sums and
+// accumulators is exact: the epilogue combines them as
+//   out = (O_A 2^((m_A-M)c) + O_B 2^((m_B-M)c)) / (l_A 2^((m_A-M)c) + l_B 2^((m_B-M)c)),
+// M = max(m_A, m_B).  The halves never wait for each other inside the loop.
 //
-// Handshakes are per score buffer: "S in buffer b is ready" and "P in buffer
-// b is ready".  A buffer's next use needs the MMA warp to have consumed the
-// current one, so neither barrier can run two phases ahead of its waiter.
+// Why three MMA warps: one thread can issue a tcgen05.mma only every ~60-80
+// cycles, while an N = 64 product needs ~32 cycles of tensor-core time, and
+// that thread also loses issue slots to the busy softmax warps on its SM
+// sub-partition.  Spread over three issuers (descriptors precomputed in
+// registers, loops unrolled so indices are constants) the tensor cores see a
+// steady stream.
 //
-// The running maximum is rescaled in O_t only when it grows by more than 2^8
-// (otherwise the stale maximum is kept; the probabilities then stay below
-// 256, exact in fp32 and fine in bf16), decided per row.  A rescale at tile j
-// needs PV_t(j-1) complete: it waits for the release of tile j-1's K/V stage,
-// which is committed after both products of that tile.
+// Score tiles rotate through three tensor-memory buffers (S_j in buffer
+// j mod 3): while the softmax works on S_j, S_{j+1} is ready and S_{j+2} is
+// being computed.  Issuers are ordered only through barriers:
+//   S ready (per buffer)           S issuer -> softmax,
+//   P_h ready (per buffer, half)   softmax half h -> PV issuer h,
+//   stage released (count 2)      both PV issuers -> TMA producer, S issuer
+//                                  (S_{j+2} overwrites tile j-1's buffer, so
+//                                  it waits for tile j-1's release) and a
+//                                  softmax that must rescale O_h,
+//   output final (count 2)         both PV issuers -> epilogue.
+// A buffer's next use needs its current use to be consumed, so no barrier
+// can run two phases ahead of its waiter.
+//
+// The running maximum is rescaled in O_h only when it grows by more than
+// 2^8 (otherwise the stale maximum is kept; the probabilities then stay below
+// 256, exact in fp32 and fine in bf16), decided per row.
 //
 // Tensor memory (512 columns): S buffers [0,128), [128,256), [256,384);
-// O0 [384,448), O1 [448,512).  P overwrites the first 64 columns of its S
-// buffer.
+// O_A [384,448), O_B [448,512).  P_A sits in buffer columns [0,32) and P_B
+// in [64,96): each half writes over scores it has already read.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -54,39 +66,37 @@
 namespace mha {
 namespace {
 
-constexpr int BM = 128;        // query rows per tile
+constexpr int BM = 128;        // query rows per CTA
 constexpr int BN = 128;        // keys per tile
 constexpr int HD = kAttnHeadDim;
-constexpr int NQ = 2;          // query tiles per CTA
 constexpr int STAGES = 4;      // K/V ring depth
-constexpr int kThreads = 320;  // 8 softmax warps + load warp + MMA warp
+constexpr int kSBufs = 3;      // score buffers in tensor memory
+constexpr int kThreads = 384;  // 8 softmax warps + load warp + 3 MMA warps
+constexpr int kSoftmaxWarps = 8;
 constexpr int kLoadWarp = 8;
-constexpr int kMmaWarp = 9;
+constexpr int kMmaSWarp = 9;   // issues S = Q K^T
+constexpr int kMmaPvWarp = 10; // warps 10, 11 issue PV for key halves A, B
 constexpr uint32_t kTileBytes = BM * HD * 2;  // 16 KiB, one 128 x 64 bf16 tile
 constexpr uint32_t kTmemCols = 512;
-constexpr int kSBufs = 3;                    // score buffers in tensor memory
+constexpr uint32_t kOCol = 384;  // O_A [384,448), O_B [448,512)
 constexpr float kRescaleThreshold = 8.0f;    // log2 units
 
-// Score slots are numbered in issue order over the (tile j, query tile t)
-// pairs that exist (query tile t has n_t key tiles): slot u uses buffer
-// u mod 3 (128 columns each) for the (u / 3)-th time.
-__device__ __forceinline__ int score_slot(int j, int t, int n0, int n1) {
-    return min(j, n0) + min(j, n1) + ((t == 1 && j < n0) ? 1 : 0);
-}
-__device__ __forceinline__ uint32_t s_col(int u) { return 128u * static_cast<uint32_t>(u % kSBufs); }
-__device__ __forceinline__ uint32_t o_col(int t) { return 384u + 64u * static_cast<uint32_t>(t); }
+__device__ __forceinline__ uint32_t s_col(int j) { return 128u * static_cast<uint32_t>(j % kSBufs); }
 
 struct __align__(1024) SmemAttn {
-    uint8_t q[NQ][kTileBytes];
+    uint8_t q[kTileBytes];
     uint8_t k[STAGES][kTileBytes];
     uint8_t v[STAGES][kTileBytes];
+    float red_m[2][BM];  // [column half][row]: final running maximum
+    float red_l[2][BM];  // [column half][row]: final running sum
     uint64_t q_full;
     uint64_t kv_full[STAGES];
     uint64_t kv_empty[STAGES];
     uint64_t s_full[kSBufs];
-    uint64_t p_full[kSBufs];
-    uint64_t o_final[NQ];
-    uint64_t drain;
+    uint64_t p_full[kSBufs][2];  // [buffer][column half]
+    uint64_t l_ready;
+    uint64_t o_final;
+    uint64_t drain[3];  // one per MMA-issuing warp
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -108,39 +118,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qb = p.num_qblocks - 1 - static_cast<int>(blockIdx.y);  // longest first
     const int b = bh / p.H;
     const int hh = bh - b * p.H;
-    const int q0 = qb * (NQ * BM);
+    const int q0 = qb * BM;
     const bool causal = (p.mask & kMaskCausalBit) != 0;
 
-    // Visible key range of each query tile.
+    // Visible key range of the query tile: keys [0, kv_end).
     int kv_len = p.Tk;
     if ((p.mask & kMaskPaddingBit) && p.key_lens) kv_len = min(max(p.key_lens[b], 0), p.Tk);
-    int n_tiles[NQ];
-#pragma unroll
-    for (int t = 0; t < NQ; ++t) {
-        const int row_lo = q0 + t * BM;
-        int end = kv_len;
-        if (row_lo >= p.Tq) end = 0;
-        else if (causal) end = min(end, min(row_lo + BM, p.Tq));
-        n_tiles[t] = (end + BN - 1) / BN;
-    }
-    const int n_kv = max(n_tiles[0], n_tiles[1]);
+    const int kv_end = causal ? min(kv_len, min(q0 + BM, p.Tq)) : kv_len;
+    const int n_kv = (kv_end + BN - 1) / BN;
 
     if (threadIdx.x == 0) {
         mbar_init(&sm.q_full, 1);
         for (int i = 0; i < STAGES; ++i) {
             mbar_init(&sm.kv_full[i], 1);
-            mbar_init(&sm.kv_empty[i], 1);
+            mbar_init(&sm.kv_empty[i], 2);  // one commit per PV issuer
         }
-        for (int b = 0; b < kSBufs; ++b) {
-            mbar_init(&sm.s_full[b], 1);
-            mbar_init(&sm.p_full[b], BM / 32);  // one arrival per softmax warp
+        for (int i = 0; i < kSBufs; ++i) {
+            mbar_init(&sm.s_full[i], 1);
+            mbar_init(&sm.p_full[i][0], kSoftmaxWarps / 2);  // one arrival per warp of a half
+            mbar_init(&sm.p_full[i][1], kSoftmaxWarps / 2);
         }
-        for (int t = 0; t < NQ; ++t) mbar_init(&sm.o_final[t], 1);
-        mbar_init(&sm.drain, 1);
+        mbar_init(&sm.l_ready, kSoftmaxWarps);
+        mbar_init(&sm.o_final, 2);          // one commit per PV issuer
+        for (int i = 0; i < 3; ++i) mbar_init(&sm.drain[i], 1);
         sm.abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == kMmaWarp) {
+    if (warp == kMmaSWarp) {
         tmem_alloc(&sm.tmem_base, kTmemCols);
         tmem_relinquish();
     }
@@ -158,8 +162,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kLoadWarp) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0 && n_kv > 0) {
-            mbar_arrive_expect_tx(&sm.q_full, NQ * kTileBytes);
-            for (int t = 0; t < NQ; ++t) tma_load_3d(&tmap_q, &sm.q_full, sm.q[t], 0, q0 + t * BM, bh);
+            mbar_arrive_expect_tx(&sm.q_full, kTileBytes);
+            tma_load_3d(&tmap_q, &sm.q_full, sm.q, 0, q0, bh);
             int issued = 0;
             for (int j = 0; j < n_kv; ++j) {
                 const int st = j % STAGES;
@@ -175,215 +179,208 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = max(0, issued - STAGES); j < issued; ++j)
                 mbar_wait_drain(&sm.kv_full[j % STAGES], (j / STAGES) & 1);
         }
-    } else if (warp == kMmaWarp) {
-        // ------------------------------------------------------- MMA issuer
+    } else if (warp == kMmaSWarp) {
+        // ----------------------------------------------------- S issuer
+        // One thread can issue a tcgen05.mma only every ~60-80 cycles, so the
+        // MMAs of a tile are spread over three issuing warps: this one issues
+        // S_{j+2} = Q K_{j+2}^T (4 MMAs, N = 128), warps 10 and 11 the two
+        // P.V halves.  They are ordered only through barriers: S_{j+2}
+        // overwrites the buffer of tile j-1, so it waits for the release of
+        // tile j-1's stage (both P.V halves of tile j-1 complete).
         if (lane == 0 && n_kv > 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, false, false);
-            constexpr uint32_t idesc_o = idesc_bf16_f32(BM, HD, false, true);
-            const int n0 = n_tiles[0], n1 = n_tiles[1];
-            // Shared-memory descriptors, built once.  Tiles of one kind are
-            // contiguous, so stage st adds st * 16 KiB (>> 4 = 1024) to the
-            // start-address field; a K step of 16 adds 32 bytes (2) within a
-            // K-major row and 16 V rows (2 KiB, 128) for the MN-major V tile.
-            const uint64_t q_desc0 = smem_desc_sw128(smem_u32(sm.q[0]), 16, 1024);
-            const uint64_t k_desc0 = smem_desc_sw128(smem_u32(sm.k[0]), 16, 1024);
-            const uint64_t v_desc0 = smem_desc_sw128(smem_u32(sm.v[0]), 1024, 1024);
+            // Shared-memory descriptors, built once into registers (a K step
+            // of 16 adds 32 bytes = 2 in a K-major row; stage st adds
+            // st * 16 KiB >> 4).  The loop is unrolled by 12 = lcm(3 buffers,
+            // 4 stages) so buffers and stages are compile-time constants.
             constexpr uint64_t kTileDesc = kTileBytes >> 4;
-
-            // One group per query tile t: S_t(j_s) (if has_s) and PV_t(j_pv)
-            // (if has_pv), interleaved so the PV chain (one accumulator) and
-            // the S chain overlap in the tensor pipe.  The group opens with
-            // two PV MMAs: the S it carries overwrites a buffer the previous
-            // group's PV read, and the gap keeps that reuse off the critical
-            // path.  The S-ready commit follows the last S MMA (it also
-            // covers the PV MMAs issued before it).
-            auto issue_group = [&](int t, bool has_s, int st_s, int j_s, bool has_pv, int st_pv,
-                                   int j_pv) {
-                const int us = has_s ? score_slot(j_s, t, n0, n1) : 0;
-                const int up = has_pv ? score_slot(j_pv, t, n0, n1) : 0;
-                const uint32_t d_s = tmem + s_col(us);
-                const uint32_t a_p = tmem + s_col(up);
-                const uint32_t d_o = tmem + o_col(t);
-                const uint64_t qd = q_desc0 + static_cast<uint64_t>(t) * kTileDesc;
-                const uint64_t kd = k_desc0 + static_cast<uint64_t>(st_s) * kTileDesc;
-                const uint64_t vd = v_desc0 + static_cast<uint64_t>(st_pv) * kTileDesc;
-                const uint32_t acc0 = j_pv > 0 ? 1u : 0u;
-                // schedule: PV0 PV1 S0 PV2 S1 PV3 S2 PV4 S3 [commit] PV5 PV6 PV7
+            const uint64_t q_desc = smem_desc_sw128(smem_u32(sm.q), 16, 1024);
+            const uint64_t k_desc0 = smem_desc_sw128(smem_u32(sm.k[0]), 16, 1024);
+            uint64_t qd[HD / 16], kd[STAGES][HD / 16];
 #pragma unroll
-                for (int step = 0; step < 13; ++step) {
-                    constexpr int kind_tab[13] = {0, 0, 1, 0, 1, 0, 1, 0, 1, 2, 0, 0, 0};
-                    constexpr int idx_tab[13] = {0, 1, 0, 2, 1, 3, 2, 4, 3, 0, 5, 6, 7};
-                    const int kind = kind_tab[step], i = idx_tab[step];
-                    if (kind == 0 && has_pv)
-                        mma_bf16_ts(d_o, a_p + 8 * i, vd + 128 * i, idesc_o, (i > 0) ? 1u : acc0);
-                    else if (kind == 1 && has_s)
-                        mma_bf16_ss(d_s, qd + 2 * i, kd + 2 * i, idesc_s, i > 0 ? 1u : 0u);
-                    else if (kind == 2 && has_s)
-                        mma_commit(&sm.s_full[us % kSBufs]);
-                }
+            for (int kk = 0; kk < HD / 16; ++kk) qd[kk] = q_desc + 2 * kk;
+#pragma unroll
+            for (int st = 0; st < STAGES; ++st)
+#pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk) kd[st][kk] = k_desc0 + st * kTileDesc + 2 * kk;
+            // S_j into buffer sb = j mod 3 from stage st = j mod 4.
+            auto issue_s = [&](int sb, int st) {
+                const uint32_t d = tmem + 128u * sb;
+#pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk)
+                    mma_bf16_ss(d, qd[kk], kd[st][kk], idesc_s, kk > 0 ? 1u : 0u);
+                mma_commit(&sm.s_full[sb]);
             };
-            // P of query tile t, key tile j is ready.
-            auto wait_p = [&](int t, int j) {
-                const int u = score_slot(j, t, n0, n1);
-                return mbar_wait(&sm.p_full[u % kSBufs], (u / kSBufs) & 1, ab);
-            };
-            // Each wait sits right after an MMA group has been issued, so the
-            // tensor pipe has queued work while this thread polls.
-            auto wait_kv = [&](int j) {
-                return mbar_wait(&sm.kv_full[j % STAGES], (j / STAGES) & 1, ab);
-            };
-            bool ok = mbar_wait(&sm.q_full, 0, ab) && wait_kv(0);
+            bool ok = mbar_wait(&sm.q_full, 0, ab) && mbar_wait(&sm.kv_full[0], 0, ab);
             if (ok) {
                 tc_fence_after_sync();
-                if (n0 > 0) issue_group(0, true, 0, 0, false, 0, 0);
-                if (n1 > 0) issue_group(1, true, 0, 0, false, 0, 0);
-                if (n_kv > 1) ok = wait_kv(1);
+                issue_s(0, 0);
+                if (n_kv > 1 && (ok = mbar_wait(&sm.kv_full[1], 0, ab))) issue_s(1, 1);
             }
-            for (int j = 0; ok && j < n_kv; ++j) {
-                const int st = j % STAGES;
-                const int st1 = (j + 1) % STAGES;
-                const bool next0 = j + 1 < n0, next1 = j + 1 < n1;
-                const bool pv0 = j < n0, pv1 = j < n1;
-                // K/V of tiles j and j+1 are resident (waited one group ago).
-                // Tile 0: S_0(j+1) looks ahead into the buffer PV_1(j-1) has
-                // already consumed; PV_0(j) needs P_0(j).
-                if (pv0 && !(ok = wait_p(0, j))) break;
-                tc_fence_after_sync();
-                issue_group(0, next0, st1, j + 1, pv0, st, j);
-                if (pv0 && j == n0 - 1) mma_commit(&sm.o_final[0]);
-                // Tile 1: S_1(j+1) reuses the buffer of P_0(j), read by the
-                // group just issued (tensor-core operations of one thread run
-                // in order).
-                if (pv1 && !(ok = wait_p(1, j))) break;
-                tc_fence_after_sync();
-                issue_group(1, next1, st1, j + 1, pv1, st, j);
-                if (pv1 && j == n1 - 1) mma_commit(&sm.o_final[1]);
-                mma_commit(&sm.kv_empty[st]);
-                if (j + 2 < n_kv && !(ok = wait_kv(j + 2))) break;
+            for (int jb = 0; ok && jb + 2 < n_kv; jb += 12) {
+#pragma unroll
+                for (int u = 0; u < 12; ++u) {
+                    const int j = jb + u;  // issue S_{j+2}
+                    if (j + 2 >= n_kv) break;
+                    if (!(ok = mbar_wait(&sm.kv_full[(u + 2) % STAGES], ((j + 2) >> 2) & 1, ab))) break;
+                    if (j >= 1 && !(ok = mbar_wait(&sm.kv_empty[(u + 3) % STAGES], ((j - 1) >> 2) & 1, ab)))
+                        break;
+                    tc_fence_after_sync();
+                    issue_s((u + 2) % kSBufs, (u + 2) % STAGES);
+                }
             }
             // Always wait (time-bounded, whatever the abort state) until every
             // MMA this thread issued has completed: tensor memory is released
             // and the CTA exits only after that.
-            mma_commit(&sm.drain);
-            mbar_wait_drain(&sm.drain, 0);
+            mma_commit(&sm.drain[0]);
+            mbar_wait_drain(&sm.drain[0], 0);
+        }
+    } else if (warp >= kMmaPvWarp) {
+        // ---------------------------------------------------- PV issuers
+        // Warp 10 + h: O_h (+)= P_h,j V_j[keys 64h .. 64h+63], A = P_h in
+        // tensor memory (8 columns per 16 keys, at buffer columns 64h..),
+        // B = V tile (MN-major, 16 keys = 2 KiB = 128 per K step).
+        const int hf = warp - kMmaPvWarp;
+        if (lane == 0 && n_kv > 0) {
+            constexpr uint32_t idesc_o = idesc_bf16_f32(BM, HD, false, true);
+            constexpr uint64_t kTileDesc = kTileBytes >> 4;
+            const uint64_t v_desc0 = smem_desc_sw128(smem_u32(sm.v[0]), 1024, 1024);
+            uint64_t vd[STAGES][4];
+#pragma unroll
+            for (int st = 0; st < STAGES; ++st)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    vd[st][kk] = v_desc0 + st * kTileDesc + 128 * (4 * hf + kk);
+            const uint32_t d_o = tmem + kOCol + 64u * hf;
+            bool ok = true;
+            for (int jb = 0; ok && jb < n_kv; jb += 12) {
+                const uint32_t acc_first = jb > 0 ? 1u : 0u;
+#pragma unroll
+                for (int u = 0; u < 12; ++u) {
+                    const int j = jb + u;
+                    if (j >= n_kv) break;
+                    // P_h,j ready (use j / 3 of its buffer: parity (u / 3) & 1
+                    // since jb / 3 is even) and V_j resident.
+                    if (!(ok = mbar_wait(&sm.p_full[u % kSBufs][hf], (u / kSBufs) & 1, ab))) break;
+                    if (!(ok = mbar_wait(&sm.kv_full[u % STAGES], (j >> 2) & 1, ab))) break;
+                    tc_fence_after_sync();
+                    const uint32_t a = tmem + 128u * (u % kSBufs) + 64u * hf;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16_ts(d_o, a + 8 * kk, vd[u % STAGES][kk], idesc_o,
+                                    (u > 0 || kk > 0) ? 1u : acc_first);
+                    if (j == n_kv - 1) mma_commit(&sm.o_final);
+                    mma_commit(&sm.kv_empty[u % STAGES]);
+                }
+            }
+            mma_commit(&sm.drain[1 + hf]);
+            mbar_wait_drain(&sm.drain[1 + hf], 0);
         }
     } else {
         // --------------------------------------------------------- softmax
-        const int t = warp >> 2;
+        // Half h owns keys [64h, 64h+64) of every tile with its own running
+        // maximum m_h, running sum l_h and accumulator O_h; the two halves
+        // are combined once, in the epilogue.
+        const int half = warp >> 2;
         const uint32_t lane_base = static_cast<uint32_t>(warp & 3) * 32;
-        const int r = static_cast<int>(lane_base) + lane;  // row in tile = TMEM lane
-        const int row = q0 + t * BM + r;                   // query index
+        const int r = static_cast<int>(lane_base) + lane;    // row in tile = TMEM lane
+        const int row = q0 + r;                              // query index
         const uint32_t tl = tmem_addr(tmem, lane_base, 0);
-        const uint32_t to = tl + o_col(t);
-        const int nt = t == 0 ? n_tiles[0] : n_tiles[1];
+        const uint32_t to = tl + kOCol + 64u * half;         // O_h: 64 columns
         const float C = p.scale_log2;
         const int row_lim = causal ? min(kv_len, row + 1) : kv_len;  // keys < row_lim visible
-        const int tile_row_lo = q0 + t * BM;
-        float m_run = -INFINITY;
+        float m_run = -INFINITY;  // -inf until this half has seen a visible key
         float l_run = 0.f;
         bool ok = true;
 
-        for (int j = 0; j < nt; ++j) {
-            const int u = score_slot(j, t, n_tiles[0], n_tiles[1]);
+        for (int j = 0; j < n_kv; ++j) {
             ok = __all_sync(0xffffffffu,
-                            mbar_wait(&sm.s_full[u % kSBufs], (u / kSBufs) & 1, ab));
+                            mbar_wait(&sm.s_full[j % kSBufs], (j / kSBufs) & 1, ab));
             if (!ok) break;
             tc_fence_after_sync();
-            const uint32_t ts = tl + s_col(u);
-            uint32_t s0[32], s1[32], s2[32], s3[32];
-            tmem_ld32(ts + 0, s0);
+            const uint32_t ts = tl + s_col(j) + 64u * half;
+            uint32_t s0[32], s1[32];
+            tmem_ld32(ts, s0);
             tmem_ld32(ts + 32, s1);
-            tmem_ld32(ts + 64, s2);
-            tmem_ld32(ts + 96, s3);
             tmem_ld_wait(s0);
             reg_fence32(s1);
-            reg_fence32(s2);
-            reg_fence32(s3);
 
             // In-tile mask: only tiles that reach past the padding length or
             // the diagonal need it (tile-uniform branch).  Keys with index
             // >= row_lim get -inf, i.e. weight exactly zero.
-            const int k0 = j * BN;
-            if ((k0 + BN > kv_len) || (causal && k0 + BN - 1 > tile_row_lo)) {
-                const int lim = row_lim - k0;
+            if ((j * BN + BN > kv_len) || (causal && j * BN + BN - 1 > q0)) {
+                const int lim = row_lim - (j * BN + 64 * half);
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
                     if (c >= lim) s0[c] = f2u(-INFINITY);
                     if (c + 32 >= lim) s1[c] = f2u(-INFINITY);
-                    if (c + 64 >= lim) s2[c] = f2u(-INFINITY);
-                    if (c + 96 >= lim) s3[c] = f2u(-INFINITY);
                 }
             }
 
-            // Row maximum of the tile: eight independent chains of three-input
-            // maxima, then a small tree.
-            float tm[8];
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                tm[i] = fmaxf(u2f(s0[i]), u2f(s0[i + 2]));
-                tm[2 + i] = fmaxf(u2f(s1[i]), u2f(s1[i + 2]));
-                tm[4 + i] = fmaxf(u2f(s2[i]), u2f(s2[i + 2]));
-                tm[6 + i] = fmaxf(u2f(s3[i]), u2f(s3[i + 2]));
-            }
+            // Maximum over this half's 64 scores: four chains of three-input
+            // maxima.
+            float tm0 = fmaxf(u2f(s0[0]), u2f(s0[1])), tm1 = fmaxf(u2f(s0[2]), u2f(s0[3]));
+            float tm2 = fmaxf(u2f(s1[0]), u2f(s1[1])), tm3 = fmaxf(u2f(s1[2]), u2f(s1[3]));
 #pragma unroll
             for (int c = 4; c < 32; c += 4) {
-#pragma unroll
-                for (int i = 0; i < 2; ++i) {
-                    tm[i] = fmax3(tm[i], u2f(s0[c + i]), u2f(s0[c + i + 2]));
-                    tm[2 + i] = fmax3(tm[2 + i], u2f(s1[c + i]), u2f(s1[c + i + 2]));
-                    tm[4 + i] = fmax3(tm[4 + i], u2f(s2[c + i]), u2f(s2[c + i + 2]));
-                    tm[6 + i] = fmax3(tm[6 + i], u2f(s3[c + i]), u2f(s3[c + i + 2]));
-                }
+                tm0 = fmax3(tm0, u2f(s0[c]), u2f(s0[c + 1]));
+                tm1 = fmax3(tm1, u2f(s0[c + 2]), u2f(s0[c + 3]));
+                tm2 = fmax3(tm2, u2f(s1[c]), u2f(s1[c + 1]));
+                tm3 = fmax3(tm3, u2f(s1[c + 2]), u2f(s1[c + 3]));
             }
-            tm[0] = fmax3(tm[0], tm[1], tm[2]);
-            tm[3] = fmax3(tm[3], tm[4], tm[5]);
-            tm[0] = fmax3(tm[0], tm[3], fmaxf(tm[6], tm[7]));
+            const float mx = fmaxf(fmax3(tm0, tm1, tm2), tm3);
 
             // Running maximum: keep the stale one unless it grew by > 2^8.
-            // The decision is per row, so a row's result never depends on
-            // another row's scores; the warp only shares the tensor-memory
-            // access (rows that keep their maximum scale O by exactly 1).
-            const float m_new = fmaxf(m_run, tm[0]);
-            const bool grow = j > 0 && (m_new - m_run) * C > kRescaleThreshold;
+            // Decided per row, so a row's result never depends on another
+            // row's scores; the warp only shares the tensor-memory access
+            // (rows that keep their maximum scale O_h by exactly 1).  While
+            // m_h is still -inf, O_h and l_h are exactly zero and need no
+            // rescale.
+            const float m_new = fmaxf(m_run, mx);
+            const bool grow = m_run != -INFINITY && (m_new - m_run) * C > kRescaleThreshold;
             const bool rescale = __any_sync(0xffffffffu, grow);
             float alpha = 1.f;
-            if (j == 0) {
+            if (m_run == -INFINITY) {
                 m_run = m_new;
             } else if (grow) {
                 alpha = ex2_approx((m_run - m_new) * C);
                 l_run *= alpha;
                 m_run = m_new;
             }
-            const float mc = m_run * C;
+            const float mc = m_run == -INFINITY ? 0.f : m_run * C;
 
-            // P = 2^(s*c - m*c) in bf16 over the first 64 columns of the
-            // buffer (column c holds keys 2c, 2c+1; chunk q of 32 scores
-            // becomes P columns [16q, 16q+16), all already read).
-            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#define MHA_EXP_CHUNK(SRC, COL)                                               \
-            {                                                                 \
-                uint32_t pk[16];                                              \
-                _Pragma("unroll") for (int c = 0; c < 16; ++c) {              \
-                    const float e0 = ex2_approx(fmaf(u2f(SRC[2 * c]), C, -mc));     \
-                    const float e1 = ex2_approx(fmaf(u2f(SRC[2 * c + 1]), C, -mc)); \
-                    acc[(2 * c) & 7] += e0;                                   \
-                    acc[(2 * c + 1) & 7] += e1;                               \
-                    pk[c] = pack_bf16x2(e0, e1);                              \
-                }                                                             \
-                tmem_st16(ts + (COL), pk);                                    \
+            // P = 2^(s*c - m*c) in bf16, written over this half's first 32
+            // score columns (column c holds keys 2c, 2c+1 of the half).
+            // Packed fp32x2 FMA / add (one instruction per two scores) keep
+            // the instruction count -- and the issue slots taken from the MMA
+            // warp on the same sub-partition -- down.
+            const uint64_t c2 = f32x2_pack(C, C), nmc2 = f32x2_pack(-mc, -mc);
+            uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+            uint32_t pk[32];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                float x0, x1, x2, x3;
+                f32x2_unpack(fma_f32x2(f32x2_pack(u2f(s0[2 * c]), u2f(s0[2 * c + 1])), c2, nmc2), x0, x1);
+                f32x2_unpack(fma_f32x2(f32x2_pack(u2f(s1[2 * c]), u2f(s1[2 * c + 1])), c2, nmc2), x2, x3);
+                const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
+                const float e2 = ex2_approx(x2), e3 = ex2_approx(x3);
+                acc2[c & 1] = add_f32x2(acc2[c & 1], f32x2_pack(e0, e1));
+                acc2[2 + (c & 1)] = add_f32x2(acc2[2 + (c & 1)], f32x2_pack(e2, e3));
+                pk[c] = pack_bf16x2(e0, e1);
+                pk[16 + c] = pack_bf16x2(e2, e3);
             }
-            MHA_EXP_CHUNK(s0, 0)
-            MHA_EXP_CHUNK(s1, 16)
-            MHA_EXP_CHUNK(s2, 32)
-            MHA_EXP_CHUNK(s3, 48)
-#undef MHA_EXP_CHUNK
-            l_run += ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+            tmem_st32(ts, pk);
+            {
+                float u0, u1;
+                f32x2_unpack(add_f32x2(add_f32x2(acc2[0], acc2[1]), add_f32x2(acc2[2], acc2[3])), u0, u1);
+                l_run += u0 + u1;
+            }
 
             if (rescale) {
-                // O_t must hold exactly sum_{j' < j} P V: wait for the
-                // release of tile j-1's stage (committed after PV_0(j-1) and
-                // PV_1(j-1)).  Its next release needs P_t(j), which this
-                // thread has not yet published, so the parity cannot alias.
+                // O_h must hold exactly sum_{j' < j} P V: wait for the release
+                // of tile j-1's stage (committed after both products of tile
+                // j-1).  Its next release needs P_j, which this thread has not
+                // yet published, so the parity cannot alias.
                 ok = __all_sync(0xffffffffu, mbar_wait(&sm.kv_empty[(j - 1) % STAGES],
                                                        ((j - 1) / STAGES) & 1, ab));
                 if (!ok) {
@@ -407,36 +404,52 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st_wait();
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.p_full[u % kSBufs]);
+            if (lane == 0) mbar_arrive(&sm.p_full[j % kSBufs][half]);
         }
 
         // ----------------------------------------------------------- epilogue
-        if (ok && nt > 0) ok = __all_sync(0xffffffffu, mbar_wait(&sm.o_final[t], 0, ab));
+        // out = (O_A w_A + O_B w_B) / (l_A w_A + l_B w_B), w_h = 2^((m_h - M) c),
+        // M = max(m_A, m_B); a half that saw no visible key has weight 0.
+        // Half h stores output columns [32h, 32h+32).
         if (ok) {
-            uint32_t o0[32], o1[32];
-            if (nt > 0) {
+            sm.red_m[half][r] = m_run;
+            sm.red_l[half][r] = l_run;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.l_ready);
+            ok = __all_sync(0xffffffffu, mbar_wait(&sm.l_ready, 0, ab));
+        }
+        if (ok && n_kv > 0) ok = __all_sync(0xffffffffu, mbar_wait(&sm.o_final, 0, ab));
+        if (ok) {
+            uint32_t oa[32], ob[32];
+            if (n_kv > 0) {
                 tc_fence_after_sync();
-                tmem_ld32(to, o0);
-                tmem_ld32(to + 32, o1);
-                tmem_ld_wait(o0);
-                reg_fence32(o1);
+                tmem_ld32(tl + kOCol + 32u * half, oa);
+                tmem_ld32(tl + kOCol + 64u + 32u * half, ob);
+                tmem_ld_wait(oa);
+                reg_fence32(ob);
             } else {
 #pragma unroll
-                for (int c = 0; c < 32; ++c) o0[c] = o1[c] = 0u;
+                for (int c = 0; c < 32; ++c) oa[c] = ob[c] = 0u;
             }
             if (row < p.Tq) {
-                const float inv = l_run > 0.f ? 1.0f / l_run : 0.f;
-                uint32_t packed[32];
+                const float ma = sm.red_m[0][r], mb = sm.red_m[1][r];
+                const float la = sm.red_l[0][r], lb = sm.red_l[1][r];
+                const float M = fmaxf(ma, mb);
+                const float wa = la > 0.f ? ex2_approx((ma - M) * C) : 0.f;
+                const float wb = lb > 0.f ? ex2_approx((mb - M) * C) : 0.f;
+                const float L = la * wa + lb * wb;
+                const float inv = L > 0.f ? 1.0f / L : 0.f;
+                const float fa = wa * inv, fb = wb * inv;
+                uint32_t packed[16];
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    packed[c] = pack_bf16x2(u2f(o0[2 * c]) * inv, u2f(o0[2 * c + 1]) * inv);
-                    packed[c + 16] = pack_bf16x2(u2f(o1[2 * c]) * inv, u2f(o1[2 * c + 1]) * inv);
-                }
+                for (int c = 0; c < 16; ++c)
+                    packed[c] = pack_bf16x2(u2f(oa[2 * c]) * fa + u2f(ob[2 * c]) * fb,
+                                            u2f(oa[2 * c + 1]) * fa + u2f(ob[2 * c + 1]) * fb);
                 __nv_bfloat16 *dst = p.o + b * p.o_stride_b + hh * p.o_stride_h +
-                                     static_cast<long long>(row) * p.o_stride_t;
+                                     static_cast<long long>(row) * p.o_stride_t + 32 * half;
                 uint4 *d4 = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
+                for (int c = 0; c < 4; ++c)
                     d4[c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2],
                                        packed[4 * c + 3]);
             }
@@ -445,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == kMmaWarp) {
+    if (warp == kMmaSWarp) {
         tc_fence_after_sync();
         tmem_dealloc(tmem, kTmemCols);
     }

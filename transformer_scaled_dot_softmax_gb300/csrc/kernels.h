@@ -22,7 +22,7 @@ struct AttnParams {
     int num_qblocks;   // ceil(Tq / rows per CTA)
     int *status;
 };
-constexpr int kAttnRowsPerCta = 256;  // two 128-row query tiles per CTA
+constexpr int kAttnRowsPerCta = 128;  // one 128-row query tile per CTA
 constexpr int kAttnHeadDim = 64;
 
 // q, k, v: head-split (B, H, T, 64) bf16 tensors described by 3-D TMA maps

@@ -330,6 +330,27 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
     return m;
 }
 
+// Packed fp32x2 arithmetic (sm_100 and later): a 64-bit register holds two
+// fp32 lanes {lo, hi}; one instruction does both.
+__device__ __forceinline__ uint64_t f32x2_pack(float lo, float hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ __forceinline__ void f32x2_unpack(uint64_t r, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+    return r;
+}
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+    uint64_t r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+    return r;
+}
+
 // Packs two fp32 values into bf16x2 (round to nearest even): `lo` goes to
 // the low half (the lower column / k index), `hi` to the high half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
