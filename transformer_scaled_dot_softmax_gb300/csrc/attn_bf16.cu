@@ -11,7 +11,7 @@
 // One CTA owns one 128-row query tile of one (b, h) and streams the visible
 // K/V tiles through shared memory.  Warp roles:
 //
-//   warp 8      TMA producer: Q once; K_j and V_j together into a 4-stage
+//   warp 8      TMA producer: Q once; K_j and V_j together into a 6-stage
 //               ring (one barrier per stage for both tiles).
 //   warp 9      issues S_j = Q K_j^T (tcgen05.mma kind::f16, M=128 N=128,
 //               fp32 accumulator in tensor memory).
@@ -69,7 +69,8 @@ namespace {
 constexpr int BM = 128;        // query rows per CTA
 constexpr int BN = 128;        // keys per tile
 constexpr int HD = kAttnHeadDim;
-constexpr int STAGES = 4;      // K/V ring depth
+constexpr int STAGES = 6;      // K/V ring depth
+static_assert(12 % STAGES == 0, "the main loops are unrolled by 12");
 constexpr int kSBufs = 3;      // score buffers in tensor memory
 constexpr int kThreads = 384;  // 8 softmax warps + load warp + 3 MMA warps
 constexpr int kSoftmaxWarps = 8;
@@ -222,8 +223,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int u = 0; u < 12; ++u) {
                     const int j = jb + u;  // issue S_{j+2}
                     if (j + 2 >= n_kv) break;
-                    if (!(ok = mbar_wait(&sm.kv_full[(u + 2) % STAGES], ((j + 2) >> 2) & 1, ab))) break;
-                    if (j >= 1 && !(ok = mbar_wait(&sm.kv_empty[(u + 3) % STAGES], ((j - 1) >> 2) & 1, ab)))
+                    if (!(ok = mbar_wait(&sm.kv_full[(u + 2) % STAGES], ((j + 2) / STAGES) & 1, ab)))
+                        break;
+                    if (j >= 1 && !(ok = mbar_wait(&sm.kv_empty[(u + STAGES - 1) % STAGES],
+                                                   ((j - 1) / STAGES) & 1, ab)))
                         break;
                     tc_fence_after_sync();
                     issue_s((u + 2) % kSBufs, (u + 2) % STAGES);
@@ -262,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // P_h,j ready (use j / 3 of its buffer: parity (u / 3) & 1
                     // since jb / 3 is even) and V_j resident.
                     if (!(ok = mbar_wait(&sm.p_full[u % kSBufs][hf], (u / kSBufs) & 1, ab))) break;
-                    if (!(ok = mbar_wait(&sm.kv_full[u % STAGES], (j >> 2) & 1, ab))) break;
+                    if (!(ok = mbar_wait(&sm.kv_full[u % STAGES], (j / STAGES) & 1, ab))) break;
                     tc_fence_after_sync();
                     const uint32_t a = tmem + 128u * (u % kSBufs) + 64u * hf;
 #pragma unroll
