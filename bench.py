@@ -278,11 +278,86 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> int:
     if not args.no_e2e:
         e2e = run_e2e(args, q, k, v, out, w, stream, dev, dist, flops, world)
 
+    others = None
+    if rank == 0 and not args.no_other_workloads:
+        others = time_other_workloads(dev, stream, flush)
     if rank == 0:
-        emit(args, w, x, ms, ms_mean, value, flops, world, clocks, e2e)
+        emit(args, w, x, ms, ms_mean, value, flops, world, clocks, e2e, others)
     if dist is not None:
         dist.destroy_process_group()
     return 0
+
+
+def visible_pairs(w: si.Workload, key_lens) -> float:
+    """Exact number of visible (query, key) pairs of a workload."""
+    total = 0.0
+    for b in range(w.B):
+        L = w.T_k if key_lens is None else int(min(max(key_lens[b], 0), w.T_k))
+        if w.mask & si.MASK_CAUSAL:
+            i = np.arange(w.T_q)
+            total += float(np.minimum(i + 1, L).sum())
+        else:
+            total += float(w.T_q) * L
+    return total * w.h
+
+
+def mha_flops(w: si.Workload, key_lens) -> float:
+    """Projections (2 M K N each) plus attention over visible pairs."""
+    hd = w.h * w.d_k
+    proj = 2.0 * w.B * w.T_q * w.d_model * hd + 2.0 * 2 * w.B * w.T_k * w.d_model * hd \
+        + 2.0 * w.B * w.T_q * hd * w.d_model
+    return proj + 2.0 * (w.d_k + w.d_v) * visible_pairs(w, key_lens)
+
+
+def time_other_workloads(dev, stream, flush, iters=20):
+    """The four other workloads of the table: fp32 SDPA latency and the three
+    MHA forwards end to end (three launches), device-resident inputs, L2
+    flushed between calls, CUDA events around each call."""
+    import torch
+    import transformer_scaled_dot_softmax_gb300 as tsds
+
+    def dv(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(
+            torch.bfloat16)
+
+    def timed(fn):
+        for _ in range(3):
+            flush.zero_()
+            fn()
+        ev = []
+        for _ in range(iters):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            ev.append((a, b))
+        torch.cuda.synchronize(dev)
+        return float(np.median([a.elapsed_time(b) for a, b in ev]))
+
+    res = {}
+    w = si.WORKLOADS[0]
+    x = si.make_inputs(w)
+    q, k, v = (torch.from_numpy(x[n].astype(np.float32)).to(dev) for n in ("q", "k", "v"))
+    o = torch.empty_like(q)
+    ms = timed(lambda: tsds.sdpa_forward(q, k, v, o, scale=w.scale, stream=stream))
+    res[w.name] = {"ms": ms, "us": 1e3 * ms, "kind": "fp32 SIMT SDPA, launch-bound"}
+    for w in si.WORKLOADS[1:4]:
+        x = si.make_inputs(w)
+        xq = dv(x["x_q_bits"])
+        xkv = dv(x["x_kv_bits"]) if w.cross else xq
+        wts = [dv(x[n + "_bits"]) for n in ("w_q", "w_k", "w_v", "w_o")]
+        lens = None if x["key_lens"] is None else torch.from_numpy(x["key_lens"]).to(dev)
+        out = torch.empty((w.B, w.T_q, w.d_model), dtype=torch.bfloat16, device=dev)
+        ws = torch.empty(tsds.mha_workspace_bytes(w.B, w.h, w.T_q, w.T_k), dtype=torch.uint8,
+                         device=dev)
+        ms = timed(lambda: tsds.mha_forward(xq, xkv, *wts, h=w.h, out=out, workspace=ws,
+                                            scale=w.scale, mask=w.mask, key_lens=lens,
+                                            stream=stream))
+        fl = mha_flops(w, x["key_lens"])
+        res[w.name] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12, "flops": fl,
+                       "kind": "bf16 MHA forward: grouped QKV GEMM + fused attention + W^O GEMM"}
+    return res
 
 
 def run_e2e(args, q, k, v, out, w, stream, dev, dist, flops, world):
@@ -318,7 +393,7 @@ def run_e2e(args, q, k, v, out, w, stream, dev, dist, flops, world):
             "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
 
-def emit(args, w, x, ms, ms_mean, value, flops, world, clocks, e2e):
+def emit(args, w, x, ms, ms_mean, value, flops, world, clocks, e2e, others=None):
     peaks, peak_src = load_peaks()
     peak = float(peaks["bf16_tflops"])
     achieved = flops / (float(ms.mean()) * 1e-3) / 1e12
@@ -347,6 +422,7 @@ def emit(args, w, x, ms, ms_mean, value, flops, world, clocks, e2e):
         "gpu_launches": args.steps,
         "clocks": clocks.summary(),
         "ms_min": float(ms.min()), "ms_median": float(np.median(ms)),
+        "other_workloads": others,
     }
     print(json.dumps(line), flush=True)
 
@@ -361,6 +437,8 @@ def parse(argv=None):
                     help="CPU baseline: time every n-th query row of every head")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="skip timing the fp32 SDPA and the three MHA workloads")
     ap.add_argument("--shape", default=None,
                     help="B,h,T override of the causal workload (profiling and sweeps only; "
                          "the reported line then names the changed workload)")

@@ -78,3 +78,15 @@ def test_two_rank_aggregation_gloo():
     for _, ms_max, value in res:
         assert ms_max == 3.0
         assert value == pytest.approx(2 * 1e12 / 3e-3 / 1e12)
+
+
+def test_visible_pairs_and_mha_flops():
+    w = si.WORKLOADS[2].replace(B=1, h=1, T_q=4, T_k=4, d_model=64)
+    assert bench.visible_pairs(w, None) == 1 + 2 + 3 + 4          # causal triangle
+    w2 = si.WORKLOADS[1].replace(B=2, h=3, T_q=5, T_k=7, d_model=64)
+    lens = np.array([7, 2], dtype=np.int32)
+    assert bench.visible_pairs(w2, lens) == 3 * 5 * (7 + 2)
+    # projections 2MKN each: Q and O with M = B*T_q, K and V with M = B*T_k
+    hd = w2.h * 64
+    proj = 2 * 10 * 64 * hd + 2 * 2 * 14 * 64 * hd + 2 * 10 * hd * 64
+    assert bench.mha_flops(w2, lens) == pytest.approx(proj + 256 * 3 * 5 * 9)
