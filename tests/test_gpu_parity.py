@@ -173,6 +173,25 @@ def test_bf16_constant_values(lib):
     np.testing.assert_allclose(host(out), 1.5, rtol=0, atol=1.5 * 2 ** -7)
 
 
+@pytest.mark.parametrize("mask", [si.MASK_NONE, si.MASK_CAUSAL])
+@pytest.mark.parametrize("profile", ["growing", "jump", "shrinking"])
+def test_bf16_reference_maximum_updates(lib, profile, mask):
+    """Key tiles (128 keys) scaled so that a row's maximum score keeps growing
+    (every tile by ~20 log2 units: the exact step runs tile after tile),
+    jumps far enough that exponentials against the old maximum overflow
+    fp32, or only shrinks (the first maximum stays the reference)."""
+    w = si.WORKLOADS[4].replace(B=1, h=2, T_q=1024, T_k=1024, mask=mask, seed=36)
+    x = si.make_inputs(w)
+    nt = w.T_k // 128
+    f = {"growing": [6 * j + 1 for j in range(nt)],
+         "jump": [80 if j in (2, 5) else 1 for j in range(nt)],
+         "shrinking": [6 * (nt - j) + 1 for j in range(nt)]}[profile]
+    k = si.round_bf16(x["k"] * np.repeat(np.array(f, dtype=np.float64), 128)[None, None, :, None])
+    out = run_sdpa_bf16(lib, w, x, k=bf16_dev(si.f64_to_bf16_bits(k)))
+    ref = oracle.sdpa(x["q"], k, x["v"], scale=w.scale, mask=mask)
+    check_bf16(host(out), ref, "%s mask%d" % (profile, mask))
+
+
 def test_bf16_zero_length_rows_are_zero(lib):
     w = si.WORKLOADS[4].replace(B=2, h=1, T_q=130, T_k=300, mask=si.MASK_KEY_PADDING, seed=34)
     x = si.make_inputs(w)

@@ -51,9 +51,12 @@
 // A buffer's next use needs its current use to be consumed, so no barrier
 // can run two phases ahead of its waiter.
 //
-// The running maximum is rescaled in O_h only when it grows by more than
-// 2^8 (otherwise the stale maximum is kept; the probabilities then stay below
-// 256, exact in fp32 and fine in bf16), decided per row.
+// No maximum pass per tile: a tile is exponentiated against the half's
+// current reference maximum (softmax is shift-invariant, so any reference
+// that keeps the exponentials finite gives the same result), and only a row
+// whose tile sum exceeds 2^16 -- its maximum grew by 10 to 16 log2 units or
+// more -- or that has no reference yet takes the exact step (tile maximum,
+// O_h and l_h rescaled, P recomputed).  Decided per row.
 //
 // Tensor memory (512 columns): S buffers [0,128), [128,256), [256,384);
 // O_A [384,448), O_B [448,512).  P_A sits in buffer columns [0,32) and P_B
@@ -80,7 +83,7 @@ constexpr int kMmaPvWarp = 10; // warps 10, 11 issue PV for key halves A, B
 constexpr uint32_t kTileBytes = BM * HD * 2;  // 16 KiB, one 128 x 64 bf16 tile
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 384;  // O_A [384,448), O_B [448,512)
-constexpr float kRescaleThreshold = 8.0f;    // log2 units
+constexpr float kTileSumLimit = 65536.0f;  // 2^16: a tile sum above it takes the exact step
 
 __device__ __forceinline__ uint32_t s_col(int j) { return 128u * static_cast<uint32_t>(j % kSBufs); }
 
@@ -182,50 +185,46 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kMmaSWarp) {
         // ----------------------------------------------------- S issuer
-        // One thread can issue a tcgen05.mma only every ~60-80 cycles, so the
-        // MMAs of a tile are spread over three issuing warps: this one issues
-        // S_{j+2} = Q K_{j+2}^T (4 MMAs, N = 128), warps 10 and 11 the two
-        // P.V halves.  They are ordered only through barriers: S_{j+2}
-        // overwrites the buffer of tile j-1, so it waits for the release of
-        // tile j-1's stage (both P.V halves of tile j-1 complete).
-        if (lane == 0 && n_kv > 0) {
+        // S_{j+2} = Q K_{j+2}^T (4 MMAs, N = 128).  The whole warp runs the
+        // loop and one elected lane issues (see warp_mma_bf16_ss).  Issuers
+        // are ordered only through barriers: S_{j+2} overwrites the buffer of
+        // tile j-1, so it waits for the release of tile j-1's stage (both
+        // P.V halves of tile j-1 complete).
+        if (n_kv > 0) {
             constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, false, false);
-            // Shared-memory descriptors, built once into registers (a K step
-            // of 16 adds 32 bytes = 2 in a K-major row; stage st adds
-            // st * 16 KiB >> 4).  The loop is unrolled by 12 = lcm(3 buffers,
-            // 4 stages) so buffers and stages are compile-time constants.
+            // Descriptors as base + compile-time offsets: a K step of 16 adds
+            // 32 bytes (2 in the descriptor) in a K-major row, a stage adds
+            // 16 KiB.  The loop is unrolled by 12 = lcm(3 buffers, 6 stages)
+            // so buffer and stage are constants.
             constexpr uint64_t kTileDesc = kTileBytes >> 4;
             const uint64_t q_desc = smem_desc_sw128(smem_u32(sm.q), 16, 1024);
             const uint64_t k_desc0 = smem_desc_sw128(smem_u32(sm.k[0]), 16, 1024);
-            uint64_t qd[HD / 16], kd[STAGES][HD / 16];
-#pragma unroll
-            for (int kk = 0; kk < HD / 16; ++kk) qd[kk] = q_desc + 2 * kk;
-#pragma unroll
-            for (int st = 0; st < STAGES; ++st)
-#pragma unroll
-                for (int kk = 0; kk < HD / 16; ++kk) kd[st][kk] = k_desc0 + st * kTileDesc + 2 * kk;
-            // S_j into buffer sb = j mod 3 from stage st = j mod 4.
+            // S_j into buffer sb = j mod 3 from stage st = j mod 6.
             auto issue_s = [&](int sb, int st) {
                 const uint32_t d = tmem + 128u * sb;
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk)
-                    mma_bf16_ss(d, qd[kk], kd[st][kk], idesc_s, kk > 0 ? 1u : 0u);
-                mma_commit(&sm.s_full[sb]);
+                    warp_mma_bf16_ss(d, q_desc + 2 * kk, k_desc0 + st * kTileDesc + 2 * kk, idesc_s,
+                                     kk > 0 ? 1u : 0u);
+                warp_commit(&sm.s_full[sb]);
             };
-            bool ok = mbar_wait(&sm.q_full, 0, ab) && mbar_wait(&sm.kv_full[0], 0, ab);
+            bool ok = warp_wait(&sm.q_full, 0, ab) && warp_wait(&sm.kv_full[0], 0, ab);
             if (ok) {
                 tc_fence_after_sync();
                 issue_s(0, 0);
-                if (n_kv > 1 && (ok = mbar_wait(&sm.kv_full[1], 0, ab))) issue_s(1, 1);
+                if (n_kv > 1 && (ok = warp_wait(&sm.kv_full[1], 0, ab))) {
+                    tc_fence_after_sync();
+                    issue_s(1, 1);
+                }
             }
             for (int jb = 0; ok && jb + 2 < n_kv; jb += 12) {
 #pragma unroll
                 for (int u = 0; u < 12; ++u) {
                     const int j = jb + u;  // issue S_{j+2}
                     if (j + 2 >= n_kv) break;
-                    if (!(ok = mbar_wait(&sm.kv_full[(u + 2) % STAGES], ((j + 2) / STAGES) & 1, ab)))
+                    if (!(ok = warp_wait(&sm.kv_full[(u + 2) % STAGES], ((j + 2) / STAGES) & 1, ab)))
                         break;
-                    if (j >= 1 && !(ok = mbar_wait(&sm.kv_empty[(u + STAGES - 1) % STAGES],
+                    if (j >= 1 && !(ok = warp_wait(&sm.kv_empty[(u + STAGES - 1) % STAGES],
                                                    ((j - 1) / STAGES) & 1, ab)))
                         break;
                     tc_fence_after_sync();
@@ -233,28 +232,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             // Always wait (time-bounded, whatever the abort state) until every
-            // MMA this thread issued has completed: tensor memory is released
+            // MMA this warp issued has completed: tensor memory is released
             // and the CTA exits only after that.
-            mma_commit(&sm.drain[0]);
+            warp_commit(&sm.drain[0]);
             mbar_wait_drain(&sm.drain[0], 0);
         }
     } else if (warp >= kMmaPvWarp) {
         // ---------------------------------------------------- PV issuers
         // Warp 10 + h: O_h (+)= P_h,j V_j[keys 64h .. 64h+63], A = P_h in
         // tensor memory (8 columns per 16 keys, at buffer columns 64h..),
-        // B = V tile (MN-major, 16 keys = 2 KiB = 128 per K step).
+        // B = V tile (MN-major, 16 keys = 2 KiB = 128 per K step).  Whole
+        // warp, one elected lane issues.
         const int hf = warp - kMmaPvWarp;
-        if (lane == 0 && n_kv > 0) {
+        if (n_kv > 0) {
             constexpr uint32_t idesc_o = idesc_bf16_f32(BM, HD, false, true);
             constexpr uint64_t kTileDesc = kTileBytes >> 4;
-            const uint64_t v_desc0 = smem_desc_sw128(smem_u32(sm.v[0]), 1024, 1024);
-            uint64_t vd[STAGES][4];
-#pragma unroll
-            for (int st = 0; st < STAGES; ++st)
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    vd[st][kk] = v_desc0 + st * kTileDesc + 128 * (4 * hf + kk);
+            const uint64_t v_desc = smem_desc_sw128(smem_u32(sm.v[0]), 1024, 1024) + 128 * 4 * hf;
             const uint32_t d_o = tmem + kOCol + 64u * hf;
+            const uint32_t p_col = tmem + 64u * hf;
             bool ok = true;
             for (int jb = 0; ok && jb < n_kv; jb += 12) {
                 const uint32_t acc_first = jb > 0 ? 1u : 0u;
@@ -264,26 +259,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (j >= n_kv) break;
                     // P_h,j ready (use j / 3 of its buffer: parity (u / 3) & 1
                     // since jb / 3 is even) and V_j resident.
-                    if (!(ok = mbar_wait(&sm.p_full[u % kSBufs][hf], (u / kSBufs) & 1, ab))) break;
-                    if (!(ok = mbar_wait(&sm.kv_full[u % STAGES], (j / STAGES) & 1, ab))) break;
+                    if (!(ok = warp_wait(&sm.p_full[u % kSBufs][hf], (u / kSBufs) & 1, ab))) break;
+                    if (!(ok = warp_wait(&sm.kv_full[u % STAGES], (j / STAGES) & 1, ab))) break;
                     tc_fence_after_sync();
-                    const uint32_t a = tmem + 128u * (u % kSBufs) + 64u * hf;
+                    const uint32_t a = p_col + 128u * (u % kSBufs);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16_ts(d_o, a + 8 * kk, vd[u % STAGES][kk], idesc_o,
-                                    (u > 0 || kk > 0) ? 1u : acc_first);
-                    if (j == n_kv - 1) mma_commit(&sm.o_final);
-                    mma_commit(&sm.kv_empty[u % STAGES]);
+                        warp_mma_bf16_ts(d_o, a + 8 * kk, v_desc + (u % STAGES) * kTileDesc + 128 * kk,
+                                         idesc_o, (u > 0 || kk > 0) ? 1u : acc_first);
+                    if (j == n_kv - 1) warp_commit(&sm.o_final);
+                    warp_commit(&sm.kv_empty[u % STAGES]);
                 }
             }
-            mma_commit(&sm.drain[1 + hf]);
+            warp_commit(&sm.drain[1 + hf]);
             mbar_wait_drain(&sm.drain[1 + hf], 0);
         }
     } else {
         // --------------------------------------------------------- softmax
-        // Half h owns keys [64h, 64h+64) of every tile with its own running
+        // Half h owns keys [64h, 64h+64) of every tile with its own reference
         // maximum m_h, running sum l_h and accumulator O_h; the two halves
         // are combined once, in the epilogue.
+        //
+        // Softmax is unchanged by a common shift of a row's scores, so P may
+        // be taken against any reference m_h that keeps 2^(s c - m_h c)
+        // finite; the running maximum is only one such choice.  A tile is
+        // therefore exponentiated straight against the current m_h (no
+        // maximum pass), and the row checks its own tile sum: only a row
+        // whose sum exceeds 2^16 (its maximum grew by 10 to 16 log2 units or
+        // more, or overflowed) or that has not yet seen a visible key takes
+        // the exact step -- tile maximum, new m_h, O_h and l_h scaled by
+        // 2^((m_old - m_new) c), P recomputed.  Each decision uses only the
+        // row's own visible scores, so a row's result never depends on
+        // another row or on masked keys.
         const int half = warp >> 2;
         const uint32_t lane_base = static_cast<uint32_t>(warp & 3) * 32;
         const int r = static_cast<int>(lane_base) + lane;    // row in tile = TMEM lane
@@ -296,75 +303,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         float l_run = 0.f;
         bool ok = true;
 
-        for (int j = 0; j < n_kv; ++j) {
-            ok = __all_sync(0xffffffffu,
-                            mbar_wait(&sm.s_full[j % kSBufs], (j / kSBufs) & 1, ab));
-            if (!ok) break;
-            tc_fence_after_sync();
-            const uint32_t ts = tl + s_col(j) + 64u * half;
-            uint32_t s0[32], s1[32];
-            tmem_ld32(ts, s0);
-            tmem_ld32(ts + 32, s1);
-            tmem_ld_wait(s0);
-            reg_fence32(s1);
-
-            // In-tile mask: only tiles that reach past the padding length or
-            // the diagonal need it (tile-uniform branch).  Keys with index
-            // >= row_lim get -inf, i.e. weight exactly zero.
-            if ((j * BN + BN > kv_len) || (causal && j * BN + BN - 1 > q0)) {
-                const int lim = row_lim - (j * BN + 64 * half);
+        // Keys at or past `lim` (relative to the half's first key) get -inf:
+        // weight exactly zero.
+        auto mask_scores = [](uint32_t(&a)[32], uint32_t(&b)[32], int lim) {
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    if (c >= lim) s0[c] = f2u(-INFINITY);
-                    if (c + 32 >= lim) s1[c] = f2u(-INFINITY);
-                }
+            for (int c = 0; c < 32; ++c) {
+                if (c >= lim) a[c] = f2u(-INFINITY);
+                if (c + 32 >= lim) b[c] = f2u(-INFINITY);
             }
-
-            // Maximum over this half's 64 scores: four chains of three-input
-            // maxima.
-            float tm0 = fmaxf(u2f(s0[0]), u2f(s0[1])), tm1 = fmaxf(u2f(s0[2]), u2f(s0[3]));
-            float tm2 = fmaxf(u2f(s1[0]), u2f(s1[1])), tm3 = fmaxf(u2f(s1[2]), u2f(s1[3]));
-#pragma unroll
-            for (int c = 4; c < 32; c += 4) {
-                tm0 = fmax3(tm0, u2f(s0[c]), u2f(s0[c + 1]));
-                tm1 = fmax3(tm1, u2f(s0[c + 2]), u2f(s0[c + 3]));
-                tm2 = fmax3(tm2, u2f(s1[c]), u2f(s1[c + 1]));
-                tm3 = fmax3(tm3, u2f(s1[c + 2]), u2f(s1[c + 3]));
-            }
-            const float mx = fmaxf(fmax3(tm0, tm1, tm2), tm3);
-
-            // Running maximum: keep the stale one unless it grew by > 2^8.
-            // Decided per row, so a row's result never depends on another
-            // row's scores; the warp only shares the tensor-memory access
-            // (rows that keep their maximum scale O_h by exactly 1).  While
-            // m_h is still -inf, O_h and l_h are exactly zero and need no
-            // rescale.
-            const float m_new = fmaxf(m_run, mx);
-            const bool grow = m_run != -INFINITY && (m_new - m_run) * C > kRescaleThreshold;
-            const bool rescale = __any_sync(0xffffffffu, grow);
-            float alpha = 1.f;
-            if (m_run == -INFINITY) {
-                m_run = m_new;
-            } else if (grow) {
-                alpha = ex2_approx((m_run - m_new) * C);
-                l_run *= alpha;
-                m_run = m_new;
-            }
-            const float mc = m_run == -INFINITY ? 0.f : m_run * C;
-
-            // P = 2^(s*c - m*c) in bf16, written over this half's first 32
-            // score columns (column c holds keys 2c, 2c+1 of the half).
-            // Packed fp32x2 FMA / add (one instruction per two scores) keep
-            // the instruction count -- and the issue slots taken from the MMA
-            // warp on the same sub-partition -- down.
+        };
+        // P = 2^(s c - mc) in bf16 (column c of the packed tile holds keys
+        // 2c, 2c+1 of the half) and the fp32 row sum of P.  Packed fp32x2
+        // FMA / add (one instruction per two scores) keep the instruction
+        // count -- and the issue slots taken from the MMA warps -- down.
+        auto exp_tile = [C](const uint32_t(&a)[32], const uint32_t(&b)[32], float mc,
+                            uint32_t(&pk)[32]) -> float {
             const uint64_t c2 = f32x2_pack(C, C), nmc2 = f32x2_pack(-mc, -mc);
             uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
-            uint32_t pk[32];
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
                 float x0, x1, x2, x3;
-                f32x2_unpack(fma_f32x2(f32x2_pack(u2f(s0[2 * c]), u2f(s0[2 * c + 1])), c2, nmc2), x0, x1);
-                f32x2_unpack(fma_f32x2(f32x2_pack(u2f(s1[2 * c]), u2f(s1[2 * c + 1])), c2, nmc2), x2, x3);
+                f32x2_unpack(fma_f32x2(f32x2_pack(u2f(a[2 * c]), u2f(a[2 * c + 1])), c2, nmc2), x0, x1);
+                f32x2_unpack(fma_f32x2(f32x2_pack(u2f(b[2 * c]), u2f(b[2 * c + 1])), c2, nmc2), x2, x3);
                 const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
                 const float e2 = ex2_approx(x2), e3 = ex2_approx(x3);
                 acc2[c & 1] = add_f32x2(acc2[c & 1], f32x2_pack(e0, e1));
@@ -372,43 +332,99 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pk[c] = pack_bf16x2(e0, e1);
                 pk[16 + c] = pack_bf16x2(e2, e3);
             }
-            tmem_st32(ts, pk);
-            {
-                float u0, u1;
-                f32x2_unpack(add_f32x2(add_f32x2(acc2[0], acc2[1]), add_f32x2(acc2[2], acc2[3])), u0, u1);
-                l_run += u0 + u1;
-            }
-
-            if (rescale) {
-                // O_h must hold exactly sum_{j' < j} P V: wait for the release
-                // of tile j-1's stage (committed after both products of tile
-                // j-1).  Its next release needs P_j, which this thread has not
-                // yet published, so the parity cannot alias.
-                ok = __all_sync(0xffffffffu, mbar_wait(&sm.kv_empty[(j - 1) % STAGES],
-                                                       ((j - 1) / STAGES) & 1, ab));
-                if (!ok) {
-                    tmem_st_wait();  // no tensor-memory store may outlive the CTA
-                    break;
-                }
-                tc_fence_after_sync();
-                uint32_t o0[32], o1[32];
-                tmem_ld32(to, o0);
-                tmem_ld32(to + 32, o1);
-                tmem_ld_wait(o0);
-                reg_fence32(o1);
+            float u0, u1;
+            f32x2_unpack(add_f32x2(add_f32x2(acc2[0], acc2[1]), add_f32x2(acc2[2], acc2[3])), u0, u1);
+            return u0 + u1;
+        };
+        // Row maximum of the half's 64 scores: four chains of three-input max.
+        auto row_max = [](const uint32_t(&a)[32], const uint32_t(&b)[32]) -> float {
+            float t0 = fmaxf(u2f(a[0]), u2f(a[1])), t1 = fmaxf(u2f(a[2]), u2f(a[3]));
+            float t2 = fmaxf(u2f(b[0]), u2f(b[1])), t3 = fmaxf(u2f(b[2]), u2f(b[3]));
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    o0[c] = f2u(u2f(o0[c]) * alpha);
-                    o1[c] = f2u(u2f(o1[c]) * alpha);
-                }
-                tmem_st32(to, o0);
-                tmem_st32(to + 32, o1);
+            for (int c = 4; c < 32; c += 4) {
+                t0 = fmax3(t0, u2f(a[c]), u2f(a[c + 1]));
+                t1 = fmax3(t1, u2f(a[c + 2]), u2f(a[c + 3]));
+                t2 = fmax3(t2, u2f(b[c]), u2f(b[c + 1]));
+                t3 = fmax3(t3, u2f(b[c + 2]), u2f(b[c + 3]));
             }
+            return fmaxf(fmax3(t0, t1, t2), t3);
+        };
+
+        for (int j = 0; j < n_kv; ++j) {
+            ok = __all_sync(0xffffffffu,
+                            mbar_wait(&sm.s_full[j % kSBufs], (j / kSBufs) & 1, ab));
+            if (!ok) break;
+            tc_fence_after_sync();
+            const uint32_t ts = tl + s_col(j) + 64u * half;
+            // In-tile mask only on tiles that reach past the padding length
+            // or the diagonal (tile-uniform branch).
+            const bool edge = (j * BN + BN > kv_len) || (causal && j * BN + BN - 1 > q0);
+            const int lim = row_lim - (j * BN + 64 * half);
+
+            uint32_t pk[32];
+            float lt = 0.f;
+            bool need = true;  // tile 0: no row has a reference yet
+            if (j > 0) {
+                uint32_t s0[32], s1[32];
+                tmem_ld32(ts, s0);
+                tmem_ld32(ts + 32, s1);
+                tmem_ld_wait(s0);
+                reg_fence32(s1);
+                if (edge) mask_scores(s0, s1, lim);
+                lt = exp_tile(s0, s1, m_run == -INFINITY ? 0.f : m_run * C, pk);
+                need = m_run == -INFINITY || !(lt <= kTileSumLimit);
+            }
+            if (__any_sync(0xffffffffu, need)) {
+                // Exact step for the rows that need it (scores reloaded from
+                // tensor memory: P has not been written over them yet).
+                uint32_t s0[32], s1[32];
+                tmem_ld32(ts, s0);
+                tmem_ld32(ts + 32, s1);
+                tmem_ld_wait(s0);
+                reg_fence32(s1);
+                if (edge) mask_scores(s0, s1, lim);
+                float alpha = 1.f;
+                if (need) {
+                    const float m_new = fmaxf(m_run, row_max(s0, s1));
+                    if (m_run != -INFINITY) alpha = ex2_approx((m_run - m_new) * C);
+                    m_run = m_new;  // stays -inf while every key so far is masked
+                    l_run *= alpha;
+                    lt = exp_tile(s0, s1, m_run == -INFINITY ? 0.f : m_run * C, pk);
+                }
+                if (__any_sync(0xffffffffu, alpha != 1.f)) {
+                    // O_h must hold exactly sum_{j' < j} P V: wait for the
+                    // release of tile j-1's stage (committed after both
+                    // products of tile j-1; j >= 1 here since no row has a
+                    // finite reference at tile 0).  Its next release needs
+                    // P_j, which this thread has not yet published, so the
+                    // parity cannot alias.  Rows with alpha == 1 are
+                    // rewritten unchanged.
+                    ok = __all_sync(0xffffffffu, mbar_wait(&sm.kv_empty[(j - 1) % STAGES],
+                                                           ((j - 1) / STAGES) & 1, ab));
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    uint32_t o0[32], o1[32];
+                    tmem_ld32(to, o0);
+                    tmem_ld32(to + 32, o1);
+                    tmem_ld_wait(o0);
+                    reg_fence32(o1);
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        o0[c] = f2u(u2f(o0[c]) * alpha);
+                        o1[c] = f2u(u2f(o1[c]) * alpha);
+                    }
+                    tmem_st32(to, o0);
+                    tmem_st32(to + 32, o1);
+                }
+            }
+            tmem_st32(ts, pk);
+            l_run += lt;
             tmem_st_wait();
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.p_full[j % kSBufs][half]);
         }
+        if (!ok) tmem_st_wait();  // no tensor-memory store may outlive the CTA
 
         // ----------------------------------------------------------- epilogue
         // out = (O_A w_A + O_B w_B) / (l_A w_A + l_B w_B), w_h = 2^((m_h - M) c),

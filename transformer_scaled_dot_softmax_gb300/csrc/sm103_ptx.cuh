@@ -316,6 +316,51 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
         : "memory");
 }
 
+// Warp-converged forms: all 32 lanes execute the call, `elect.sync` picks one
+// lane, and only that lane issues.  For a given converged warp the same lane
+// is elected every time, so a warp_commit tracks exactly the MMAs issued by
+// the warp_mma calls before it.  Measured on GB300, one lane issuing from a
+// converged warp with descriptors formed as base + constant keeps an M=128
+// N=64 stream at ~33 cycles per MMA (the tensor core's own rate), where the
+// same stream issued inside `if (lane == 0)` needs 50-77 cycles per MMA.
+__device__ __forceinline__ void warp_mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc,
+                                                 uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void warp_mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem,
+                                                 uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void warp_commit(uint64_t *bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+// All lanes wait; the warp leaves converged with one common verdict.
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const AbortState &ab) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, ab));
+}
+
 // ----------------------------------------------------------------- numeric
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
