@@ -134,6 +134,9 @@ mha_status run_attention_bf16(const void *q, const void *k, const void *v, void 
     p.o_stride_h = o_sh;
     p.o_stride_t = o_st;
     p.num_qblocks = (T_q + mha::kAttnRowsPerCta - 1) / mha::kAttnRowsPerCta;
+    const long long items = BH * p.num_qblocks;
+    if (items >= (1ll << 30)) return MHA_ERR_UNSUPPORTED;
+    p.total_items = static_cast<int>(items);
     p.status = status_dev;
     return launch_status(mha::launch_attn_bf16(tq, tk, tv, p, stream), "attention launch");
 }

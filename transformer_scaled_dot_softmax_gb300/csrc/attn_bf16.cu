@@ -4,15 +4,19 @@
 // ("Attention Is All You Need" (azimuth.plus), "The idea: every word queries
 // every word"; aiany.app Step 6, matrix form S = QK^T/sqrt(d_k),
 // A = softmax(S), Z = AV) without ever writing S or A to global memory: the
-// softmax is taken online over 128-key tiles (running row maximum m and row
-// sum l, rescaling the partial output when m grows), which reaches the same
+// softmax is taken online over 128-key tiles (running reference maximum m and
+// row sum l, the partial output rescaled when m moves), which reaches the same
 // result up to rounding order.
 //
-// One CTA owns one 128-row query tile of one (b, h) and streams the visible
-// K/V tiles through shared memory.  Warp roles:
+// Work item = one 128-row query tile of one (b, h).  The kernel is persistent:
+// one CTA per SM walks a static list of items (longest first, dealt to the
+// CTAs in snake order so every CTA gets the same number of key tiles), and
+// every role runs ahead into the next item as soon as its resources free up,
+// so loads, score products and the output of consecutive items overlap.
+// Warp roles (16 warps):
 //
-//   warp 8      TMA producer: Q once; K_j and V_j together into a 6-stage
-//               ring (one barrier per stage for both tiles).
+//   warp 8      TMA producer: Q of each item into one of two Q buffers; K_j and
+//               V_j together into a 5-stage ring (one barrier per stage).
 //   warp 9      issues S_j = Q K_j^T (tcgen05.mma kind::f16, M=128 N=128,
 //               fp32 accumulator in tensor memory).
 //   warps 10,11 issue O_A += P_A,j V_j and O_B += P_B,j V_j for key halves
@@ -23,31 +27,37 @@
 //               thread loads its 64 scores, applies the causal / key-padding
 //               mask in-tile (masked score = -inf, i.e. exactly zero weight:
 //               aiany.app Step 10; notebook chapter "Masked Attention in the
-//               Decoder"), keeps its own running maximum m_h and sum l_h, and
-//               writes P_h = bf16(2^(s*c - m_h*c)) back over its scores.
+//               Decoder"), keeps its own reference maximum m_h and sum l_h,
+//               and writes P_h = bf16(2^(s*c - m_h*c)) back over its scores.
+//   warps 12-15 output: once an item's products are complete, combine the
+//               halves, normalise, store, and hand the accumulators back.
 //
 // Splitting the row over two halves with their own maxima, sums and
-// accumulators is exact: the epilogue combines them as
+// accumulators is exact: the output is
 //   out = (O_A 2^((m_A-M)c) + O_B 2^((m_B-M)c)) / (l_A 2^((m_A-M)c) + l_B 2^((m_B-M)c)),
 // M = max(m_A, m_B).  The halves never wait for each other inside the loop.
 //
-// Why three MMA warps: one thread can issue a tcgen05.mma only every ~60-80
-// cycles, while an N = 64 product needs ~32 cycles of tensor-core time, and
-// that thread also loses issue slots to the busy softmax warps on its SM
-// sub-partition.  Spread over three issuers (descriptors precomputed in
-// registers, loops unrolled so indices are constants) the tensor cores see a
-// steady stream.
+// MMA issue: one thread can issue a tcgen05.mma only every ~50-80 cycles
+// when it runs alone inside `if (lane == 0)`, while an N = 64 product needs
+// ~32 cycles of tensor-core time; issued by an elected lane of a converged
+// warp with descriptors formed as base + constant, the rate matches the
+// tensor core.  Three issuing warps keep S and the two P.V halves
+// independent of each other.
 //
-// Score tiles rotate through three tensor-memory buffers (S_j in buffer
-// j mod 3): while the softmax works on S_j, S_{j+1} is ready and S_{j+2} is
-// being computed.  Issuers are ordered only through barriers:
+// Score tiles rotate through three tensor-memory buffers (global tile g of
+// the CTA in buffer g mod 3): while the softmax works on S_g, S_{g+1} is
+// ready and S_{g+2} is being computed.  Issuers are ordered only through
+// barriers:
 //   S ready (per buffer)           S issuer -> softmax,
 //   P_h ready (per buffer, half)   softmax half h -> PV issuer h,
 //   stage released (count 2)      both PV issuers -> TMA producer, S issuer
-//                                  (S_{j+2} overwrites tile j-1's buffer, so
-//                                  it waits for tile j-1's release) and a
+//                                  (S_g overwrites tile g-3's buffer, so it
+//                                  waits for tile g-3's release) and a
 //                                  softmax that must rescale O_h,
-//   output final (count 2)         both PV issuers -> epilogue.
+//   Q released (per Q buffer)      S issuer -> TMA producer,
+//   output final (count 2)         both PV issuers -> output warps,
+//   row statistics (count 8)      softmax -> output warps, and back,
+//   accumulators free (count 4)    output warps -> PV issuers.
 // A buffer's next use needs its current use to be consumed, so no barrier
 // can run two phases ahead of its waiter.
 //
@@ -69,44 +79,74 @@
 namespace mha {
 namespace {
 
-constexpr int BM = 128;        // query rows per CTA
-constexpr int BN = 128;        // keys per tile
+constexpr int BM = kAttnRowsPerCta;  // query rows per item
+constexpr int BN = 128;              // keys per tile
 constexpr int HD = kAttnHeadDim;
-constexpr int STAGES = 6;      // K/V ring depth
-static_assert(12 % STAGES == 0, "the main loops are unrolled by 12");
-constexpr int kSBufs = 3;      // score buffers in tensor memory
-constexpr int kThreads = 384;  // 8 softmax warps + load warp + 3 MMA warps
+constexpr int STAGES = 5;            // K/V ring depth
+constexpr int kSBufs = 3;            // score buffers in tensor memory
+constexpr int kThreads = 512;        // 8 softmax + load + 3 MMA + 4 output warps
 constexpr int kSoftmaxWarps = 8;
 constexpr int kLoadWarp = 8;
-constexpr int kMmaSWarp = 9;   // issues S = Q K^T
-constexpr int kMmaPvWarp = 10; // warps 10, 11 issue PV for key halves A, B
+constexpr int kMmaSWarp = 9;         // issues S = Q K^T
+constexpr int kMmaPvWarp = 10;       // warps 10, 11 issue PV for key halves A, B
+constexpr int kOutWarp = 12;         // warps 12-15: output
 constexpr uint32_t kTileBytes = BM * HD * 2;  // 16 KiB, one 128 x 64 bf16 tile
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 384;  // O_A [384,448), O_B [448,512)
 constexpr float kTileSumLimit = 65536.0f;  // 2^16: a tile sum above it takes the exact step
 
-__device__ __forceinline__ uint32_t s_col(int j) { return 128u * static_cast<uint32_t>(j % kSBufs); }
-
 struct __align__(1024) SmemAttn {
-    uint8_t q[kTileBytes];
+    uint8_t q[2][kTileBytes];
     uint8_t k[STAGES][kTileBytes];
     uint8_t v[STAGES][kTileBytes];
-    float red_m[2][BM];  // [column half][row]: final running maximum
-    float red_l[2][BM];  // [column half][row]: final running sum
-    uint64_t q_full;
+    float red_m[2][BM];  // [column half][row]: reference maximum at the end of an item
+    float red_l[2][BM];  // [column half][row]: row sum at the end of an item
+    uint64_t q_full[2];
+    uint64_t q_empty[2];
     uint64_t kv_full[STAGES];
     uint64_t kv_empty[STAGES];
     uint64_t s_full[kSBufs];
     uint64_t p_full[kSBufs][2];  // [buffer][column half]
-    uint64_t l_ready;
-    uint64_t o_final;
-    uint64_t drain[3];  // one per MMA-issuing warp
+    uint64_t ml_full;            // row statistics written (8 softmax warps)
+    uint64_t ml_free;            // row statistics read (4 output warps)
+    uint64_t o_final;            // both P.V halves of an item complete
+    uint64_t o_free;             // accumulators read (4 output warps)
+    uint64_t drain[3];           // one per MMA-issuing warp
     uint32_t tmem_base;
     int abort_flag;
 };
 
 __device__ __forceinline__ float u2f(uint32_t x) { return __uint_as_float(x); }
 __device__ __forceinline__ uint32_t f2u(float x) { return __float_as_uint(x); }
+
+// Geometry of one work item.  Items are numbered longest first (query block
+// qb from the last down, then (b, h)); round t of the walk gives CTA c the
+// item t*G + c (t even) or t*G + G-1-c (t odd).
+struct Item {
+    int bh, b, hh, q0;
+    int kv_len;  // keys [0, kv_len) exist for this batch (padding)
+    int n_kv;    // key tiles to visit
+};
+
+__device__ __forceinline__ int item_index(int t, int c, int G) {
+    return t * G + ((t & 1) ? (G - 1 - c) : c);
+}
+
+__device__ __forceinline__ Item make_item(const AttnParams &p, int k) {
+    Item it;
+    const int BH = p.B * p.H;
+    const int qb = p.num_qblocks - 1 - k / BH;
+    it.bh = k - (k / BH) * BH;
+    it.b = it.bh / p.H;
+    it.hh = it.bh - it.b * p.H;
+    it.q0 = qb * BM;
+    int kv_len = p.Tk;
+    if ((p.mask & kMaskPaddingBit) && p.key_lens) kv_len = min(max(p.key_lens[it.b], 0), p.Tk);
+    it.kv_len = kv_len;
+    const int kv_end = (p.mask & kMaskCausalBit) ? min(kv_len, min(it.q0 + BM, p.Tq)) : kv_len;
+    it.n_kv = (kv_end + BN - 1) / BN;
+    return it;
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q,
@@ -118,21 +158,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int bh = blockIdx.x;
-    const int qb = p.num_qblocks - 1 - static_cast<int>(blockIdx.y);  // longest first
-    const int b = bh / p.H;
-    const int hh = bh - b * p.H;
-    const int q0 = qb * BM;
+    const int G = static_cast<int>(gridDim.x);
+    const int cta = static_cast<int>(blockIdx.x);
+    const int total = p.total_items;
     const bool causal = (p.mask & kMaskCausalBit) != 0;
 
-    // Visible key range of the query tile: keys [0, kv_end).
-    int kv_len = p.Tk;
-    if ((p.mask & kMaskPaddingBit) && p.key_lens) kv_len = min(max(p.key_lens[b], 0), p.Tk);
-    const int kv_end = causal ? min(kv_len, min(q0 + BM, p.Tq)) : kv_len;
-    const int n_kv = (kv_end + BN - 1) / BN;
-
     if (threadIdx.x == 0) {
-        mbar_init(&sm.q_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.q_full[i], 1);
+            mbar_init(&sm.q_empty[i], 1);
+        }
         for (int i = 0; i < STAGES; ++i) {
             mbar_init(&sm.kv_full[i], 1);
             mbar_init(&sm.kv_empty[i], 2);  // one commit per PV issuer
@@ -142,8 +177,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sm.p_full[i][0], kSoftmaxWarps / 2);  // one arrival per warp of a half
             mbar_init(&sm.p_full[i][1], kSoftmaxWarps / 2);
         }
-        mbar_init(&sm.l_ready, kSoftmaxWarps);
-        mbar_init(&sm.o_final, 2);          // one commit per PV issuer
+        mbar_init(&sm.ml_full, kSoftmaxWarps);
+        mbar_init(&sm.ml_free, 4);
+        mbar_init(&sm.o_final, 2);  // one commit per PV issuer
+        mbar_init(&sm.o_free, 4);
         for (int i = 0; i < 3; ++i) mbar_init(&sm.drain[i], 1);
         sm.abort_flag = 0;
         fence_barrier_init();
@@ -163,122 +200,137 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = sm.tmem_base;
     const AbortState ab{&sm.abort_flag, p.status};
 
+    // Every role walks the same item list and counts, over the items that
+    // have key tiles, the items (v: Q buffer v mod 2 and the per-item
+    // barriers' phases) and the key tiles (g: stage g mod STAGES, score buffer
+    // g mod 3).  Items without key tiles only produce zero rows.
     if (warp == kLoadWarp) {
         // ------------------------------------------------------ TMA producer
-        if (lane == 0 && n_kv > 0) {
-            mbar_arrive_expect_tx(&sm.q_full, kTileBytes);
-            tma_load_3d(&tmap_q, &sm.q_full, sm.q, 0, q0, bh);
-            int issued = 0;
-            for (int j = 0; j < n_kv; ++j) {
-                const int st = j % STAGES;
-                if (j >= STAGES && !mbar_wait(&sm.kv_empty[st], ((j / STAGES) - 1) & 1, ab)) break;
-                mbar_arrive_expect_tx(&sm.kv_full[st], 2 * kTileBytes);
-                tma_load_3d(&tmap_k, &sm.kv_full[st], sm.k[st], 0, j * BN, bh);
-                tma_load_3d(&tmap_v, &sm.kv_full[st], sm.v[st], 0, j * BN, bh);
-                issued = j + 1;
+        if (lane == 0) {
+            int g = 0, v = 0;
+            bool ok = true;
+            for (int t = 0; ok; ++t) {
+                const int k = item_index(t, cta, G);
+                if (k >= total) break;
+                const Item it = make_item(p, k);
+                if (it.n_kv == 0) continue;
+                const int qbuf = v & 1;
+                // Q buffer qbuf last served item v-2: wait until all of its
+                // score products have completed.
+                if (v >= 2 && !(ok = mbar_wait(&sm.q_empty[qbuf], ((v - 2) >> 1) & 1, ab))) break;
+                mbar_arrive_expect_tx(&sm.q_full[qbuf], kTileBytes);
+                tma_load_3d(&tmap_q, &sm.q_full[qbuf], sm.q[qbuf], 0, it.q0, it.bh);
+                ++v;
+                for (int j = 0; j < it.n_kv; ++j, ++g) {
+                    const int st = g % STAGES;
+                    if (g >= STAGES && !(ok = mbar_wait(&sm.kv_empty[st], ((g / STAGES) - 1) & 1, ab)))
+                        break;
+                    mbar_arrive_expect_tx(&sm.kv_full[st], 2 * kTileBytes);
+                    tma_load_3d(&tmap_k, &sm.kv_full[st], sm.k[st], 0, j * BN, it.bh);
+                    tma_load_3d(&tmap_v, &sm.kv_full[st], sm.v[st], 0, j * BN, it.bh);
+                }
             }
             // Let every copy still in flight land before the CTA exits (on the
             // normal path these phases completed long ago).
-            mbar_wait_drain(&sm.q_full, 0);
-            for (int j = max(0, issued - STAGES); j < issued; ++j)
-                mbar_wait_drain(&sm.kv_full[j % STAGES], (j / STAGES) & 1);
+            for (int x = max(0, g - STAGES); x < g; ++x)
+                mbar_wait_drain(&sm.kv_full[x % STAGES], (x / STAGES) & 1);
+            for (int x = max(0, v - 2); x < v; ++x) mbar_wait_drain(&sm.q_full[x & 1], (x >> 1) & 1);
         }
     } else if (warp == kMmaSWarp) {
         // ----------------------------------------------------- S issuer
-        // S_{j+2} = Q K_{j+2}^T (4 MMAs, N = 128).  The whole warp runs the
-        // loop and one elected lane issues (see warp_mma_bf16_ss).  Issuers
-        // are ordered only through barriers: S_{j+2} overwrites the buffer of
-        // tile j-1, so it waits for the release of tile j-1's stage (both
-        // P.V halves of tile j-1 complete).
-        if (n_kv > 0) {
-            constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, false, false);
-            // Descriptors as base + compile-time offsets: a K step of 16 adds
-            // 32 bytes (2 in the descriptor) in a K-major row, a stage adds
-            // 16 KiB.  The loop is unrolled by 12 = lcm(3 buffers, 6 stages)
-            // so buffer and stage are constants.
-            constexpr uint64_t kTileDesc = kTileBytes >> 4;
-            const uint64_t q_desc = smem_desc_sw128(smem_u32(sm.q), 16, 1024);
-            const uint64_t k_desc0 = smem_desc_sw128(smem_u32(sm.k[0]), 16, 1024);
-            // S_j into buffer sb = j mod 3 from stage st = j mod 6.
-            auto issue_s = [&](int sb, int st) {
-                const uint32_t d = tmem + 128u * sb;
+        // S_g = Q K_g^T (4 MMAs, N = 128) into buffer g mod 3.  The whole
+        // warp runs the loop and one elected lane issues (warp_mma_bf16_ss).
+        // S_g overwrites the buffer of tile g-3, so it waits for the release
+        // of tile g-3's stage (both P.V halves of tile g-3 complete; the
+        // release of tile g-3+STAGES needs S_{g+2}, not yet issued, so the
+        // parity cannot alias).
+        constexpr uint32_t idesc_s = idesc_bf16_f32(BM, BN, false, false);
+        // A K step of 16 adds 32 bytes (2 in the descriptor) in a K-major
+        // row; a stage or Q buffer adds 16 KiB.
+        constexpr uint64_t kTileDesc = kTileBytes >> 4;
+        const uint64_t q_desc0 = smem_desc_sw128(smem_u32(sm.q[0]), 16, 1024);
+        const uint64_t k_desc0 = smem_desc_sw128(smem_u32(sm.k[0]), 16, 1024);
+        int g = 0, v = 0;
+        bool ok = true;
+        for (int t = 0; ok; ++t) {
+            const int k = item_index(t, cta, G);
+            if (k >= total) break;
+            const Item it = make_item(p, k);
+            if (it.n_kv == 0) continue;
+            const int qbuf = v & 1;
+            if (!(ok = warp_wait(&sm.q_full[qbuf], (v >> 1) & 1, ab))) break;
+            const uint64_t qd = q_desc0 + static_cast<uint64_t>(qbuf) * kTileDesc;
+            for (int j = 0; j < it.n_kv; ++j, ++g) {
+                const int st = g % STAGES, sb = g % kSBufs;
+                if (!(ok = warp_wait(&sm.kv_full[st], (g / STAGES) & 1, ab))) break;
+                if (g >= kSBufs) {
+                    const int gp = g - kSBufs;
+                    if (!(ok = warp_wait(&sm.kv_empty[gp % STAGES], (gp / STAGES) & 1, ab))) break;
+                }
+                tc_fence_after_sync();
+                const uint32_t d = tmem + 128u * static_cast<uint32_t>(sb);
+                const uint64_t kd = k_desc0 + static_cast<uint64_t>(st) * kTileDesc;
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk)
-                    warp_mma_bf16_ss(d, q_desc + 2 * kk, k_desc0 + st * kTileDesc + 2 * kk, idesc_s,
-                                     kk > 0 ? 1u : 0u);
+                    warp_mma_bf16_ss(d, qd + 2 * kk, kd + 2 * kk, idesc_s, kk > 0 ? 1u : 0u);
                 warp_commit(&sm.s_full[sb]);
-            };
-            bool ok = warp_wait(&sm.q_full, 0, ab) && warp_wait(&sm.kv_full[0], 0, ab);
-            if (ok) {
-                tc_fence_after_sync();
-                issue_s(0, 0);
-                if (n_kv > 1 && (ok = warp_wait(&sm.kv_full[1], 0, ab))) {
-                    tc_fence_after_sync();
-                    issue_s(1, 1);
-                }
             }
-            for (int jb = 0; ok && jb + 2 < n_kv; jb += 12) {
-#pragma unroll
-                for (int u = 0; u < 12; ++u) {
-                    const int j = jb + u;  // issue S_{j+2}
-                    if (j + 2 >= n_kv) break;
-                    if (!(ok = warp_wait(&sm.kv_full[(u + 2) % STAGES], ((j + 2) / STAGES) & 1, ab)))
-                        break;
-                    if (j >= 1 && !(ok = warp_wait(&sm.kv_empty[(u + STAGES - 1) % STAGES],
-                                                   ((j - 1) / STAGES) & 1, ab)))
-                        break;
-                    tc_fence_after_sync();
-                    issue_s((u + 2) % kSBufs, (u + 2) % STAGES);
-                }
-            }
-            // Always wait (time-bounded, whatever the abort state) until every
-            // MMA this warp issued has completed: tensor memory is released
-            // and the CTA exits only after that.
-            warp_commit(&sm.drain[0]);
-            mbar_wait_drain(&sm.drain[0], 0);
+            if (!ok) break;
+            // Every score product of this item is issued: the Q buffer is
+            // free once they complete.
+            warp_commit(&sm.q_empty[qbuf]);
+            ++v;
         }
-    } else if (warp >= kMmaPvWarp) {
+        // Always wait (time-bounded, whatever the abort state) until every
+        // MMA this warp issued has completed: tensor memory is released and
+        // the CTA exits only after that.
+        warp_commit(&sm.drain[0]);
+        mbar_wait_drain(&sm.drain[0], 0);
+    } else if (warp == kMmaPvWarp || warp == kMmaPvWarp + 1) {
         // ---------------------------------------------------- PV issuers
-        // Warp 10 + h: O_h (+)= P_h,j V_j[keys 64h .. 64h+63], A = P_h in
+        // Warp 10 + h: O_h (+)= P_h,g V_g[keys 64h .. 64h+63], A = P_h in
         // tensor memory (8 columns per 16 keys, at buffer columns 64h..),
-        // B = V tile (MN-major, 16 keys = 2 KiB = 128 per K step).  Whole
-        // warp, one elected lane issues.
+        // B = V tile (MN-major, 16 keys = 2 KiB = 128 per K step).  The
+        // first product of an item overwrites O_h, so it waits until the
+        // output warps have read the previous item's accumulators.
         const int hf = warp - kMmaPvWarp;
-        if (n_kv > 0) {
-            constexpr uint32_t idesc_o = idesc_bf16_f32(BM, HD, false, true);
-            constexpr uint64_t kTileDesc = kTileBytes >> 4;
-            const uint64_t v_desc = smem_desc_sw128(smem_u32(sm.v[0]), 1024, 1024) + 128 * 4 * hf;
-            const uint32_t d_o = tmem + kOCol + 64u * hf;
-            const uint32_t p_col = tmem + 64u * hf;
-            bool ok = true;
-            for (int jb = 0; ok && jb < n_kv; jb += 12) {
-                const uint32_t acc_first = jb > 0 ? 1u : 0u;
+        constexpr uint32_t idesc_o = idesc_bf16_f32(BM, HD, false, true);
+        constexpr uint64_t kTileDesc = kTileBytes >> 4;
+        const uint64_t v_desc = smem_desc_sw128(smem_u32(sm.v[0]), 1024, 1024) + 128 * 4 * hf;
+        const uint32_t d_o = tmem + kOCol + 64u * static_cast<uint32_t>(hf);
+        const uint32_t p_col = tmem + 64u * static_cast<uint32_t>(hf);
+        int g = 0, v = 0;
+        bool ok = true;
+        for (int t = 0; ok; ++t) {
+            const int k = item_index(t, cta, G);
+            if (k >= total) break;
+            const Item it = make_item(p, k);
+            if (it.n_kv == 0) continue;
+            if (v >= 1 && !(ok = warp_wait(&sm.o_free, (v - 1) & 1, ab))) break;
+            for (int j = 0; j < it.n_kv; ++j, ++g) {
+                const int st = g % STAGES, sb = g % kSBufs;
+                if (!(ok = warp_wait(&sm.p_full[sb][hf], (g / kSBufs) & 1, ab))) break;
+                if (!(ok = warp_wait(&sm.kv_full[st], (g / STAGES) & 1, ab))) break;
+                tc_fence_after_sync();
+                const uint32_t a = p_col + 128u * static_cast<uint32_t>(sb);
+                const uint64_t vd = v_desc + static_cast<uint64_t>(st) * kTileDesc;
 #pragma unroll
-                for (int u = 0; u < 12; ++u) {
-                    const int j = jb + u;
-                    if (j >= n_kv) break;
-                    // P_h,j ready (use j / 3 of its buffer: parity (u / 3) & 1
-                    // since jb / 3 is even) and V_j resident.
-                    if (!(ok = warp_wait(&sm.p_full[u % kSBufs][hf], (u / kSBufs) & 1, ab))) break;
-                    if (!(ok = warp_wait(&sm.kv_full[u % STAGES], (j / STAGES) & 1, ab))) break;
-                    tc_fence_after_sync();
-                    const uint32_t a = p_col + 128u * (u % kSBufs);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        warp_mma_bf16_ts(d_o, a + 8 * kk, v_desc + (u % STAGES) * kTileDesc + 128 * kk,
-                                         idesc_o, (u > 0 || kk > 0) ? 1u : acc_first);
-                    if (j == n_kv - 1) warp_commit(&sm.o_final);
-                    warp_commit(&sm.kv_empty[u % STAGES]);
-                }
+                for (int kk = 0; kk < 4; ++kk)
+                    warp_mma_bf16_ts(d_o, a + 8 * kk, vd + 128 * kk, idesc_o,
+                                     (j > 0 || kk > 0) ? 1u : 0u);
+                if (j == it.n_kv - 1) warp_commit(&sm.o_final);
+                warp_commit(&sm.kv_empty[st]);
             }
-            warp_commit(&sm.drain[1 + hf]);
-            mbar_wait_drain(&sm.drain[1 + hf], 0);
+            if (!ok) break;
+            ++v;
         }
-    } else {
+        warp_commit(&sm.drain[1 + hf]);
+        mbar_wait_drain(&sm.drain[1 + hf], 0);
+    } else if (warp < kSoftmaxWarps) {
         // --------------------------------------------------------- softmax
         // Half h owns keys [64h, 64h+64) of every tile with its own reference
         // maximum m_h, running sum l_h and accumulator O_h; the two halves
-        // are combined once, in the epilogue.
+        // are combined by the output warps.
         //
         // Softmax is unchanged by a common shift of a row's scores, so P may
         // be taken against any reference m_h that keeps 2^(s c - m_h c)
@@ -294,14 +346,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int half = warp >> 2;
         const uint32_t lane_base = static_cast<uint32_t>(warp & 3) * 32;
         const int r = static_cast<int>(lane_base) + lane;    // row in tile = TMEM lane
-        const int row = q0 + r;                              // query index
         const uint32_t tl = tmem_addr(tmem, lane_base, 0);
         const uint32_t to = tl + kOCol + 64u * half;         // O_h: 64 columns
         const float C = p.scale_log2;
-        const int row_lim = causal ? min(kv_len, row + 1) : kv_len;  // keys < row_lim visible
-        float m_run = -INFINITY;  // -inf until this half has seen a visible key
-        float l_run = 0.f;
-        bool ok = true;
 
         // Keys at or past `lim` (relative to the half's first key) get -inf:
         // weight exactly zero.
@@ -350,128 +397,174 @@ __global__ void __launch_bounds__(kThreads, 1)
             return fmaxf(fmax3(t0, t1, t2), t3);
         };
 
-        for (int j = 0; j < n_kv; ++j) {
-            ok = __all_sync(0xffffffffu,
-                            mbar_wait(&sm.s_full[j % kSBufs], (j / kSBufs) & 1, ab));
-            if (!ok) break;
-            tc_fence_after_sync();
-            const uint32_t ts = tl + s_col(j) + 64u * half;
-            // In-tile mask only on tiles that reach past the padding length
-            // or the diagonal (tile-uniform branch).
-            const bool edge = (j * BN + BN > kv_len) || (causal && j * BN + BN - 1 > q0);
-            const int lim = row_lim - (j * BN + 64 * half);
+        int g = 0, v = 0;
+        bool ok = true;
+        for (int t = 0; ok; ++t) {
+            const int k = item_index(t, cta, G);
+            if (k >= total) break;
+            const Item it = make_item(p, k);
+            if (it.n_kv == 0) continue;
+            const int row = it.q0 + r;  // query index
+            const int row_lim = causal ? min(it.kv_len, row + 1) : it.kv_len;  // keys < row_lim visible
+            float m_run = -INFINITY;  // -inf until this half has seen a visible key
+            float l_run = 0.f;
 
-            uint32_t pk[32];
-            float lt = 0.f;
-            bool need = true;  // tile 0: no row has a reference yet
-            if (j > 0) {
-                uint32_t s0[32], s1[32];
-                tmem_ld32(ts, s0);
-                tmem_ld32(ts + 32, s1);
-                tmem_ld_wait(s0);
-                reg_fence32(s1);
-                if (edge) mask_scores(s0, s1, lim);
-                lt = exp_tile(s0, s1, m_run == -INFINITY ? 0.f : m_run * C, pk);
-                need = m_run == -INFINITY || !(lt <= kTileSumLimit);
-            }
-            if (__any_sync(0xffffffffu, need)) {
-                // Exact step for the rows that need it (scores reloaded from
-                // tensor memory: P has not been written over them yet).
-                uint32_t s0[32], s1[32];
-                tmem_ld32(ts, s0);
-                tmem_ld32(ts + 32, s1);
-                tmem_ld_wait(s0);
-                reg_fence32(s1);
-                if (edge) mask_scores(s0, s1, lim);
-                float alpha = 1.f;
-                if (need) {
-                    const float m_new = fmaxf(m_run, row_max(s0, s1));
-                    if (m_run != -INFINITY) alpha = ex2_approx((m_run - m_new) * C);
-                    m_run = m_new;  // stays -inf while every key so far is masked
-                    l_run *= alpha;
+            for (int j = 0; j < it.n_kv; ++j, ++g) {
+                const int sb = g % kSBufs;
+                ok = __all_sync(0xffffffffu, mbar_wait(&sm.s_full[sb], (g / kSBufs) & 1, ab));
+                if (!ok) break;
+                tc_fence_after_sync();
+                const uint32_t ts = tl + 128u * static_cast<uint32_t>(sb) + 64u * half;
+                // In-tile mask only on tiles that reach past the padding
+                // length or the diagonal (tile-uniform branch).
+                const bool edge =
+                    (j * BN + BN > it.kv_len) || (causal && j * BN + BN - 1 > it.q0);
+                const int lim = row_lim - (j * BN + 64 * half);
+
+                uint32_t pk[32];
+                float lt = 0.f;
+                bool need = true;  // first tile of the item: no row has a reference yet
+                if (j > 0) {
+                    uint32_t s0[32], s1[32];
+                    tmem_ld32(ts, s0);
+                    tmem_ld32(ts + 32, s1);
+                    tmem_ld_wait(s0);
+                    reg_fence32(s1);
+                    if (edge) mask_scores(s0, s1, lim);
                     lt = exp_tile(s0, s1, m_run == -INFINITY ? 0.f : m_run * C, pk);
+                    need = m_run == -INFINITY || !(lt <= kTileSumLimit);
                 }
-                if (__any_sync(0xffffffffu, alpha != 1.f)) {
-                    // O_h must hold exactly sum_{j' < j} P V: wait for the
-                    // release of tile j-1's stage (committed after both
-                    // products of tile j-1; j >= 1 here since no row has a
-                    // finite reference at tile 0).  Its next release needs
-                    // P_j, which this thread has not yet published, so the
-                    // parity cannot alias.  Rows with alpha == 1 are
-                    // rewritten unchanged.
-                    ok = __all_sync(0xffffffffu, mbar_wait(&sm.kv_empty[(j - 1) % STAGES],
-                                                           ((j - 1) / STAGES) & 1, ab));
-                    if (!ok) break;
-                    tc_fence_after_sync();
-                    uint32_t o0[32], o1[32];
-                    tmem_ld32(to, o0);
-                    tmem_ld32(to + 32, o1);
-                    tmem_ld_wait(o0);
-                    reg_fence32(o1);
-#pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        o0[c] = f2u(u2f(o0[c]) * alpha);
-                        o1[c] = f2u(u2f(o1[c]) * alpha);
+                if (__any_sync(0xffffffffu, need)) {
+                    // Exact step for the rows that need it (scores reloaded
+                    // from tensor memory: P has not been written over them).
+                    uint32_t s0[32], s1[32];
+                    tmem_ld32(ts, s0);
+                    tmem_ld32(ts + 32, s1);
+                    tmem_ld_wait(s0);
+                    reg_fence32(s1);
+                    if (edge) mask_scores(s0, s1, lim);
+                    float alpha = 1.f;
+                    if (need) {
+                        const float m_new = fmaxf(m_run, row_max(s0, s1));
+                        if (m_run != -INFINITY) alpha = ex2_approx((m_run - m_new) * C);
+                        m_run = m_new;  // stays -inf while every key so far is masked
+                        l_run *= alpha;
+                        lt = exp_tile(s0, s1, m_run == -INFINITY ? 0.f : m_run * C, pk);
                     }
-                    tmem_st32(to, o0);
-                    tmem_st32(to + 32, o1);
+                    if (__any_sync(0xffffffffu, alpha != 1.f)) {
+                        // O_h must hold exactly sum_{j' < j} P V: wait for
+                        // the release of tile g-1's stage (committed after
+                        // both products of tile g-1; j >= 1 here since no row
+                        // has a finite reference on an item's first tile).
+                        // Its next release needs P_g, which this thread has
+                        // not yet published, so the parity cannot alias.
+                        // Rows with alpha == 1 are rewritten unchanged.
+                        ok = __all_sync(0xffffffffu, mbar_wait(&sm.kv_empty[(g - 1) % STAGES],
+                                                               ((g - 1) / STAGES) & 1, ab));
+                        if (!ok) break;
+                        tc_fence_after_sync();
+                        uint32_t o0[32], o1[32];
+                        tmem_ld32(to, o0);
+                        tmem_ld32(to + 32, o1);
+                        tmem_ld_wait(o0);
+                        reg_fence32(o1);
+#pragma unroll
+                        for (int c = 0; c < 32; ++c) {
+                            o0[c] = f2u(u2f(o0[c]) * alpha);
+                            o1[c] = f2u(u2f(o1[c]) * alpha);
+                        }
+                        tmem_st32(to, o0);
+                        tmem_st32(to + 32, o1);
+                    }
                 }
+                tmem_st32(ts, pk);
+                l_run += lt;
+                tmem_st_wait();
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sm.p_full[sb][half]);
             }
-            tmem_st32(ts, pk);
-            l_run += lt;
-            tmem_st_wait();
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.p_full[j % kSBufs][half]);
-        }
-        if (!ok) tmem_st_wait();  // no tensor-memory store may outlive the CTA
-
-        // ----------------------------------------------------------- epilogue
-        // out = (O_A w_A + O_B w_B) / (l_A w_A + l_B w_B), w_h = 2^((m_h - M) c),
-        // M = max(m_A, m_B); a half that saw no visible key has weight 0.
-        // Half h stores output columns [32h, 32h+32).
-        if (ok) {
+            if (!ok) break;
+            // Row statistics of this item for the output warps, once they have
+            // read the previous item's.
+            if (v >= 1 && !(ok = __all_sync(0xffffffffu, mbar_wait(&sm.ml_free, (v - 1) & 1, ab))))
+                break;
             sm.red_m[half][r] = m_run;
             sm.red_l[half][r] = l_run;
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.l_ready);
-            ok = __all_sync(0xffffffffu, mbar_wait(&sm.l_ready, 0, ab));
+            if (lane == 0) mbar_arrive(&sm.ml_full);
+            ++v;
         }
-        if (ok && n_kv > 0) ok = __all_sync(0xffffffffu, mbar_wait(&sm.o_final, 0, ab));
-        if (ok) {
-            uint32_t oa[32], ob[32];
-            if (n_kv > 0) {
-                tc_fence_after_sync();
-                tmem_ld32(tl + kOCol + 32u * half, oa);
-                tmem_ld32(tl + kOCol + 64u + 32u * half, ob);
+        if (!ok) tmem_st_wait();  // no tensor-memory store may outlive the CTA
+    } else if (warp >= kOutWarp) {
+        // ------------------------------------------------------------ output
+        // Warp 12 + q serves rows 32q .. 32q+31 (tensor-memory lane quadrant
+        // q):
+        //   out = (O_A w_A + O_B w_B) / (l_A w_A + l_B w_B),
+        //   w_h = 2^((m_h - M) c), M = max(m_A, m_B);
+        // a half that saw no visible key has weight 0, a row with no visible
+        // key at all outputs 0.
+        const uint32_t lane_base = static_cast<uint32_t>(warp & 3) * 32;
+        const int r = static_cast<int>(lane_base) + lane;
+        const uint32_t tl = tmem_addr(tmem, lane_base, 0);
+        const float C = p.scale_log2;
+        int v = 0;
+        bool ok = true;
+        for (int t = 0; ok; ++t) {
+            const int k = item_index(t, cta, G);
+            if (k >= total) break;
+            const Item it = make_item(p, k);
+            const int row = it.q0 + r;
+            __nv_bfloat16 *dst = p.o + it.b * p.o_stride_b + it.hh * p.o_stride_h +
+                                 static_cast<long long>(row) * p.o_stride_t;
+            uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+            if (it.n_kv == 0) {
+                if (row < p.Tq) {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) d4[c] = make_uint4(0u, 0u, 0u, 0u);
+                }
+                continue;
+            }
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(&sm.ml_full, v & 1, ab)))) break;
+            const float ma = sm.red_m[0][r], mb = sm.red_m[1][r];
+            const float la = sm.red_l[0][r], lb = sm.red_l[1][r];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.ml_free);
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(&sm.o_final, v & 1, ab)))) break;
+            tc_fence_after_sync();
+            const float M = fmaxf(ma, mb);
+            const float wa = la > 0.f ? ex2_approx((ma - M) * C) : 0.f;
+            const float wb = lb > 0.f ? ex2_approx((mb - M) * C) : 0.f;
+            const float L = la * wa + lb * wb;
+            const float inv = L > 0.f ? 1.0f / L : 0.f;
+            const float fa = wa * inv, fb = wb * inv;
+#pragma unroll
+            for (int part = 0; part < 2; ++part) {
+                uint32_t oa[32], ob[32];
+                tmem_ld32(tl + kOCol + 32u * part, oa);
+                tmem_ld32(tl + kOCol + 64u + 32u * part, ob);
                 tmem_ld_wait(oa);
                 reg_fence32(ob);
-            } else {
+                if (part == 1) {
+                    // O_A and O_B are read: the next item's products may
+                    // overwrite them.
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sm.o_free);
+                }
+                if (row < p.Tq) {
+                    uint32_t packed[16];
 #pragma unroll
-                for (int c = 0; c < 32; ++c) oa[c] = ob[c] = 0u;
+                    for (int c = 0; c < 16; ++c)
+                        packed[c] = pack_bf16x2(u2f(oa[2 * c]) * fa + u2f(ob[2 * c]) * fb,
+                                                u2f(oa[2 * c + 1]) * fa + u2f(ob[2 * c + 1]) * fb);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        d4[4 * part + c] = make_uint4(packed[4 * c], packed[4 * c + 1],
+                                                      packed[4 * c + 2], packed[4 * c + 3]);
+                }
             }
-            if (row < p.Tq) {
-                const float ma = sm.red_m[0][r], mb = sm.red_m[1][r];
-                const float la = sm.red_l[0][r], lb = sm.red_l[1][r];
-                const float M = fmaxf(ma, mb);
-                const float wa = la > 0.f ? ex2_approx((ma - M) * C) : 0.f;
-                const float wb = lb > 0.f ? ex2_approx((mb - M) * C) : 0.f;
-                const float L = la * wa + lb * wb;
-                const float inv = L > 0.f ? 1.0f / L : 0.f;
-                const float fa = wa * inv, fb = wb * inv;
-                uint32_t packed[16];
-#pragma unroll
-                for (int c = 0; c < 16; ++c)
-                    packed[c] = pack_bf16x2(u2f(oa[2 * c]) * fa + u2f(ob[2 * c]) * fb,
-                                            u2f(oa[2 * c + 1]) * fa + u2f(ob[2 * c + 1]) * fb);
-                __nv_bfloat16 *dst = p.o + b * p.o_stride_b + hh * p.o_stride_h +
-                                     static_cast<long long>(row) * p.o_stride_t + 32 * half;
-                uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    d4[c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2],
-                                       packed[4 * c + 3]);
-            }
+            ++v;
         }
     }
 
@@ -492,7 +585,13 @@ cudaError_t launch_attn_bf16(const CUtensorMap &tq, const CUtensorMap &tk,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    dim3 grid(static_cast<unsigned>(p.B * p.H), static_cast<unsigned>(p.num_qblocks));
+    // One persistent CTA per SM (fewer if there are fewer items).
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return e;
+    const int grid = p.total_items < sms ? p.total_items : sms;
+    if (grid <= 0) return cudaSuccess;
     attn_fwd_bf16_kernel<<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
     return cudaGetLastError();
 }

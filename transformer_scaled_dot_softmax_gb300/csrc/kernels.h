@@ -19,10 +19,11 @@ struct AttnParams {
     const int32_t *key_lens;
     __nv_bfloat16 *o;  // output; element (b, h, t, c) at o + b*sb + h*sh + t*st + c
     long long o_stride_b, o_stride_h, o_stride_t;
-    int num_qblocks;   // ceil(Tq / rows per CTA)
+    int num_qblocks;   // ceil(Tq / rows per item)
+    int total_items;   // B * H * num_qblocks work items (query tiles)
     int *status;
 };
-constexpr int kAttnRowsPerCta = 128;  // one 128-row query tile per CTA
+constexpr int kAttnRowsPerCta = 128;  // one work item = one 128-row query tile
 constexpr int kAttnHeadDim = 64;
 
 // q, k, v: head-split (B, H, T, 64) bf16 tensors described by 3-D TMA maps
