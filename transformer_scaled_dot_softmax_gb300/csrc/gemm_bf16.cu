@@ -6,16 +6,22 @@
 // Concat(head_1..head_h) W^O: muhitai.com "Multi-Head Attention Formula").
 //
 // One launch runs up to three independent problems (the Q, K and V
-// projections share a launch); a CTA owns one 128 x 128 output tile:
+// projections share a launch), cut into 128 x 128 output tiles.  The kernel
+// is persistent: one CTA per SM takes tiles c, c + G, c + 2G, ... (all tiles
+// of a launch have the same K, so round robin balances them), and the
+// accumulator is double-buffered in tensor memory, so the epilogue of one
+// tile overlaps the main loop of the next:
 //
 //   warp 0      TMA producer: A tile (128 rows x 64 k, K-major) and B tile
 //               (64 k x 128 n of W, N contiguous = MN-major) per k-block,
-//               4-stage ring.
-//   warp 1      MMA issuer: tcgen05.mma kind::f16, M=128 N=128 K=16,
-//               fp32 accumulator in 128 tensor-memory columns.
-//   warps 2-5   epilogue: tensor memory -> registers -> bf16 -> global.  In
-//               head-split mode column n = head*64 + c of row m = b*T + t is
-//               stored at ((b*H + head)*T + t)*64 + c, i.e. straight into the
+//               6-stage ring.
+//   warp 1      MMA issuer: tcgen05.mma kind::f16, M=128 N=128 K=16, fp32
+//               accumulators in two 128-column tensor-memory buffers; the
+//               whole warp runs the loop and one elected lane issues.
+//   warps 2-5   epilogue: tensor memory -> registers (the buffer is handed
+//               back as soon as it is read) -> bf16 -> global.  In head-split
+//               mode column n = head*64 + c of row m = b*T + t is stored at
+//               ((b*H + head)*T + t)*64 + c, i.e. straight into the
 //               (B, H, T, 64) layout attention reads -- the view/transpose of
 //               the head split costs no extra pass over memory.
 #include <cuda_bf16.h>
@@ -27,22 +33,38 @@ namespace mha {
 namespace {
 
 constexpr int BM = kGemmBM, BN = kGemmBN, BK = kGemmBK;
-constexpr int STAGES = 4;
+constexpr int STAGES = 6;
 constexpr int kThreads = 192;
 constexpr uint32_t kABytes = BM * BK * 2;  // 16 KiB
 constexpr uint32_t kBBytes = BK * BN * 2;  // 16 KiB: two 64-column blocks of 8 KiB
-constexpr uint32_t kTmemCols = 128;
+constexpr uint32_t kTmemCols = 2 * BN;     // two accumulators
 
 struct __align__(1024) SmemGemm {
     uint8_t a[STAGES][kABytes];
     uint8_t b[STAGES][kBBytes];
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
-    uint64_t acc_full;
+    uint64_t acc_full[2];   // MMA -> epilogue (commit)
+    uint64_t acc_empty[2];  // epilogue -> MMA (4 warps)
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
 };
+
+// Problem and tile coordinates of launch-wide tile `tile`.
+struct Tile {
+    int pi, tm, tn;
+};
+__device__ __forceinline__ Tile locate(const GemmParams &p, int tile) {
+    Tile t;
+    int pi = 0;
+    while (pi + 1 < p.num_problems && tile >= p.prob[pi + 1].tile_start) ++pi;
+    const int local = tile - p.prob[pi].tile_start;
+    t.pi = pi;
+    t.tm = local / p.prob[pi].tiles_n;
+    t.tn = local - t.tm * p.prob[pi].tiles_n;
+    return t;
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap a0, const __grid_constant__ CUtensorMap a1,
@@ -54,25 +76,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-
-    // Which problem and tile.
-    const int tile = blockIdx.x;
-    int pi = 0;
-    while (pi + 1 < p.num_problems && tile >= p.prob[pi + 1].tile_start) ++pi;
-    const GemmProblem &pr = p.prob[pi];
-    const int local = tile - pr.tile_start;
-    const int tm = local / pr.tiles_n;
-    const int tn = local - tm * pr.tiles_n;
-    const int num_k = (pr.K + BK - 1) / BK;
-    const CUtensorMap *ta = pi == 0 ? &a0 : (pi == 1 ? &a1 : &a2);
-    const CUtensorMap *tb = pi == 0 ? &b0 : (pi == 1 ? &b1 : &b2);
+    const int G = static_cast<int>(gridDim.x);
+    const int num_k = (p.prob[0].K + BK - 1) / BK;  // the same K for every problem of a launch
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < STAGES; ++i) {
             mbar_init(&sm.full[i], 1);
             mbar_init(&sm.empty[i], 1);
         }
-        mbar_init(&sm.acc_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.acc_full[i], 1);
+            mbar_init(&sm.acc_empty[i], 4);
+        }
         mbar_init(&sm.drain, 1);
         sm.abort_flag = 0;
         fence_barrier_init();
@@ -82,8 +97,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_relinquish();
     }
     if (warp == 0 && lane == 0) {
-        prefetch_tensormap(ta);
-        prefetch_tensormap(tb);
+        prefetch_tensormap(&a0);
+        prefetch_tensormap(&b0);
+        if (p.num_problems > 1) {
+            prefetch_tensormap(&a1);
+            prefetch_tensormap(&b1);
+        }
+        if (p.num_problems > 2) {
+            prefetch_tensormap(&a2);
+            prefetch_tensormap(&b2);
+        }
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -92,83 +115,123 @@ __global__ void __launch_bounds__(kThreads, 1)
     const AbortState ab{&sm.abort_flag, p.status};
 
     if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
         if (lane == 0) {
-            int issued = 0;
-            for (int kb = 0; kb < num_k; ++kb) {
-                const int st = kb % STAGES;
-                if (kb >= STAGES && !mbar_wait(&sm.empty[st], ((kb / STAGES) - 1) & 1, ab)) break;
-                mbar_arrive_expect_tx(&sm.full[st], kABytes + kBBytes);
-                tma_load_2d(ta, &sm.full[st], sm.a[st], kb * BK, tm * BM);
-                tma_load_3d(tb, &sm.full[st], sm.b[st], 0, kb * BK, tn * (BN / 64));
-                issued = kb + 1;
+            int kg = 0;  // k-blocks issued over all tiles of this CTA
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += G) {
+                const Tile t = locate(p, tile);
+                const CUtensorMap *ta = t.pi == 0 ? &a0 : (t.pi == 1 ? &a1 : &a2);
+                const CUtensorMap *tb = t.pi == 0 ? &b0 : (t.pi == 1 ? &b1 : &b2);
+                for (int kb = 0; kb < num_k; ++kb, ++kg) {
+                    const int st = kg % STAGES;
+                    if (kg >= STAGES && !(ok = mbar_wait(&sm.empty[st], ((kg / STAGES) - 1) & 1, ab)))
+                        break;
+                    mbar_arrive_expect_tx(&sm.full[st], kABytes + kBBytes);
+                    tma_load_2d(ta, &sm.full[st], sm.a[st], kb * BK, t.tm * BM);
+                    tma_load_3d(tb, &sm.full[st], sm.b[st], 0, kb * BK, t.tn * (BN / 64));
+                }
             }
             // Let every copy still in flight land before the CTA exits.
-            for (int kb = max(0, issued - STAGES); kb < issued; ++kb)
-                mbar_wait_drain(&sm.full[kb % STAGES], (kb / STAGES) & 1);
+            for (int x = max(0, kg - STAGES); x < kg; ++x)
+                mbar_wait_drain(&sm.full[x % STAGES], (x / STAGES) & 1);
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, false, true);
-            bool ok = true;
-            for (int kb = 0; kb < num_k; ++kb) {
-                const int st = kb % STAGES;
-                if (!(ok = mbar_wait(&sm.full[st], (kb / STAGES) & 1, ab))) break;
+        // ----------------------------------------------------- MMA issuer
+        // Accumulator i % 2 for the CTA's i-th tile; it is reused once the
+        // epilogue has read tile i-2 out of it.  Descriptors as base +
+        // constant: a K step of 16 adds 32 bytes (2) to the K-major A row and
+        // 16 rows of 256 bytes (2 KiB = 128) to the MN-major B tile.
+        constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, false, true);
+        const uint64_t a_desc0 = smem_desc_sw128(smem_u32(sm.a[0]), 16, 1024);
+        const uint64_t b_desc0 = smem_desc_sw128(smem_u32(sm.b[0]), kBBytes / 2, 1024);
+        constexpr uint64_t kADesc = kABytes >> 4, kBDesc = kBBytes >> 4;
+        int kg = 0, i = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += G, ++i) {
+            const int acc = i & 1;
+            if (i >= 2 && !(ok = warp_wait(&sm.acc_empty[acc], ((i - 2) >> 1) & 1, ab))) break;
+            tc_fence_after_sync();
+            const uint32_t d = tmem + static_cast<uint32_t>(acc) * BN;
+            for (int kb = 0; kb < num_k; ++kb, ++kg) {
+                const int st = kg % STAGES;
+                if (!(ok = warp_wait(&sm.full[st], (kg / STAGES) & 1, ab))) break;
                 tc_fence_after_sync();
-                const uint32_t aa = smem_u32(sm.a[st]);
-                const uint32_t ba = smem_u32(sm.b[st]);
+                const uint64_t ad = a_desc0 + static_cast<uint64_t>(st) * kADesc;
+                const uint64_t bd = b_desc0 + static_cast<uint64_t>(st) * kBDesc;
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk)
-                    mma_bf16_ss(tmem, smem_desc_sw128(aa + kk * 32, 16, 1024),
-                                smem_desc_sw128(ba + kk * 2048, kBBytes / 2, 1024), idesc,
-                                (kb > 0 || kk > 0) ? 1u : 0u);
-                mma_commit(&sm.empty[st]);
+                    warp_mma_bf16_ss(d, ad + 2 * kk, bd + 128 * kk, idesc,
+                                     (kb > 0 || kk > 0) ? 1u : 0u);
+                warp_commit(&sm.empty[st]);
             }
-            if (ok) mma_commit(&sm.acc_full);
-            // Always wait (time-bounded, whatever the abort state) until every
-            // MMA this thread issued has completed before tensor memory is
-            // released.
-            mma_commit(&sm.drain);
-            mbar_wait_drain(&sm.drain, 0);
+            if (!ok) break;
+            warp_commit(&sm.acc_full[acc]);
         }
+        // Always wait (time-bounded, whatever the abort state) until every
+        // MMA this warp issued has completed before tensor memory is
+        // released.
+        warp_commit(&sm.drain);
+        mbar_wait_drain(&sm.drain, 0);
     } else {
-        // Epilogue: warp w reads tensor-memory lanes 32*(w%4) .. +31.
+        // --------------------------------------------------------- epilogue
+        // Warp w reads tensor-memory lanes 32*(w%4) .. +31 (warps 2-5 cover
+        // the four quadrants).
         const uint32_t lane_base = static_cast<uint32_t>(warp & 3) * 32;
-        const int m = tm * BM + static_cast<int>(lane_base) + lane;
-        const bool ok = __all_sync(0xffffffffu, mbar_wait(&sm.acc_full, 0, ab));
-        if (ok) {
+        int i = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < p.total_tiles; tile += G, ++i) {
+            const Tile t = locate(p, tile);
+            const GemmProblem &pr = p.prob[t.pi];
+            const int acc = i & 1;
+            if (!(ok = __all_sync(0xffffffffu, mbar_wait(&sm.acc_full[acc], (i >> 1) & 1, ab))))
+                break;
             tc_fence_after_sync();
-            long long row_off = 0;
+            uint32_t r[4][32];
+            const uint32_t src = tmem_addr(tmem, lane_base, static_cast<uint32_t>(acc) * BN);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tmem_ld32(src + 32u * c, r[c]);
+            tmem_ld_wait(r[0]);
+            reg_fence32(r[1]);
+            reg_fence32(r[2]);
+            reg_fence32(r[3]);
+            // The accumulator is read: the MMA warp may start the tile after
+            // next in it.
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.acc_empty[acc]);
+
+            const int m = t.tm * BM + static_cast<int>(lane_base) + lane;
             if (m < pr.M) {
+                long long row_off;
                 if (pr.out_mode == kOutHeadSplit) {
-                    const int bb = m / pr.T, t = m - bb * pr.T;
-                    row_off = static_cast<long long>(bb) * pr.H * pr.T + t;  // + head*T later
+                    const int bb = m / pr.T, tt = m - bb * pr.T;
+                    row_off = static_cast<long long>(bb) * pr.H * pr.T + tt;  // + head*T below
                 } else {
                     row_off = static_cast<long long>(m) * pr.N;
                 }
-            }
-#pragma unroll 1
-            for (int chunk = 0; chunk < BN / 32; ++chunk) {
-                uint32_t r[32];
-                tmem_ld32(tmem_addr(tmem, lane_base, chunk * 32), r);
-                tmem_ld_wait(r);
-                const int n0 = tn * BN + chunk * 32;
-                if (m < pr.M && n0 < pr.N) {
-                    uint32_t packed[16];
 #pragma unroll
-                    for (int c = 0; c < 16; ++c)
-                        packed[c] = pack_bf16x2(__uint_as_float(r[2 * c]), __uint_as_float(r[2 * c + 1]));
-                    __nv_bfloat16 *dst;
-                    if (pr.out_mode == kOutHeadSplit) {
-                        const int head = n0 >> 6, c0 = n0 & 63;
-                        dst = pr.out + (row_off + static_cast<long long>(head) * pr.T) * 64 + c0;
-                    } else {
-                        dst = pr.out + row_off + n0;
+                for (int c = 0; c < 4; ++c) {
+                    const int n0 = t.tn * BN + c * 32;
+                    if (n0 < pr.N) {
+                        uint32_t packed[16];
+#pragma unroll
+                        for (int q = 0; q < 16; ++q)
+                            packed[q] = pack_bf16x2(__uint_as_float(r[c][2 * q]),
+                                                    __uint_as_float(r[c][2 * q + 1]));
+                        __nv_bfloat16 *dst;
+                        if (pr.out_mode == kOutHeadSplit) {
+                            const int head = n0 >> 6, c0 = n0 & 63;
+                            dst = pr.out + (row_off + static_cast<long long>(head) * pr.T) * 64 + c0;
+                        } else {
+                            dst = pr.out + row_off + n0;
+                        }
+                        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q)
+                            d4[q] = make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2],
+                                               packed[4 * q + 3]);
                     }
-                    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        d4[c] = make_uint4(packed[4 * c], packed[4 * c + 1], packed[4 * c + 2],
-                                           packed[4 * c + 3]);
                 }
             }
         }
@@ -192,8 +255,14 @@ cudaError_t launch_gemm_bf16(const CUtensorMap (&a)[kGemmMaxProblems],
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    gemm_bf16_kernel<<<p.total_tiles, kThreads, smem, stream>>>(a[0], a[1], a[2], b[0], b[1], b[2],
-                                                                  p);
+    // One persistent CTA per SM (fewer if there are fewer tiles).
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return e;
+    const int grid = p.total_tiles < sms ? p.total_tiles : sms;
+    if (grid <= 0) return cudaSuccess;
+    gemm_bf16_kernel<<<grid, kThreads, smem, stream>>>(a[0], a[1], a[2], b[0], b[1], b[2], p);
     return cudaGetLastError();
 }
 
