@@ -242,6 +242,9 @@ MHA_SMALL = [
     (2, 70, 333, 128, 2, si.MASK_KEY_PADDING, True),
     (1, 257, 129, 256, 4, si.MASK_NONE, True),
     (2, 64, 64, 64, 1, si.MASK_CAUSAL_KEY_PADDING, False),
+    # enough tiles for 128 x 256 projection tiles, with a ragged last row tile
+    (3, 1000, 1000, 512, 8, si.MASK_CAUSAL, False),
+    (2, 700, 900, 512, 8, si.MASK_KEY_PADDING, True),
 ]
 
 

@@ -91,12 +91,27 @@ mha_status encode_act(CUtensorMap *m, const void *base, long long M, int K) {
     return encode_bf16(m, base, 2, dims, strides, box);
 }
 
-// Weight (K rows x N) row-major viewed as (64, K, N/64): box (64, 64, 2).
-mha_status encode_weight(CUtensorMap *m, const void *base, int K, int N) {
+// Weight (K rows x N) row-major viewed as (64, K, N/64): box (64, 64, bn/64).
+mha_status encode_weight(CUtensorMap *m, const void *base, int K, int N, int bn) {
     const uint64_t dims[3] = {64, static_cast<uint64_t>(K), static_cast<uint64_t>(N / 64)};
     const uint64_t strides[2] = {static_cast<uint64_t>(N) * 2, 128};
-    const uint32_t box[3] = {64, 64, 2};
+    const uint32_t box[3] = {64, 64, static_cast<uint32_t>(bn / 64)};
     return encode_bf16(m, base, 3, dims, strides, box);
+}
+
+// Output tile width for a launch: a 128 x 256 tile reads A from shared memory
+// once per 256 columns and costs about 1.8 times a 128 x 128 tile, but halves
+// the tile count; take the width with the smaller cost in whole waves over
+// the SMs (small launches keep 128 so that every SM gets work).
+int choose_bn(const long long *M, int np, int N, int sms) {
+    long long t128 = 0, t256 = 0;
+    for (int i = 0; i < np; ++i) {
+        const long long mt = (M[i] + mha::kGemmBM - 1) / mha::kGemmBM;
+        t128 += mt * ((N + 127) / 128);
+        t256 += mt * ((N + 255) / 256);
+    }
+    const long long w128 = (t128 + sms - 1) / sms, w256 = (t256 + sms - 1) / sms;
+    return 10 * w256 * 18 < 100 * w128 ? 256 : 128;
 }
 
 bool valid_mask(int mask) { return mask >= MHA_MASK_NONE && mask <= MHA_MASK_CAUSAL_KEY_PADDING; }
@@ -228,6 +243,9 @@ MHA_EXPORT mha_status mha_forward(mha_dtype dt, const void *x_q, const void *x_k
     void *vh = static_cast<uint8_t *>(kh) + round256(bh * T_k * 128);
     void *om = static_cast<uint8_t *>(vh) + round256(bh * T_k * 128);
     const long long Mq = static_cast<long long>(B) * T_q, Mk = static_cast<long long>(B) * T_k;
+    int sms = 0;
+    if (mha::sm_count(&sms) != cudaSuccess || sms <= 0)
+        return cuda_fail("cudaDeviceGetAttribute", "SM count");
 
     // 1. Q, K, V projections with the head split folded into the epilogue.
     CUtensorMap ta[mha::kGemmMaxProblems], tb[mha::kGemmMaxProblems];
@@ -240,16 +258,21 @@ MHA_EXPORT mha_status mha_forward(mha_dtype dt, const void *x_q, const void *x_k
         long long M;
         int T;
     } ins[3] = {{x_q, w_q, qh, Mq, T_q}, {x_kv, w_k, kh, Mk, T_k}, {x_kv, w_v, vh, Mk, T_k}};
+    long long Ms[3];
+    int nm = 0;
+    for (int i = 0; i < 3; ++i)
+        if (ins[i].M > 0) Ms[nm++] = ins[i].M;
+    gp.bn = choose_bn(Ms, nm, hd, sms);
     int np = 0, tiles = 0;
     for (int i = 0; i < 3; ++i) {
         if (ins[i].M == 0) continue;
         if ((s = encode_act(&ta[np], ins[i].x, ins[i].M, d_model)) != MHA_OK) return s;
-        if ((s = encode_weight(&tb[np], ins[i].w, d_model, hd)) != MHA_OK) return s;
+        if ((s = encode_weight(&tb[np], ins[i].w, d_model, hd, gp.bn)) != MHA_OK) return s;
         mha::GemmProblem &pr = gp.prob[np];
         pr.M = static_cast<int>(ins[i].M);
         pr.N = hd;
         pr.K = d_model;
-        pr.tiles_n = (hd + mha::kGemmBN - 1) / mha::kGemmBN;
+        pr.tiles_n = (hd + gp.bn - 1) / gp.bn;
         pr.tile_start = tiles;
         pr.tile_count = pr.tiles_n * static_cast<int>((ins[i].M + mha::kGemmBM - 1) / mha::kGemmBM);
         pr.out = static_cast<__nv_bfloat16 *>(ins[i].out);
@@ -278,8 +301,9 @@ MHA_EXPORT mha_status mha_forward(mha_dtype dt, const void *x_q, const void *x_k
     // 3. Output projection Concat(heads) W^O.
     mha::GemmParams go{};
     go.status = status_dev;
+    go.bn = choose_bn(&Mq, 1, d_model, sms);
     if ((s = encode_act(&ta[0], om, Mq, hd)) != MHA_OK) return s;
-    if ((s = encode_weight(&tb[0], w_o, hd, d_model)) != MHA_OK) return s;
+    if ((s = encode_weight(&tb[0], w_o, hd, d_model, go.bn)) != MHA_OK) return s;
     for (int i = 1; i < mha::kGemmMaxProblems; ++i) {
         ta[i] = ta[0];
         tb[i] = tb[0];
@@ -288,7 +312,7 @@ MHA_EXPORT mha_status mha_forward(mha_dtype dt, const void *x_q, const void *x_k
     pr.M = static_cast<int>(Mq);
     pr.N = d_model;
     pr.K = hd;
-    pr.tiles_n = (d_model + mha::kGemmBN - 1) / mha::kGemmBN;
+    pr.tiles_n = (d_model + go.bn - 1) / go.bn;
     pr.tile_start = 0;
     pr.tile_count = pr.tiles_n * static_cast<int>((Mq + mha::kGemmBM - 1) / mha::kGemmBM);
     pr.out = static_cast<__nv_bfloat16 *>(out);

@@ -6,18 +6,22 @@
 // Concat(head_1..head_h) W^O: muhitai.com "Multi-Head Attention Formula").
 //
 // One launch runs up to three independent problems (the Q, K and V
-// projections share a launch), cut into 128 x 128 output tiles.  The kernel
+// projections share a launch), cut into 128 x BN output tiles (BN = 128 or
+// 256, chosen per launch by the host for the better balance).  The kernel
 // is persistent: one CTA per SM takes tiles c, c + G, c + 2G, ... (all tiles
 // of a launch have the same K, so round robin balances them), and the
 // accumulator is double-buffered in tensor memory, so the epilogue of one
 // tile overlaps the main loop of the next:
 //
 //   warp 0      TMA producer: A tile (128 rows x 64 k, K-major) and B tile
-//               (64 k x 128 n of W, N contiguous = MN-major) per k-block,
-//               6-stage ring.
-//   warp 1      MMA issuer: tcgen05.mma kind::f16, M=128 N=128 K=16, fp32
-//               accumulators in two 128-column tensor-memory buffers; the
-//               whole warp runs the loop and one elected lane issues.
+//               (64 k x BN n of W, N contiguous = MN-major) per k-block,
+//               6-stage (BN = 128) or 4-stage (BN = 256) ring.
+//   warp 1      MMA issuer: tcgen05.mma kind::f16, M=128 N=BN K=16, fp32
+//               accumulators in two BN-column tensor-memory buffers; the
+//               whole warp runs the loop and one elected lane issues.  With
+//               BN = 256 the A tile is read from shared memory once per 256
+//               output columns (96 instead of 128 bytes per cycle at the
+//               tensor rate).
 //   warps 2-5   epilogue: tensor memory -> registers (the buffer is handed
 //               back as soon as it is read) -> bf16 -> global.  In head-split
 //               mode column n = head*64 + c of row m = b*T + t is stored at
@@ -32,16 +36,23 @@
 namespace mha {
 namespace {
 
-constexpr int BM = kGemmBM, BN = kGemmBN, BK = kGemmBK;
-constexpr int STAGES = 6;
+constexpr int BM = kGemmBM, BK = kGemmBK;
 constexpr int kThreads = 192;
 constexpr uint32_t kABytes = BM * BK * 2;  // 16 KiB
-constexpr uint32_t kBBytes = BK * BN * 2;  // 16 KiB: two 64-column blocks of 8 KiB
-constexpr uint32_t kTmemCols = 2 * BN;     // two accumulators
+constexpr uint32_t kBBlock = BK * 64 * 2;  // 8 KiB: one 64-column block of a B tile
 
+template <int BN>
+struct GemmCfg {
+    static constexpr int kStages = BN == 128 ? 6 : 4;
+    static constexpr uint32_t kBBytes = BK * BN * 2;  // BN/64 column blocks
+    static constexpr uint32_t kTmemCols = 2 * BN;     // two accumulators
+};
+
+template <int BN>
 struct __align__(1024) SmemGemm {
+    static constexpr int STAGES = GemmCfg<BN>::kStages;
     uint8_t a[STAGES][kABytes];
-    uint8_t b[STAGES][kBBytes];
+    uint8_t b[STAGES][GemmCfg<BN>::kBBytes];
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
     uint64_t acc_full[2];   // MMA -> epilogue (commit)
@@ -66,13 +77,17 @@ __device__ __forceinline__ Tile locate(const GemmParams &p, int tile) {
     return t;
 }
 
+template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap a0, const __grid_constant__ CUtensorMap a1,
                      const __grid_constant__ CUtensorMap a2, const __grid_constant__ CUtensorMap b0,
                      const __grid_constant__ CUtensorMap b1, const __grid_constant__ CUtensorMap b2,
                      const GemmParams p) {
+    constexpr int STAGES = GemmCfg<BN>::kStages;
+    constexpr uint32_t kBBytes = GemmCfg<BN>::kBBytes;
+    constexpr uint32_t kTmemCols = GemmCfg<BN>::kTmemCols;
     extern __shared__ uint8_t smem_raw[];
-    SmemGemm &sm = *reinterpret_cast<SmemGemm *>(
+    SmemGemm<BN> &sm = *reinterpret_cast<SmemGemm<BN> *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -141,10 +156,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Accumulator i % 2 for the CTA's i-th tile; it is reused once the
         // epilogue has read tile i-2 out of it.  Descriptors as base +
         // constant: a K step of 16 adds 32 bytes (2) to the K-major A row and
-        // 16 rows of 256 bytes (2 KiB = 128) to the MN-major B tile.
+        // 16 rows of 128 bytes (2 KiB = 128) to each 64-column block of the
+        // MN-major B tile; the blocks are 8 KiB apart (leading byte offset).
         constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, false, true);
         const uint64_t a_desc0 = smem_desc_sw128(smem_u32(sm.a[0]), 16, 1024);
-        const uint64_t b_desc0 = smem_desc_sw128(smem_u32(sm.b[0]), kBBytes / 2, 1024);
+        const uint64_t b_desc0 = smem_desc_sw128(smem_u32(sm.b[0]), kBBlock, 1024);
         constexpr uint64_t kADesc = kABytes >> 4, kBDesc = kBBytes >> 4;
         int kg = 0, i = 0;
         bool ok = true;
@@ -187,32 +203,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!(ok = __all_sync(0xffffffffu, mbar_wait(&sm.acc_full[acc], (i >> 1) & 1, ab))))
                 break;
             tc_fence_after_sync();
-            uint32_t r[4][32];
-            const uint32_t src = tmem_addr(tmem, lane_base, static_cast<uint32_t>(acc) * BN);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tmem_ld32(src + 32u * c, r[c]);
-            tmem_ld_wait(r[0]);
-            reg_fence32(r[1]);
-            reg_fence32(r[2]);
-            reg_fence32(r[3]);
-            // The accumulator is read: the MMA warp may start the tile after
-            // next in it.
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.acc_empty[acc]);
-
             const int m = t.tm * BM + static_cast<int>(lane_base) + lane;
-            if (m < pr.M) {
-                long long row_off;
-                if (pr.out_mode == kOutHeadSplit) {
-                    const int bb = m / pr.T, tt = m - bb * pr.T;
-                    row_off = static_cast<long long>(bb) * pr.H * pr.T + tt;  // + head*T below
-                } else {
-                    row_off = static_cast<long long>(m) * pr.N;
+            long long row_off = 0;
+            if (pr.out_mode == kOutHeadSplit) {
+                const int bb = m / pr.T, tt = m - bb * pr.T;
+                row_off = static_cast<long long>(bb) * pr.H * pr.T + tt;  // + head*T below
+            } else {
+                row_off = static_cast<long long>(m) * pr.N;
+            }
+            // 128 columns at a time; after the last group the accumulator is
+            // handed back (the MMA warp may start the tile after next in it).
+#pragma unroll 1
+            for (int grp = 0; grp < BN / 128; ++grp) {
+                uint32_t r[4][32];
+                const uint32_t src =
+                    tmem_addr(tmem, lane_base, static_cast<uint32_t>(acc) * BN + 128u * grp);
+#pragma unroll
+                for (int c = 0; c < 4; ++c) tmem_ld32(src + 32u * c, r[c]);
+                tmem_ld_wait(r[0]);
+                reg_fence32(r[1]);
+                reg_fence32(r[2]);
+                reg_fence32(r[3]);
+                if (grp == BN / 128 - 1) {
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sm.acc_empty[acc]);
                 }
+                if (m >= pr.M) continue;
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
-                    const int n0 = t.tn * BN + c * 32;
+                    const int n0 = t.tn * BN + grp * 128 + c * 32;
                     if (n0 < pr.N) {
                         uint32_t packed[16];
 #pragma unroll
@@ -245,25 +265,40 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-}  // namespace
-
-cudaError_t launch_gemm_bf16(const CUtensorMap (&a)[kGemmMaxProblems],
-                             const CUtensorMap (&b)[kGemmMaxProblems], const GemmParams &p,
-                             cudaStream_t stream) {
-    const size_t smem = sizeof(SmemGemm) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_kernel,
+template <int BN>
+cudaError_t launch_bn(const CUtensorMap (&a)[kGemmMaxProblems],
+                      const CUtensorMap (&b)[kGemmMaxProblems], const GemmParams &p, int sms,
+                      cudaStream_t stream) {
+    const size_t smem = sizeof(SmemGemm<BN>) + 1024;
+    cudaError_t e = cudaFuncSetAttribute(gemm_bf16_kernel<BN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     // One persistent CTA per SM (fewer if there are fewer tiles).
-    int dev = 0, sms = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-        return e;
     const int grid = p.total_tiles < sms ? p.total_tiles : sms;
     if (grid <= 0) return cudaSuccess;
-    gemm_bf16_kernel<<<grid, kThreads, smem, stream>>>(a[0], a[1], a[2], b[0], b[1], b[2], p);
+    gemm_bf16_kernel<BN><<<grid, kThreads, smem, stream>>>(a[0], a[1], a[2], b[0], b[1], b[2], p);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t sm_count(int *sms) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    return cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, dev);
+}
+
+cudaError_t launch_gemm_bf16(const CUtensorMap (&a)[kGemmMaxProblems],
+                             const CUtensorMap (&b)[kGemmMaxProblems], const GemmParams &p,
+                             cudaStream_t stream) {
+    int sms = 0;
+    cudaError_t e = sm_count(&sms);
+    if (e != cudaSuccess) return e;
+    if (p.bn == 256) return launch_bn<256>(a, b, p, sms, stream);
+    if (p.bn == 128) return launch_bn<128>(a, b, p, sms, stream);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace mha

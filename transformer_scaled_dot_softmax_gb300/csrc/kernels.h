@@ -50,15 +50,19 @@ struct GemmProblem {
 struct GemmParams {
     int num_problems;
     int total_tiles;
+    int bn;  // output tile width: 128 or 256
     GemmProblem prob[kGemmMaxProblems];
     int *status;
 };
-constexpr int kGemmBM = 128, kGemmBN = 128, kGemmBK = 64;
+constexpr int kGemmBM = 128, kGemmBK = 64;
 
 // a[i]: 2-D TMA map over the activation (K inner, M rows), box (64, 128).
-// b[i]: 3-D TMA map over the weight viewed as (64, K, N/64), box (64, 64, 2).
+// b[i]: 3-D TMA map over the weight viewed as (64, K, N/64), box (64, 64, bn/64).
 cudaError_t launch_gemm_bf16(const CUtensorMap (&a)[kGemmMaxProblems],
                              const CUtensorMap (&b)[kGemmMaxProblems], const GemmParams &p,
                              cudaStream_t stream);
+
+// Number of SMs of the current device.
+cudaError_t sm_count(int *sms);
 
 }  // namespace mha
