@@ -357,7 +357,30 @@ def time_other_workloads(dev, stream, flush, iters=20):
         fl = mha_flops(w, x["key_lens"])
         res[w.name] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12, "flops": fl,
                        "kind": "bf16 MHA forward: grouped QKV GEMM + fused attention + W^O GEMM"}
+    w = si.WORKLOADS[5]
+    x = si.make_inputs(w)
+    q, k, v = dv(x["q_bits"]), dv(x["k_bits"]), dv(x["v_bits"])
+    lens = torch.from_numpy(x["key_lens"]).to(dev)
+    o = torch.empty_like(q)
+    ms = timed(lambda: tsds.sdpa_decode_forward(q, k, v, lens, o, scale=w.scale, stream=stream))
+    nbytes = decode_bytes(w, x["key_lens"])
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    peaks, peak_kind = load_peaks()
+    peak = peaks.get("hbm_gbs")
+    res[w.name] = {"ms": ms, "us": 1e3 * ms, "gbs": gbs, "bytes": nbytes,
+                   "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s",
+                                "frac": gbs / peak if peak else None,
+                                "peak_source": peak_kind + " copy bandwidth"},
+                   "kind": "bf16 decode attention: 8-CTA cluster per (b, h), HBM-bound"}
     return res
+
+
+def decode_bytes(w, key_lens) -> int:
+    """Algorithmic bytes of one decode call: every visible cached key and
+    value row read once, the query rows read and the output rows written."""
+    lens = np.full(w.B, w.T_k) if key_lens is None else np.clip(key_lens, 0, w.T_k)
+    row = 2 * w.d_k
+    return int(w.h * (lens.sum() * 2 * row + w.B * w.T_q * 2 * row))
 
 
 def run_e2e(args, q, k, v, out, w, stream, dev, dist, flops, world):

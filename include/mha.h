@@ -95,6 +95,33 @@ mha_status sdpa_forward(mha_dtype dt, const void *q, const void *k, const void *
                         cudaStream_t stream);
 
 /*
+ * Attention for decoding steps (bf16): each of the T_q new query rows of a
+ * (b, h) attends to the first cache_lens[b] rows of that sequence's key/value
+ * cache,
+ *   o = softmax(scale * q k[0:len_b]^T) v[0:len_b].
+ * Generation emits one token at a time and feeds it back in (aiany.app,
+ * Step 10 "The decoder"); the newest row's causal mask ("Masked Attention in
+ * the Decoder") reduces to this length limit, and cross-attention over the
+ * encoder output ("The Decoder's Cross-Attention") is the same call with the
+ * source length.  The result equals sdpa_forward with a key-padding mask.
+ *
+ *   q (B, h, T_q, 64), k_cache and v_cache (B, h, T_k, 64) with T_k the
+ *   cache capacity, o (B, h, T_q, 64); bf16, contiguous, 16-byte aligned.
+ *   cache_lens: DEVICE int32 array of B entries (clamped to [0, T_k]), or
+ *   NULL for T_k keys everywhere.  1 <= T_q <= 8; d_k == d_v == 64 (other
+ *   head sizes: MHA_ERR_UNSUPPORTED).  A row with no cached key outputs 0.
+ *
+ * One launch: the keys of each (b, h) are split over an 8-CTA thread-block
+ * cluster, each CTA streams its range once from HBM (SIMT; the work per key
+ * is too small for the tensor cores), and the partial softmax states are
+ * merged exactly through distributed shared memory.  No workspace, no wait
+ * that can time out (status words are not needed).
+ */
+mha_status sdpa_decode_forward(const void *q, const void *k_cache, const void *v_cache, void *o,
+                               int B, int h, int T_q, int T_k, int d_k, int d_v, float scale,
+                               const int32_t *cache_lens, cudaStream_t stream);
+
+/*
  * Bytes of device workspace mha_forward needs: the projected Q, K, V in
  * head-split layout (B, h, T, d) and the merged attention output
  * (B, T_q, h * d_v), all bf16, each region 256-byte aligned.

@@ -146,6 +146,10 @@ WORKLOADS = [
              cross=True, seed=3),
     Workload("sdpa_causal_bf16_B2_h16_T8192_d64", "sdpa", "bf16", B=2, h=16, T_q=8192,
              T_k=8192, mask=MASK_CAUSAL, seed=4),
+    # Decoding: one new query row per sequence against a key/value cache of
+    # 8192 slots, of which the first len_b (uniform in [2048, 8192]) hold keys.
+    Workload("decode_bf16_B16_h16_Tq1_cache8192", "sdpa", "bf16", B=16, h=16, T_q=1,
+             T_k=8192, mask=MASK_KEY_PADDING, len_lo=2048, len_hi=8192, seed=5),
 ]
 
 

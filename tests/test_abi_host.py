@@ -104,3 +104,23 @@ def test_python_binding_imports_without_gpu():
     import transformer_scaled_dot_softmax_gb300 as m
     assert m.status_string(6) == "kernel wait timed out"
     assert m.MASKS["causal"] == 1
+
+
+def decode(lib, q=FAKE, k=FAKE, v=FAKE, o=FAKE, B=1, h=1, Tq=1, Tk=8, dk=64, dv=64, scale=0.125,
+           lens=None):
+    return lib.lib.sdpa_decode_forward(q, k, v, o, B, h, Tq, Tk, dk, dv, scale, lens, None)
+
+
+def test_decode_rejects_bad_arguments(lib):
+    assert decode(lib, q=None) == lib.MHA_ERR_INVALID_ARG
+    assert decode(lib, k=None) == lib.MHA_ERR_INVALID_ARG
+    assert decode(lib, o=None) == lib.MHA_ERR_INVALID_ARG
+    assert decode(lib, B=-1) == lib.MHA_ERR_INVALID_ARG
+    assert decode(lib, scale=float("inf")) == lib.MHA_ERR_INVALID_ARG
+    assert decode(lib, Tq=9) == lib.MHA_ERR_UNSUPPORTED
+    assert decode(lib, dk=128, dv=128) == lib.MHA_ERR_UNSUPPORTED
+    assert decode(lib, q=FAKE + 8) == lib.MHA_ERR_MISALIGNED
+    assert decode(lib, v=FAKE + 2) == lib.MHA_ERR_MISALIGNED
+    # empty problems are no-ops; T_k == 0 needs no cache pointers
+    assert decode(lib, B=0) == lib.MHA_OK
+    assert decode(lib, Tq=0) == lib.MHA_OK

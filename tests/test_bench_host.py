@@ -90,3 +90,12 @@ def test_visible_pairs_and_mha_flops():
     hd = w2.h * 64
     proj = 2 * 10 * 64 * hd + 2 * 2 * 14 * 64 * hd + 2 * 10 * hd * 64
     assert bench.mha_flops(w2, lens) == pytest.approx(proj + 256 * 3 * 5 * 9)
+
+
+def test_decode_bytes_counts_visible_rows():
+    w = si.WORKLOADS[5].replace(B=2, h=3, T_q=2, T_k=100)
+    # rows of 64 bf16 = 128 bytes; K and V of every visible key, q and o rows
+    assert bench.decode_bytes(w, np.array([10, 200], dtype=np.int32)) == 3 * (
+        (10 + 100) * 2 * 128 + 2 * 2 * 2 * 128)
+    assert bench.decode_bytes(w.replace(mask=si.MASK_NONE), None) == 3 * (
+        200 * 2 * 128 + 2 * 2 * 2 * 128)

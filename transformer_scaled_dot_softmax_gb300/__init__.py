@@ -5,6 +5,7 @@ only marshal arguments -- every step of the computation runs in the
 library's CUDA kernels.  PyTorch supplies device memory and the stream.
 
     out = sdpa_forward(q, k, v, mask="causal")            # (B, h, T, 64) bf16
+    out = sdpa_decode_forward(q, k_cache, v_cache, lens)   # (B, h, T_q <= 8, 64) bf16
     out = mha_forward(x_q, x_kv, w_q, w_k, w_v, w_o, h=8)  # (B, T, d_model) bf16
 """
 from __future__ import annotations
@@ -15,7 +16,7 @@ from . import _native
 from ._native import (MHA_BF16, MHA_F32, MHA_MASK_CAUSAL, MHA_MASK_CAUSAL_KEY_PADDING,
                       MHA_MASK_KEY_PADDING, MHA_MASK_NONE, MHA_OK, lib)
 
-__all__ = ["sdpa_forward", "mha_forward", "mha_workspace_bytes", "status_string", "MhaError",
+__all__ = ["sdpa_forward", "sdpa_decode_forward", "mha_forward", "mha_workspace_bytes", "status_string", "MhaError",
            "MASKS", "lib"]
 
 MASKS = {"none": MHA_MASK_NONE, "causal": MHA_MASK_CAUSAL, "key_padding": MHA_MASK_KEY_PADDING,
@@ -91,6 +92,32 @@ def sdpa_forward(q, k, v, out=None, *, scale=None, mask="none", key_lens=None, s
                           _mask_code(mask), _ptr(key_lens), _ptr(status), _stream_handle(stream))
     if rc != MHA_OK:
         raise MhaError(rc, "sdpa_forward")
+    return out
+
+
+def sdpa_decode_forward(q, k_cache, v_cache, cache_lens=None, out=None, *, scale=None,
+                        stream=None):
+    """Decoding step: each of the T_q (<= 8) query rows of q (B,h,T_q,64)
+    attends to the first cache_lens[b] rows of k_cache / v_cache
+    (B,h,T_k,64); bf16 CUDA tensors, cache_lens int32 on the device (None:
+    all T_k).  Returns out (B,h,T_q,64)."""
+    torch = _torch()
+    for n, t in (("q", q), ("k_cache", k_cache), ("v_cache", v_cache)):
+        _check_dev(n, t, torch.bfloat16)
+    B, h, T_q, d_k = q.shape
+    T_k, d_v = k_cache.shape[2], v_cache.shape[3]
+    if out is None:
+        out = torch.empty((B, h, T_q, d_v), dtype=torch.bfloat16, device=q.device)
+    _check_dev("out", out, torch.bfloat16)
+    if cache_lens is not None:
+        _check_dev("cache_lens", cache_lens, torch.int32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_k)
+    rc = lib.sdpa_decode_forward(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(out), B, h, T_q,
+                                 T_k, d_k, d_v, float(scale), _ptr(cache_lens),
+                                 _stream_handle(stream))
+    if rc != MHA_OK:
+        raise MhaError(rc, "sdpa_decode_forward")
     return out
 
 

@@ -201,6 +201,34 @@ MHA_EXPORT mha_status sdpa_forward(mha_dtype dt, const void *q, const void *k, c
                               T_q, T_k, scale, mask, key_lens, status_dev, stream);
 }
 
+MHA_EXPORT mha_status sdpa_decode_forward(const void *q, const void *k_cache,
+                                          const void *v_cache, void *o, int B, int h, int T_q,
+                                          int T_k, int d_k, int d_v, float scale,
+                                          const int32_t *cache_lens, cudaStream_t stream) {
+    if (B < 0 || h < 0 || T_q < 0 || T_k < 0 || d_k <= 0 || d_v <= 0 || !isfinite(scale))
+        return MHA_ERR_INVALID_ARG;
+    if (T_q > mha::kDecodeMaxRows) return MHA_ERR_UNSUPPORTED;
+    if (d_k != 64 || d_v != 64) return MHA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(B) * h * 8 >= (1ll << 31)) return MHA_ERR_UNSUPPORTED;
+    if (B == 0 || h == 0 || T_q == 0) return MHA_OK;
+    if (!q || !o || (T_k > 0 && (!k_cache || !v_cache))) return MHA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(o) || (T_k > 0 && (!aligned16(k_cache) || !aligned16(v_cache))))
+        return MHA_ERR_MISALIGNED;
+    mha::DecodeParams p;
+    p.B = B;
+    p.H = h;
+    p.Tq = T_q;
+    p.Tk = T_k;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.key_lens = cache_lens;
+    return launch_status(
+        mha::launch_decode_bf16(static_cast<const __nv_bfloat16 *>(q),
+                                static_cast<const __nv_bfloat16 *>(k_cache),
+                                static_cast<const __nv_bfloat16 *>(v_cache),
+                                static_cast<__nv_bfloat16 *>(o), p, stream),
+        "decode attention launch");
+}
+
 MHA_EXPORT size_t mha_workspace_bytes(int B, int h, int T_q, int T_k, int d_k, int d_v) {
     if (B < 0 || h < 0 || T_q < 0 || T_k < 0 || d_k < 0 || d_v < 0) return 0;
     const size_t bh = static_cast<size_t>(B) * h;

@@ -31,6 +31,19 @@ constexpr int kAttnHeadDim = 64;
 cudaError_t launch_attn_bf16(const CUtensorMap &tq, const CUtensorMap &tk,
                              const CUtensorMap &tv, const AttnParams &p, cudaStream_t stream);
 
+// ------------------------------------------------ bf16 decode attention
+constexpr int kDecodeMaxRows = 8;  // query rows per (b, h) in one decode call
+struct DecodeParams {
+    int B, H, Tq, Tk;
+    float scale_log2;          // scale * log2(e)
+    const int32_t *key_lens;   // cached keys per batch entry; null: all Tk
+};
+// q (B, H, Tq, 64), k and v (B, H, Tk, 64), o (B, H, Tq, 64), all bf16 and
+// contiguous; Tq <= kDecodeMaxRows.
+cudaError_t launch_decode_bf16(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
+                               const __nv_bfloat16 *v, __nv_bfloat16 *o, const DecodeParams &p,
+                               cudaStream_t stream);
+
 // ------------------------------------------------ fp32 SIMT attention
 cudaError_t launch_sdpa_f32(const float *q, const float *k, const float *v, float *o, int B,
                             int H, int Tq, int Tk, int dk, int dv, float scale, int mask,
