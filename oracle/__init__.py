@@ -42,6 +42,8 @@ def _load():
         lib.oracle_mha.argtypes = [dp, dp, dp, dp, dp, dp, dp, ci, ci, ci, ci, ci, ci, ci, cd,
                                    ci, ip, lp, cl]
         lib.oracle_mha.restype = ci
+        lib.oracle_add_layernorm.argtypes = [dp, dp, dp, dp, cd, dp, cl, ci]
+        lib.oracle_add_layernorm.restype = ci
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ci
         _lib = lib
@@ -138,3 +140,31 @@ def mha(x_q, x_kv, w_q, w_k, w_v, w_o, h, scale=None, mask=MASK_NONE, key_lens=N
     if rc:
         raise RuntimeError("oracle_mha failed")
     return out
+
+
+def add_layernorm(x, s, gamma, beta, eps=1e-5):
+    """LayerNorm(x + s) over the last axis with gain gamma and shift beta:
+    (v - mean) / sqrt(population variance + eps) * gamma + beta, v = x + s."""
+    x, s = _d(x), _d(s)
+    gamma, beta = _d(gamma), _d(beta)
+    if x.shape != s.shape or gamma.shape != (x.shape[-1],) or beta.shape != gamma.shape:
+        raise ValueError("shape mismatch")
+    D = x.shape[-1]
+    y = np.empty(x.shape)
+    rc = _load().oracle_add_layernorm(_p(x), _p(s), _p(gamma), _p(beta), float(eps), _p(y),
+                                      x.size // D, D)
+    if rc:
+        raise RuntimeError("oracle_add_layernorm failed")
+    return y
+
+
+def mha_add_layernorm(x_q, x_kv, w_q, w_k, w_v, w_o, gamma, beta, h, eps=1e-5, scale=None,
+                      mask=MASK_NONE, key_lens=None, query_rows=None):
+    """The attention sublayer with its residual and normalisation:
+    LayerNorm(x_q + MultiHead(x_q, x_kv)).  Shapes as mha(); query_rows
+    selects flat rows b*Tq + i."""
+    out = mha(x_q, x_kv, w_q, w_k, w_v, w_o, h, scale=scale, mask=mask, key_lens=key_lens,
+              query_rows=query_rows)
+    xq = _d(x_q).reshape(-1, out.shape[-1])
+    res = xq if query_rows is None else xq[np.asarray(query_rows, dtype=np.int64)]
+    return add_layernorm(res.reshape(out.shape), out, gamma, beta, eps)

@@ -295,6 +295,41 @@ done:
     return rc;
 }
 
+/*
+ * Residual connection and layer normalisation around a sublayer, per row:
+ *   v = x + s  (the sublayer's input added back to its output),
+ *   y = (v - mu) / sigma * gamma + beta,
+ * mu and sigma the mean and standard deviation of v over the D features
+ * ("Attention Is All You Need" (aiany.app) Step 9, LayerNorm(x + Sublayer(x));
+ * notebook chapter "Layer Normalization and Residual Connections",
+ * LayerNorm(x) = (x - mu)/sigma (.) gamma + beta).  Reading where the pages
+ * are silent: sigma = sqrt(mean((v - mu)^2) + eps) -- the population standard
+ * deviation with a small eps the caller chooses (eps = 0 is the formula as
+ * printed).  x, s, y (rows, D); gamma, beta (D).
+ */
+int oracle_add_layernorm(const double *x, const double *s, const double *gamma,
+                         const double *beta, double eps, double *y, long rows, int D)
+{
+    if (rows < 0 || D <= 0 || eps < 0.0) return 1;
+#pragma omp parallel for schedule(static)
+    for (long r = 0; r < rows; ++r) {
+        const double *xr = x + r * D, *sr = s + r * D;
+        double *yr = y + r * D;
+        double mu = 0.0;
+        for (int c = 0; c < D; ++c) mu += xr[c] + sr[c];
+        mu /= D;
+        double var = 0.0;
+        for (int c = 0; c < D; ++c) {
+            const double d = xr[c] + sr[c] - mu;
+            var += d * d;
+        }
+        var /= D;
+        const double sigma = sqrt(var + eps);
+        for (int c = 0; c < D; ++c) yr[c] = (xr[c] + sr[c] - mu) / sigma * gamma[c] + beta[c];
+    }
+    return 0;
+}
+
 /* Number of host threads OpenMP will use (for reporting). */
 int oracle_num_threads(void)
 {

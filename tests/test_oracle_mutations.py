@@ -27,6 +27,14 @@ MUTATIONS = [
      "matmul(x_kv, Wk, vp, Mk, D, H * dv);"),
     ("W^O transposed", "const double *wr = W + (size_t)kk * N;\n            for (int n = 0; n < N; ++n)\n                yr[n] += a * wr[n];",
      "for (int n = 0; n < N; ++n)\n                yr[n] += a * W[(size_t)(K == N ? n * K + kk : kk * N + n)];"),
+    ("layer norm with the unbiased variance", "var /= D;", "var /= (D - 1);"),
+    ("layer norm without the variance's square root", "const double sigma = sqrt(var + eps);",
+     "const double sigma = var + eps;"),
+    ("layer norm eps outside the square root", "const double sigma = sqrt(var + eps);",
+     "const double sigma = sqrt(var) + eps;"),
+    ("layer norm gain and shift swapped", "* gamma[c] + beta[c];", "* beta[c] + gamma[c];"),
+    ("residual left out of the normalised value", "yr[c] = (xr[c] + sr[c] - mu)",
+     "yr[c] = (sr[c] - mu)"),
 ]
 
 

@@ -373,3 +373,81 @@ def test_row_subsets_match_full_computation(mask):
     sub = oracle.mha(x, x, *ws, h=h, mask=mask, key_lens=np.array([7, 4], dtype=np.int32),
                      query_rows=qr)
     np.testing.assert_allclose(sub, full.reshape(-1, D)[qr], rtol=0, atol=1e-13)
+
+
+# ----------------------------------------------- residual + layer normalisation
+# aiany.app Step 9: LayerNorm(x + Sublayer(x)); notebook chapter "Layer
+# Normalization and Residual Connections": (x - mu)/sigma (.) gamma + beta over
+# the feature dimension.  Reading: sigma = sqrt(population variance + eps).
+
+def test_add_layernorm_matches_torch_layer_norm():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(61)
+    x, s = rng.normal(size=(7, 5, 48)), rng.normal(size=(7, 5, 48)) * 3
+    g, b = rng.normal(size=48), rng.normal(size=48)
+    for eps in (0.0, 1e-5, 0.3):
+        ref = torch.nn.functional.layer_norm(torch.from_numpy(x + s), (48,), torch.from_numpy(g),
+                                             torch.from_numpy(b), eps=eps).numpy()
+        np.testing.assert_allclose(oracle.add_layernorm(x, s, g, b, eps), ref, rtol=0, atol=1e-12)
+
+
+def test_add_layernorm_constant_row_gives_shift():
+    g, b = np.array([2.0, -1.0, 0.5, 3.0]), np.array([0.25, -4.0, 7.0, 1.0])
+    x = np.full((3, 4), 1.75)
+    y = oracle.add_layernorm(x, np.full((3, 4), -0.5), g, b, 1e-5)
+    np.testing.assert_array_equal(y, np.tile(b, (3, 1)))
+
+
+def test_add_layernorm_two_features_closed_form():
+    # v = (a, c): mean (a+c)/2, population sd |a-c|/2, so v normalises to
+    # (-1, +1) when a < c (eps = 0)
+    x = np.array([[1.0, 4.0], [10.0, -2.0]])
+    s = np.array([[0.5, -0.5], [0.0, 1.0]])  # v = (1.5, 3.5), (10, -1)
+    g, b = np.array([3.0, 0.5]), np.array([1.0, -1.0])
+    y = oracle.add_layernorm(x, s, g, b, 0.0)
+    np.testing.assert_allclose(y, [[-3.0 + 1.0, 0.5 - 1.0], [3.0 + 1.0, -0.5 - 1.0]], atol=1e-15)
+
+
+def test_add_layernorm_invariant_to_positive_affine_maps():
+    rng = np.random.default_rng(62)
+    v = rng.normal(size=(4, 32))
+    g, b = rng.normal(size=32), rng.normal(size=32)
+    zero = np.zeros_like(v)
+    ref = oracle.add_layernorm(v, zero, g, b, 0.0)
+    np.testing.assert_allclose(oracle.add_layernorm(5.0 * v + 3.0, zero, g, b, 0.0), ref,
+                               rtol=0, atol=1e-12)
+
+
+def test_add_layernorm_adds_the_residual():
+    rng = np.random.default_rng(63)
+    x, s = rng.normal(size=(3, 16)), rng.normal(size=(3, 16))
+    g, b = np.ones(16), np.zeros(16)
+    y = oracle.add_layernorm(x, s, g, b, 1e-5)
+    np.testing.assert_allclose(y, oracle.add_layernorm(x + s, np.zeros_like(x), g, b, 1e-5),
+                               atol=1e-13)
+    np.testing.assert_allclose(y, oracle.add_layernorm(s, x, g, b, 1e-5), atol=1e-13)
+    assert np.abs(y - oracle.add_layernorm(x, np.zeros_like(x), g, b, 1e-5)).max() > 0.1
+    # unit gain, zero shift: every row has mean 0 and variance var/(var+eps)
+    v = x + s
+    var = v.var(axis=1)
+    np.testing.assert_allclose(y.mean(axis=1), 0.0, atol=1e-13)
+    np.testing.assert_allclose((y ** 2).mean(axis=1), var / (var + 1e-5), atol=1e-12)
+
+
+def test_mha_add_layernorm_with_zero_output_projection_normalises_the_input():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(64)
+    B, T, D, h = 2, 5, 16, 2
+    x = rng.normal(size=(B, T, D))
+    w = [rng.normal(size=(D, D)) * 0.3 for _ in range(3)]
+    g, b = rng.normal(size=D), rng.normal(size=D)
+    y = oracle.mha_add_layernorm(x, x, *w, np.zeros((D, D)), g, b, h=h, eps=1e-5)
+    ref = torch.nn.functional.layer_norm(torch.from_numpy(x), (D,), torch.from_numpy(g),
+                                         torch.from_numpy(b), eps=1e-5).numpy()
+    np.testing.assert_allclose(y, ref, rtol=0, atol=1e-12)
+    # rows selected by index match the full computation
+    rows = np.array([0, 3, 7, 9])
+    w_o = rng.normal(size=(D, D)) * 0.3
+    full = oracle.mha_add_layernorm(x, x, *w, w_o, g, b, h=h, mask=MASK_CAUSAL)
+    part = oracle.mha_add_layernorm(x, x, *w, w_o, g, b, h=h, mask=MASK_CAUSAL, query_rows=rows)
+    np.testing.assert_allclose(part, full.reshape(-1, D)[rows], rtol=0, atol=1e-13)
