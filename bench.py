@@ -310,9 +310,10 @@ def mha_flops(w: si.Workload, key_lens) -> float:
 
 
 def time_other_workloads(dev, stream, flush, iters=20):
-    """The four other workloads of the table: fp32 SDPA latency and the three
-    MHA forwards end to end (three launches), device-resident inputs, L2
-    flushed between calls, CUDA events around each call."""
+    """The other workloads of the table: fp32 SDPA latency, the three MHA
+    forwards end to end (three launches; alone and with the residual +
+    layer normalisation of the sublayer) and the decode step, device-resident
+    inputs, L2 flushed between calls, CUDA events around each call."""
     import torch
     import transformer_scaled_dot_softmax_gb300 as tsds
 
@@ -357,6 +358,15 @@ def time_other_workloads(dev, stream, flush, iters=20):
         fl = mha_flops(w, x["key_lens"])
         res[w.name] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12, "flops": fl,
                        "kind": "bf16 MHA forward: grouped QKV GEMM + fused attention + W^O GEMM"}
+        ln = si.layernorm_params(w.seed, w.d_model)
+        g, bt = dv(ln["gamma_bits"]), dv(ln["beta_bits"])
+        ms_ln = timed(lambda: tsds.mha_forward_add_layernorm(
+            xq, xkv, *wts, g, bt, h=w.h, out=out, workspace=ws, scale=w.scale, mask=w.mask,
+            key_lens=lens, stream=stream))
+        res[w.name + "_add_layernorm"] = {
+            "ms": ms_ln, "tflops": fl / (ms_ln * 1e-3) / 1e12, "flops": fl,
+            "kind": "LayerNorm(x + MHA(x)): W^O GEMM with residual add and normalisation "
+                    "in its epilogue (cluster per 128-row block)"}
     w = si.WORKLOADS[5]
     x = si.make_inputs(w)
     q, k, v = dv(x["q_bits"]), dv(x["k_bits"]), dv(x["v_bits"])

@@ -154,6 +154,34 @@ mha_status mha_forward(mha_dtype dt, const void *x_q, const void *x_kv, const vo
                        const int32_t *key_lens, int *status_dev, cudaStream_t stream);
 
 /*
+ * The attention sublayer with its residual connection and post-layer
+ * normalisation, bf16:
+ *   out = LayerNorm(x_q + MultiHead(x_q, x_kv)),
+ *   LayerNorm(v) = (v - mean(v)) / sqrt(var(v) + eps) * gamma + beta per row
+ * ("Attention Is All You Need" (aiany.app) Step 9, LayerNorm(x + Sublayer(x));
+ * notebook chapter "Layer Normalization and Residual Connections").  mean and
+ * var over the d_model features, var the population variance; eps >= 0 is the
+ * caller's (the pages print none; 1e-5 is usual).  gamma, beta: d_model bf16
+ * each, device, 16-byte aligned.  Other arguments, workspace and layouts as
+ * mha_forward; additionally d_model must be a multiple of 128 and at most 2048
+ * (else MHA_ERR_UNSUPPORTED).
+ *
+ * Three launches: the projection GEMM and attention as in mha_forward, then
+ * the output projection with the residual add and the normalisation in its
+ * epilogue -- a 128-row block is computed by a cluster of d_model/256 (or
+ * /128) CTAs that exchange per-row partial sums through distributed shared
+ * memory, so the normalised row never makes an extra trip through memory.
+ */
+mha_status mha_forward_add_layernorm(mha_dtype dt, const void *x_q, const void *x_kv,
+                                     const void *w_q, const void *w_k, const void *w_v,
+                                     const void *w_o, const void *gamma, const void *beta,
+                                     float eps, void *out, void *workspace,
+                                     size_t workspace_bytes, int B, int h, int T_q, int T_k,
+                                     int d_model, int d_k, int d_v, float scale, mha_mask mask,
+                                     const int32_t *key_lens, int *status_dev,
+                                     cudaStream_t stream);
+
+/*
  * Multi-head attention forward exactly as mha_forward, but with no workspace
  * argument: the scratch lives in a device array inside the library, so the
  * call allocates nothing.  (The pages have no counterpart: this is a

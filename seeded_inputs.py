@@ -37,7 +37,8 @@ _M1 = np.uint64(0xBF58476D1CE4E5B9)
 _M2 = np.uint64(0x94D049BB133111EB)
 
 TENSOR_IDS = {"x_q": 0, "x_kv": 1, "q": 2, "k": 3, "v": 4,
-              "w_q": 5, "w_k": 6, "w_v": 7, "w_o": 8, "key_lens": 9}
+              "w_q": 5, "w_k": 6, "w_v": 7, "w_o": 8, "key_lens": 9,
+              "ln_gamma": 10, "ln_beta": 11}
 
 MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING, MASK_CAUSAL_KEY_PADDING = 0, 1, 2, 3
 
@@ -89,6 +90,18 @@ def xavier_uniform(seed: int, tensor_id: int, shape, fan_in: int, fan_out: int) 
 def key_lengths(seed: int, batch: int, lo: int, hi: int) -> np.ndarray:
     u = uniform01(seed, TENSOR_IDS["key_lens"], batch)
     return (lo + np.floor(u * (hi - lo + 1))).astype(np.int32)
+
+
+def layernorm_params(seed: int, d_model: int) -> dict:
+    """Gain and shift of a layer normalisation, bf16: gamma = 1 + N(0,1)/8,
+    beta = N(0,1)/8 (learned values near their usual initialisation 1 and 0).
+    Returns float64 values and raw bits under 'gamma', 'beta', '*_bits'."""
+    out = {}
+    for name, base in (("gamma", 1.0), ("beta", 0.0)):
+        val = round_bf16(base + normal(seed, TENSOR_IDS["ln_" + name], (d_model,)) / 8.0)
+        out[name] = val
+        out[name + "_bits"] = f64_to_bf16_bits(val)
+    return out
 
 
 def f64_to_bf16_bits(x: np.ndarray) -> np.ndarray:

@@ -124,3 +124,22 @@ def test_decode_rejects_bad_arguments(lib):
     # empty problems are no-ops; T_k == 0 needs no cache pointers
     assert decode(lib, B=0) == lib.MHA_OK
     assert decode(lib, Tq=0) == lib.MHA_OK
+
+
+def mha_ln(lib, g=FAKE, b=FAKE, eps=1e-5, D=256, **kw):
+    x, ws = kw.get("x", FAKE), kw.get("ws", FAKE)
+    return lib.lib.mha_forward_add_layernorm(1, x, x, FAKE, FAKE, FAKE, FAKE, g, b, eps, FAKE, ws,
+                                             1 << 40, 1, 4, 8, 8, D, 64, 64, 0.125, 0, None, None,
+                                             None)
+
+
+def test_mha_add_layernorm_rejects_bad_arguments(lib):
+    assert mha_ln(lib, g=None) == lib.MHA_ERR_INVALID_ARG
+    assert mha_ln(lib, b=None) == lib.MHA_ERR_INVALID_ARG
+    assert mha_ln(lib, eps=-1.0) == lib.MHA_ERR_INVALID_ARG
+    assert mha_ln(lib, eps=float("nan")) == lib.MHA_ERR_INVALID_ARG
+    assert mha_ln(lib, g=FAKE + 2) == lib.MHA_ERR_MISALIGNED
+    # the normalised row must split into <= 8 blocks of 128 or 256 features
+    assert mha_ln(lib, D=192) == lib.MHA_ERR_UNSUPPORTED
+    assert mha_ln(lib, D=4096) == lib.MHA_ERR_UNSUPPORTED
+    assert mha_ln(lib, x=None) == lib.MHA_ERR_INVALID_ARG

@@ -267,3 +267,66 @@ def test_mha_config4_full(lib):
     w = si.WORKLOADS[3]
     x = si.make_inputs(w)
     check_bf16(run_mha(lib, w, x), oracle_mha(w, x), w.name)
+
+
+# ------------------------------------- attention sublayer: residual + LayerNorm
+def run_mha_ln(lib, w, x, ln, eps=1e-5):
+    xq = bf16_dev(x["x_q_bits"])
+    xkv = bf16_dev(x["x_kv_bits"]) if w.cross else xq
+    out = torch.full((w.B, w.T_q, w.d_model), float("nan"), dtype=torch.bfloat16, device=dev())
+    status = torch.zeros(1, dtype=torch.int32, device=dev())
+    lib.mha_forward_add_layernorm(xq, xkv, bf16_dev(x["w_q_bits"]), bf16_dev(x["w_k_bits"]),
+                                  bf16_dev(x["w_v_bits"]), bf16_dev(x["w_o_bits"]),
+                                  bf16_dev(ln["gamma_bits"]), bf16_dev(ln["beta_bits"]), h=w.h,
+                                  eps=eps, out=out, scale=w.scale, mask=w.mask,
+                                  key_lens=lens_dev(x), status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return host(out)
+
+
+def oracle_mha_ln(w, x, ln, eps=1e-5, query_rows=None):
+    x_kv = x["x_kv"] if w.cross else x["x_q"]
+    return oracle.mha_add_layernorm(x["x_q"], x_kv, x["w_q"], x["w_k"], x["w_v"], x["w_o"],
+                                    ln["gamma"], ln["beta"], h=w.h, eps=eps, scale=w.scale,
+                                    mask=w.mask, key_lens=x["key_lens"], query_rows=query_rows)
+
+
+MHA_LN_SHAPES = [
+    # B, T_q, T_k, D, h, mask, cross: D/256 or D/128 CTAs per 128-row block
+    (2, 130, 130, 128, 2, si.MASK_KEY_PADDING, False),   # 1 CTA of 128 columns
+    (1, 300, 300, 256, 4, si.MASK_CAUSAL, False),        # 1 CTA of 256
+    (2, 70, 333, 384, 6, si.MASK_KEY_PADDING, True),     # 3 CTAs of 128
+    (3, 200, 200, 512, 8, si.MASK_CAUSAL, False),        # 2 CTAs of 256
+    (1, 257, 129, 1024, 16, si.MASK_NONE, True),         # 4 CTAs of 256
+]
+
+
+@pytest.mark.parametrize("B,T_q,T_k,D,h,mask,cross", MHA_LN_SHAPES)
+def test_mha_add_layernorm_vs_oracle(lib, B, T_q, T_k, D, h, mask, cross):
+    w = si.WORKLOADS[3].replace(B=B, T_q=T_q, T_k=T_k, d_model=D, h=h, mask=mask, cross=cross,
+                                len_lo=1, len_hi=T_k, seed=71)
+    x = si.make_inputs(w)
+    ln = si.layernorm_params(71, D)
+    check_bf16(run_mha_ln(lib, w, x, ln), oracle_mha_ln(w, x, ln), "mha+ln D%d" % D)
+
+
+@pytest.mark.parametrize("idx", [1, 2, 3])
+def test_mha_add_layernorm_configs_full(lib, idx):
+    w = si.WORKLOADS[idx]
+    x = si.make_inputs(w)
+    ln = si.layernorm_params(w.seed, w.d_model)
+    check_bf16(run_mha_ln(lib, w, x, ln), oracle_mha_ln(w, x, ln), w.name + " + layer norm")
+
+
+def test_mha_add_layernorm_rows_are_normalised(lib):
+    # unit gain, zero shift: every output row has mean 0 and variance
+    # var/(var+eps) (up to bf16 rounding of the stored values)
+    w = si.WORKLOADS[2].replace(B=2, T_q=300, T_k=300, seed=72)
+    x = si.make_inputs(w)
+    D = w.d_model
+    ln = {"gamma": np.ones(D), "beta": np.zeros(D),
+          "gamma_bits": si.f64_to_bf16_bits(np.ones(D)), "beta_bits": si.f64_to_bf16_bits(np.zeros(D))}
+    y = run_mha_ln(lib, w, x, ln, eps=0.0)
+    assert np.abs(y.mean(axis=-1)).max() < 5e-3
+    assert np.abs((y ** 2).mean(axis=-1) - 1.0).max() < 1e-2

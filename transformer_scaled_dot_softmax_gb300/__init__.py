@@ -16,7 +16,7 @@ from . import _native
 from ._native import (MHA_BF16, MHA_F32, MHA_MASK_CAUSAL, MHA_MASK_CAUSAL_KEY_PADDING,
                       MHA_MASK_KEY_PADDING, MHA_MASK_NONE, MHA_OK, lib)
 
-__all__ = ["sdpa_forward", "sdpa_decode_forward", "mha_forward", "mha_workspace_bytes", "status_string", "MhaError",
+__all__ = ["sdpa_forward", "sdpa_decode_forward", "mha_forward", "mha_forward_add_layernorm", "mha_workspace_bytes", "status_string", "MhaError",
            "MASKS", "lib"]
 
 MASKS = {"none": MHA_MASK_NONE, "causal": MHA_MASK_CAUSAL, "key_padding": MHA_MASK_KEY_PADDING,
@@ -125,11 +125,8 @@ def mha_workspace_bytes(B, h, T_q, T_k, d_k=64, d_v=64) -> int:
     return int(lib.mha_workspace_bytes(B, h, T_q, T_k, d_k, d_v))
 
 
-def mha_forward(x_q, x_kv, w_q, w_k, w_v, w_o, h, out=None, workspace=None, *, scale=None,
-                mask="none", key_lens=None, status=None, stream=None):
-    """Concat_i(softmax(scale (x_q W_i^Q)(x_kv W_i^K)^T + mask)(x_kv W_i^V)) W^O
-    for bf16 CUDA tensors x_q (B,T_q,D), x_kv (B,T_k,D) (may be x_q),
-    W^Q/W^K/W^V (D, h*64), W^O (h*64, D).  Returns out (B,T_q,D)."""
+def _mha_call(x_q, x_kv, w_q, w_k, w_v, w_o, h, out, workspace, scale, mask, key_lens, status,
+              stream, ln):
     torch = _torch()
     bf = torch.bfloat16
     for n, t in (("x_q", x_q), ("x_kv", x_kv), ("w_q", w_q), ("w_k", w_k), ("w_v", w_v),
@@ -152,11 +149,42 @@ def mha_forward(x_q, x_kv, w_q, w_k, w_v, w_o, h, out=None, workspace=None, *, s
         _check_dev("status", status, torch.int32)
     if scale is None:
         scale = 1.0 / math.sqrt(d_k)
-    rc = lib.mha_forward(MHA_BF16, _ptr(x_q), _ptr(x_kv), _ptr(w_q), _ptr(w_k), _ptr(w_v),
-                         _ptr(w_o), _ptr(out), _ptr(workspace),
-                         workspace.numel() * workspace.element_size(), B, h, T_q, T_k, D, d_k,
-                         d_v, float(scale), _mask_code(mask), _ptr(key_lens), _ptr(status),
-                         _stream_handle(stream))
+    ws = (_ptr(workspace), workspace.numel() * workspace.element_size())
+    tail = (B, h, T_q, T_k, D, d_k, d_v, float(scale), _mask_code(mask), _ptr(key_lens),
+            _ptr(status), _stream_handle(stream))
+    if ln is None:
+        rc = lib.mha_forward(MHA_BF16, _ptr(x_q), _ptr(x_kv), _ptr(w_q), _ptr(w_k), _ptr(w_v),
+                             _ptr(w_o), _ptr(out), *ws, *tail)
+        what = "mha_forward"
+    else:
+        gamma, beta, eps = ln
+        _check_dev("gamma", gamma, bf)
+        _check_dev("beta", beta, bf)
+        if gamma.shape != (D,) or beta.shape != (D,):
+            raise ValueError("gamma and beta must have d_model entries")
+        rc = lib.mha_forward_add_layernorm(MHA_BF16, _ptr(x_q), _ptr(x_kv), _ptr(w_q), _ptr(w_k),
+                                           _ptr(w_v), _ptr(w_o), _ptr(gamma), _ptr(beta),
+                                           float(eps), _ptr(out), *ws, *tail)
+        what = "mha_forward_add_layernorm"
     if rc != MHA_OK:
-        raise MhaError(rc, "mha_forward")
+        raise MhaError(rc, what)
     return out
+
+
+def mha_forward(x_q, x_kv, w_q, w_k, w_v, w_o, h, out=None, workspace=None, *, scale=None,
+                mask="none", key_lens=None, status=None, stream=None):
+    """Concat_i(softmax(scale (x_q W_i^Q)(x_kv W_i^K)^T + mask)(x_kv W_i^V)) W^O
+    for bf16 CUDA tensors x_q (B,T_q,D), x_kv (B,T_k,D) (may be x_q),
+    W^Q/W^K/W^V (D, h*64), W^O (h*64, D).  Returns out (B,T_q,D)."""
+    return _mha_call(x_q, x_kv, w_q, w_k, w_v, w_o, h, out, workspace, scale, mask, key_lens,
+                     status, stream, None)
+
+
+def mha_forward_add_layernorm(x_q, x_kv, w_q, w_k, w_v, w_o, gamma, beta, h, eps=1e-5,
+                              out=None, workspace=None, *, scale=None, mask="none",
+                              key_lens=None, status=None, stream=None):
+    """LayerNorm(x_q + mha_forward(...)) with gain gamma and shift beta (bf16,
+    d_model entries each): the attention sublayer with its residual
+    connection and post-normalisation.  Returns out (B,T_q,D)."""
+    return _mha_call(x_q, x_kv, w_q, w_k, w_v, w_o, h, out, workspace, scale, mask, key_lens,
+                     status, stream, (gamma, beta, eps))

@@ -26,6 +26,9 @@ SIGNATURES = {
     "mha_workspace_bytes": (_sz, [_ci, _ci, _ci, _ci, _ci, _ci]),
     "mha_forward": (_ci, [_ci, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _ci, _ci, _ci, _ci,
                           _ci, _ci, _ci, _cf, _ci, _vp, _vp, _vp]),
+    "mha_forward_add_layernorm": (_ci, [_ci, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _cf, _vp, _vp,
+                                        _sz, _ci, _ci, _ci, _ci, _ci, _ci, _ci, _cf, _ci, _vp, _vp,
+                                        _vp]),
     "mha_forward_static_workspace": (_ci, [_ci, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci,
                                            _ci, _ci, _ci, _ci, _cf, _ci, _vp, _vp, _vp]),
     "mha_status_string": (ctypes.c_char_p, [_ci]),

@@ -236,12 +236,20 @@ MHA_EXPORT size_t mha_workspace_bytes(int B, int h, int T_q, int T_k, int d_k, i
            round256(bh * T_k * d_v * 2) + round256(bh * T_q * d_v * 2);
 }
 
-MHA_EXPORT mha_status mha_forward(mha_dtype dt, const void *x_q, const void *x_kv,
-                                  const void *w_q, const void *w_k, const void *w_v,
-                                  const void *w_o, void *out, void *workspace,
-                                  size_t workspace_bytes, int B, int h, int T_q, int T_k,
-                                  int d_model, int d_k, int d_v, float scale, mha_mask mask,
-                                  const int32_t *key_lens, int *status_dev, cudaStream_t stream) {
+namespace {
+
+// Residual + layer normalisation applied after the output projection.
+struct LnArgs {
+    const void *gamma, *beta;
+    float eps;
+};
+
+mha_status mha_impl(mha_dtype dt, const void *x_q, const void *x_kv, const void *w_q,
+                    const void *w_k, const void *w_v, const void *w_o, void *out,
+                    void *workspace, size_t workspace_bytes, int B, int h, int T_q, int T_k,
+                    int d_model, int d_k, int d_v, float scale, mha_mask mask,
+                    const int32_t *key_lens, int *status_dev, cudaStream_t stream,
+                    const LnArgs *ln) {
     if (B < 0 || h <= 0 || T_q < 0 || T_k < 0 || d_model <= 0 || d_k <= 0 || d_v <= 0)
         return MHA_ERR_INVALID_ARG;
     if (!valid_mask(mask) || !isfinite(scale)) return MHA_ERR_INVALID_ARG;
@@ -249,6 +257,8 @@ MHA_EXPORT mha_status mha_forward(mha_dtype dt, const void *x_q, const void *x_k
     if (dt != MHA_BF16) return dt == MHA_F32 ? MHA_ERR_UNSUPPORTED : MHA_ERR_INVALID_ARG;
     if (d_k != 64 || d_v != 64) return MHA_ERR_UNSUPPORTED;
     if (d_model % 64 != 0) return MHA_ERR_UNSUPPORTED;
+    if (ln && mha::ln_tile_width(d_model) == 0) return MHA_ERR_UNSUPPORTED;
+    if (ln && !(ln->eps >= 0.f && isfinite(ln->eps))) return MHA_ERR_INVALID_ARG;
     if (static_cast<long long>(B) * h >= (1ll << 31) ||
         static_cast<long long>(B) * (T_q > T_k ? T_q : T_k) >= (1ll << 31))
         return MHA_ERR_UNSUPPORTED;
@@ -256,6 +266,8 @@ MHA_EXPORT mha_status mha_forward(mha_dtype dt, const void *x_q, const void *x_k
     if (B == 0 || T_q == 0) return MHA_OK;
     if (!x_q || !out || !w_q || !w_o || (T_k > 0 && (!x_kv || !w_k || !w_v)))
         return MHA_ERR_INVALID_ARG;
+    if (ln && (!ln->gamma || !ln->beta)) return MHA_ERR_INVALID_ARG;
+    if (ln && (!aligned16(ln->gamma) || !aligned16(ln->beta))) return MHA_ERR_MISALIGNED;
     if (!workspace || workspace_bytes < mha_workspace_bytes(B, h, T_q, T_k, d_k, d_v))
         return MHA_ERR_WORKSPACE;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MHA_ERR_MISALIGNED;
@@ -326,7 +338,26 @@ MHA_EXPORT mha_status mha_forward(mha_dtype dt, const void *x_q, const void *x_k
                                 mask, key_lens, status_dev, stream)) != MHA_OK)
         return s;
 
-    // 3. Output projection Concat(heads) W^O.
+    // 3. Output projection Concat(heads) W^O, alone or fused with the
+    //    residual connection and layer normalisation.
+    if (ln) {
+        mha::LnParams lp{};
+        lp.M = static_cast<int>(Mq);
+        lp.D = d_model;
+        lp.K = hd;
+        lp.bn = mha::ln_tile_width(d_model);
+        lp.resid = static_cast<const __nv_bfloat16 *>(x_q);
+        lp.gamma = static_cast<const __nv_bfloat16 *>(ln->gamma);
+        lp.beta = static_cast<const __nv_bfloat16 *>(ln->beta);
+        lp.eps = ln->eps;
+        lp.out = static_cast<__nv_bfloat16 *>(out);
+        lp.status = status_dev;
+        CUtensorMap la, lb;
+        if ((s = encode_act(&la, om, Mq, hd)) != MHA_OK) return s;
+        if ((s = encode_weight(&lb, w_o, hd, d_model, lp.bn)) != MHA_OK) return s;
+        return launch_status(mha::launch_gemm_ln_bf16(la, lb, lp, stream),
+                             "output projection + layer norm launch");
+    }
     mha::GemmParams go{};
     go.status = status_dev;
     go.bn = choose_bn(&Mq, 1, d_model, sms);
@@ -350,4 +381,28 @@ MHA_EXPORT mha_status mha_forward(mha_dtype dt, const void *x_q, const void *x_k
     go.num_problems = 1;
     go.total_tiles = pr.tile_count;
     return launch_status(mha::launch_gemm_bf16(ta, tb, go, stream), "output GEMM launch");
+}
+
+}  // namespace
+
+MHA_EXPORT mha_status mha_forward(mha_dtype dt, const void *x_q, const void *x_kv,
+                                  const void *w_q, const void *w_k, const void *w_v,
+                                  const void *w_o, void *out, void *workspace,
+                                  size_t workspace_bytes, int B, int h, int T_q, int T_k,
+                                  int d_model, int d_k, int d_v, float scale, mha_mask mask,
+                                  const int32_t *key_lens, int *status_dev, cudaStream_t stream) {
+    return mha_impl(dt, x_q, x_kv, w_q, w_k, w_v, w_o, out, workspace, workspace_bytes, B, h,
+                    T_q, T_k, d_model, d_k, d_v, scale, mask, key_lens, status_dev, stream,
+                    nullptr);
+}
+
+MHA_EXPORT mha_status mha_forward_add_layernorm(
+    mha_dtype dt, const void *x_q, const void *x_kv, const void *w_q, const void *w_k,
+    const void *w_v, const void *w_o, const void *gamma, const void *beta, float eps, void *out,
+    void *workspace, size_t workspace_bytes, int B, int h, int T_q, int T_k, int d_model,
+    int d_k, int d_v, float scale, mha_mask mask, const int32_t *key_lens, int *status_dev,
+    cudaStream_t stream) {
+    const LnArgs ln{gamma, beta, eps};
+    return mha_impl(dt, x_q, x_kv, w_q, w_k, w_v, w_o, out, workspace, workspace_bytes, B, h,
+                    T_q, T_k, d_model, d_k, d_v, scale, mask, key_lens, status_dev, stream, &ln);
 }

@@ -78,4 +78,24 @@ cudaError_t launch_gemm_bf16(const CUtensorMap (&a)[kGemmMaxProblems],
 // Number of SMs of the current device.
 cudaError_t sm_count(int *sms);
 
+// ------------------------------------ output projection + residual + LayerNorm
+constexpr int kLnMaxCluster = 8;  // CTAs per 128-row block (portable cluster size)
+struct LnParams {
+    int M, D, K;                  // out (M, D) = LN(resid + A (M, K) W (K, D))
+    int bn;                       // columns per CTA: ln_tile_width(D)
+    const __nv_bfloat16 *resid;   // (M, D)
+    const __nv_bfloat16 *gamma;   // (D)
+    const __nv_bfloat16 *beta;    // (D)
+    float eps;
+    __nv_bfloat16 *out;           // (M, D)
+    int *status;
+};
+// 256 or 128 columns per CTA for a row of D features (D / width CTAs <= 8), or
+// 0 if D is not supported.
+int ln_tile_width(int D);
+// a: 2-D TMA map over A (K inner, M rows), box (64, 128); b: 3-D map over W
+// viewed as (64, K, D/64), box (64, 64, bn/64).
+cudaError_t launch_gemm_ln_bf16(const CUtensorMap &a, const CUtensorMap &b, const LnParams &p,
+                                cudaStream_t stream);
+
 }  // namespace mha
