@@ -295,10 +295,11 @@ def oracle_mha_ln(w, x, ln, eps=1e-5, query_rows=None):
 MHA_LN_SHAPES = [
     # B, T_q, T_k, D, h, mask, cross: D/256 or D/128 CTAs per 128-row block
     (2, 130, 130, 128, 2, si.MASK_KEY_PADDING, False),   # 1 CTA of 128 columns
-    (1, 300, 300, 256, 4, si.MASK_CAUSAL, False),        # 1 CTA of 256
+    (1, 300, 300, 256, 4, si.MASK_CAUSAL, False),        # 2 CTAs of 128
     (2, 70, 333, 384, 6, si.MASK_KEY_PADDING, True),     # 3 CTAs of 128
-    (3, 200, 200, 512, 8, si.MASK_CAUSAL, False),        # 2 CTAs of 256
+    (3, 200, 200, 512, 8, si.MASK_CAUSAL, False),        # 4 CTAs of 128
     (1, 257, 129, 1024, 16, si.MASK_NONE, True),         # 4 CTAs of 256
+    (1, 130, 130, 2048, 32, si.MASK_CAUSAL, False),      # 8 CTAs of 256
 ]
 
 

@@ -257,7 +257,7 @@ mha_status mha_impl(mha_dtype dt, const void *x_q, const void *x_kv, const void 
     if (dt != MHA_BF16) return dt == MHA_F32 ? MHA_ERR_UNSUPPORTED : MHA_ERR_INVALID_ARG;
     if (d_k != 64 || d_v != 64) return MHA_ERR_UNSUPPORTED;
     if (d_model % 64 != 0) return MHA_ERR_UNSUPPORTED;
-    if (ln && mha::ln_tile_width(d_model) == 0) return MHA_ERR_UNSUPPORTED;
+    if (ln && mha::ln_tile_width(d_model, 1, 1) == 0) return MHA_ERR_UNSUPPORTED;
     if (ln && !(ln->eps >= 0.f && isfinite(ln->eps))) return MHA_ERR_INVALID_ARG;
     if (static_cast<long long>(B) * h >= (1ll << 31) ||
         static_cast<long long>(B) * (T_q > T_k ? T_q : T_k) >= (1ll << 31))
@@ -345,7 +345,7 @@ mha_status mha_impl(mha_dtype dt, const void *x_q, const void *x_kv, const void 
         lp.M = static_cast<int>(Mq);
         lp.D = d_model;
         lp.K = hd;
-        lp.bn = mha::ln_tile_width(d_model);
+        lp.bn = mha::ln_tile_width(d_model, Mq, sms);
         lp.resid = static_cast<const __nv_bfloat16 *>(x_q);
         lp.gamma = static_cast<const __nv_bfloat16 *>(ln->gamma);
         lp.beta = static_cast<const __nv_bfloat16 *>(ln->beta);

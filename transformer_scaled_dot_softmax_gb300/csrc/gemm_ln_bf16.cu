@@ -312,9 +312,16 @@ cudaError_t launch_bn(const CUtensorMap &a, const CUtensorMap &b, const LnParams
 
 }  // namespace
 
-int ln_tile_width(int D) {
-    if (D % 256 == 0 && D / 256 <= kLnMaxCluster) return 256;
-    if (D % 128 == 0 && D / 128 <= kLnMaxCluster) return 128;
+int ln_tile_width(int D, long long M, int sms) {
+    const bool w256 = D % 256 == 0 && D / 256 <= kLnMaxCluster;
+    const bool w128 = D % 128 == 0 && D / 128 <= kLnMaxCluster;
+    // 256 columns per CTA read each A tile once per 256 outputs; 128 columns
+    // double the CTAs.  Measured on GB300 (self / causal / cross MHA
+    // workloads), the narrower tiles pay only while 256-wide blocks would fill
+    // less than half of the SMs and the cluster stays at 4 CTAs or fewer.
+    const long long blocks256 = (M + BM - 1) / BM * (D / 256);
+    if (w128 && (!w256 || (2 * blocks256 < sms && D / 128 <= 4))) return 128;
+    if (w256) return 256;
     return 0;
 }
 

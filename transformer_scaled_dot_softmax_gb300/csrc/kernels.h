@@ -90,9 +90,9 @@ struct LnParams {
     __nv_bfloat16 *out;           // (M, D)
     int *status;
 };
-// 256 or 128 columns per CTA for a row of D features (D / width CTAs <= 8), or
-// 0 if D is not supported.
-int ln_tile_width(int D);
+// 256 or 128 columns per CTA for rows of D features (D / width CTAs <= 8) over
+// M rows on `sms` SMs, or 0 if D is not supported.
+int ln_tile_width(int D, long long M, int sms);
 // a: 2-D TMA map over A (K inner, M rows), box (64, 128); b: 3-D map over W
 // viewed as (64, K, D/64), box (64, 64, bn/64).
 cudaError_t launch_gemm_ln_bf16(const CUtensorMap &a, const CUtensorMap &b, const LnParams &p,
