@@ -42,6 +42,8 @@ def _load():
         lib.oracle_mha.argtypes = [dp, dp, dp, dp, dp, dp, dp, ci, ci, ci, ci, ci, ci, ci, cd,
                                    ci, ip, lp, cl]
         lib.oracle_mha.restype = ci
+        lib.oracle_sdpa_lse.argtypes = [dp, dp, dp, ci, ci, ci, ci, ci, cd, ci, ip]
+        lib.oracle_sdpa_lse.restype = ci
         lib.oracle_add_layernorm.argtypes = [dp, dp, dp, dp, cd, dp, cl, ci]
         lib.oracle_add_layernorm.restype = ci
         lib.oracle_num_threads.argtypes = []
@@ -168,3 +170,22 @@ def mha_add_layernorm(x_q, x_kv, w_q, w_k, w_v, w_o, gamma, beta, h, eps=1e-5, s
     xq = _d(x_q).reshape(-1, out.shape[-1])
     res = xq if query_rows is None else xq[np.asarray(query_rows, dtype=np.int64)]
     return add_layernorm(res.reshape(out.shape), out, gamma, beta, eps)
+
+
+def sdpa_lse(q, k, scale=None, mask=MASK_NONE, key_lens=None):
+    """Per query row log sum_{visible j} exp(scale q.k_j), shape (B,H,Tq);
+    -inf for a row with no visible key."""
+    q, k = _d(q), _d(k)
+    B, H, Tq, dk = q.shape
+    Tk = k.shape[2]
+    if k.shape != (B, H, Tk, dk):
+        raise ValueError("shape mismatch")
+    if scale is None:
+        scale = 1.0 / np.sqrt(dk)
+    kl = _lens(key_lens, B)
+    lse = np.empty((B, H, Tq))
+    rc = _load().oracle_sdpa_lse(_p(q), _p(k), _p(lse), B, H, Tq, Tk, dk, float(scale),
+                                 int(mask), _p(kl, ctypes.c_int32))
+    if rc:
+        raise RuntimeError("oracle_sdpa_lse failed")
+    return lse

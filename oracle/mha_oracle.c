@@ -296,6 +296,55 @@ done:
 }
 
 /*
+ * Log-sum-exp of each query row's visible scores,
+ *   lse_i = log sum_{j visible} exp(scale * q_i . k_j),
+ * the normaliser of the softmax (its denominator in log form; the weights
+ * are exp(s_j - lse_i)).  Computed as m + log(sum exp(s_j - m)) with m the row
+ * maximum, an exact identity.  -inf for a row with no visible key.
+ * q (B,H,Tq,dk), k (B,H,Tk,dk), lse (B,H,Tq).
+ */
+int oracle_sdpa_lse(const double *q, const double *k, double *lse, int B, int H, int Tq, int Tk,
+                    int dk, double scale, int mask_kind, const int32_t *key_lens)
+{
+    if (B < 0 || H < 0 || Tq < 0 || Tk < 0 || dk <= 0)
+        return -1;
+    long rows = (long)B * H * Tq;
+#pragma omp parallel for schedule(dynamic, 16)
+    for (long r = 0; r < rows; ++r) {
+        const int i = (int)(r % Tq);
+        const long bh = r / Tq;
+        const int b = (int)(bh / H);
+        const double *qi = q + (size_t)r * dk;
+        const double *kb = k + (size_t)bh * Tk * dk;
+        double m = -INFINITY;
+        for (int j = 0; j < Tk; ++j) {
+            if (!key_visible(mask_kind, key_lens, b, i, j))
+                continue;
+            double dot = 0.0;
+            for (int c = 0; c < dk; ++c)
+                dot += qi[c] * kb[(size_t)j * dk + c];
+            if (scale * dot > m)
+                m = scale * dot;
+        }
+        if (m == -INFINITY) {
+            lse[r] = -INFINITY;
+            continue;
+        }
+        double sum = 0.0;
+        for (int j = 0; j < Tk; ++j) {
+            if (!key_visible(mask_kind, key_lens, b, i, j))
+                continue;
+            double dot = 0.0;
+            for (int c = 0; c < dk; ++c)
+                dot += qi[c] * kb[(size_t)j * dk + c];
+            sum += exp(scale * dot - m);
+        }
+        lse[r] = m + log(sum);
+    }
+    return 0;
+}
+
+/*
  * Residual connection and layer normalisation around a sublayer, per row:
  *   v = x + s  (the sublayer's input added back to its output),
  *   y = (v - mu) / sigma * gamma + beta,

@@ -35,6 +35,8 @@ MUTATIONS = [
     ("layer norm gain and shift swapped", "* gamma[c] + beta[c];", "* beta[c] + gamma[c];"),
     ("residual left out of the normalised value", "yr[c] = (xr[c] + sr[c] - mu)",
      "yr[c] = (sr[c] - mu)"),
+    ("log-sum-exp without its maximum", "lse[r] = m + log(sum);", "lse[r] = log(sum);"),
+    ("log-sum-exp sum without the scale", "sum += exp(scale * dot - m);", "sum += exp(dot - m);"),
 ]
 
 

@@ -451,3 +451,44 @@ def test_mha_add_layernorm_with_zero_output_projection_normalises_the_input():
     full = oracle.mha_add_layernorm(x, x, *w, w_o, g, b, h=h, mask=MASK_CAUSAL)
     part = oracle.mha_add_layernorm(x, x, *w, w_o, g, b, h=h, mask=MASK_CAUSAL, query_rows=rows)
     np.testing.assert_allclose(part, full.reshape(-1, D)[rows], rtol=0, atol=1e-13)
+
+
+# ----------------------------------------------------------- log-sum-exp
+@pytest.mark.parametrize("mask", [MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING])
+def test_lse_matches_torch_logsumexp(mask):
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(81)
+    q, k = rng.normal(size=(2, 3, 9, 8)), rng.normal(size=(2, 3, 11, 8))
+    lens = np.array([11, 4], dtype=np.int32)
+    scale = 0.37
+    s = torch.from_numpy(np.einsum("bhqd,bhkd->bhqk", q, k) * scale)
+    i = torch.arange(9)[:, None]
+    j = torch.arange(11)[None, :]
+    vis = torch.ones(2, 1, 9, 11, dtype=torch.bool)
+    if mask & MASK_CAUSAL:
+        vis = vis & (j <= i)
+    if mask & MASK_KEY_PADDING:
+        vis = vis & (j[None, None] < torch.from_numpy(lens)[:, None, None, None])
+    ref = torch.logsumexp(s.masked_fill(~vis, float("-inf")), dim=-1).numpy()
+    got = oracle.sdpa_lse(q, k, scale=scale, mask=mask,
+                          key_lens=lens if mask & MASK_KEY_PADDING else None)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-12)
+
+
+def test_lse_closed_forms_and_consistency_with_weights():
+    # equal scores s over n visible keys: lse = s + log n
+    q = np.ones((1, 1, 3, 4))
+    k = np.full((1, 1, 5, 4), 0.5)  # q.k = 2 for every key
+    got = oracle.sdpa_lse(q, k, scale=1.5, mask=MASK_CAUSAL)
+    np.testing.assert_allclose(got[0, 0], [3.0 + math.log(1), 3.0 + math.log(2), 3.0 + math.log(3)],
+                               atol=1e-14)
+    # weights are exp(s - lse)
+    rng = np.random.default_rng(82)
+    q, k, v = rng.normal(size=(1, 2, 6, 8)), rng.normal(size=(1, 2, 7, 8)), rng.normal(size=(1, 2, 7, 8))
+    _, w = oracle.sdpa(q, k, v, scale=0.5, return_weights=True)
+    lse = oracle.sdpa_lse(q, k, scale=0.5)
+    s = np.einsum("bhqd,bhkd->bhqk", q, k) * 0.5
+    np.testing.assert_allclose(w, np.exp(s - lse[..., None]), atol=1e-14)
+    # no visible key: -inf
+    got = oracle.sdpa_lse(q, k, scale=0.5, mask=MASK_KEY_PADDING, key_lens=np.array([0], np.int32))
+    assert np.all(np.isneginf(got))
