@@ -67,6 +67,15 @@ static int key_visible(int mask_kind, const int32_t *key_lens, int b, int i, int
     return 1;
 }
 
+/* q_i . k_j over the dk key features. */
+static double qk_dot(const double *qi, const double *kb, int j, int dk)
+{
+    double dot = 0.0;
+    for (int c = 0; c < dk; ++c)
+        dot += qi[c] * kb[(size_t)j * dk + c];
+    return dot;
+}
+
 /* One output row of scaled dot-product attention.
  * qi: dk values; kb: Tk x dk; vb: Tk x dv; oi: dv values out;
  * wi: Tk weights out (may be NULL); s: Tk doubles of scratch. */
@@ -79,9 +88,7 @@ static void sdpa_row(const double *qi, const double *kb, const double *vb, doubl
     for (int j = 0; j < Tk; ++j) {
         if (!key_visible(mask_kind, key_lens, b, i, j))
             continue;
-        double dot = 0.0;
-        for (int c = 0; c < dk; ++c)
-            dot += qi[c] * kb[(size_t)j * dk + c];
+        const double dot = qk_dot(qi, kb, j, dk);
         s[j] = scale * dot;
         if (!any || s[j] > m)
             m = s[j];
@@ -320,9 +327,7 @@ int oracle_sdpa_lse(const double *q, const double *k, double *lse, int B, int H,
         for (int j = 0; j < Tk; ++j) {
             if (!key_visible(mask_kind, key_lens, b, i, j))
                 continue;
-            double dot = 0.0;
-            for (int c = 0; c < dk; ++c)
-                dot += qi[c] * kb[(size_t)j * dk + c];
+            const double dot = qk_dot(qi, kb, j, dk);
             if (scale * dot > m)
                 m = scale * dot;
         }
@@ -334,9 +339,7 @@ int oracle_sdpa_lse(const double *q, const double *k, double *lse, int B, int H,
         for (int j = 0; j < Tk; ++j) {
             if (!key_visible(mask_kind, key_lens, b, i, j))
                 continue;
-            double dot = 0.0;
-            for (int c = 0; c < dk; ++c)
-                dot += qi[c] * kb[(size_t)j * dk + c];
+            const double dot = qk_dot(qi, kb, j, dk);
             sum += exp(scale * dot - m);
         }
         lse[r] = m + log(sum);
