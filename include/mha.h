@@ -95,6 +95,20 @@ mha_status sdpa_forward(mha_dtype dt, const void *q, const void *k, const void *
                         cudaStream_t stream);
 
 /*
+ * sdpa_forward (bf16 only) that also writes, per query row, the log-sum-exp of
+ * its visible scores,
+ *   lse[b, h, i] = log sum_{j visible} exp(scale * q_i . k_j)   (natural log),
+ * the softmax normaliser (the weights are exp(scale q_i.k_j - lse)), which a
+ * backward pass needs to recompute the weights.  lse: DEVICE fp32 array of
+ * B*h*T_q entries (required when the problem is not empty); -inf for a row
+ * with no visible key.  MHA_F32 returns MHA_ERR_UNSUPPORTED.
+ */
+mha_status sdpa_forward_lse(mha_dtype dt, const void *q, const void *k, const void *v, void *o,
+                            float *lse, int B, int h, int T_q, int T_k, int d_k, int d_v,
+                            float scale, mha_mask mask, const int32_t *key_lens, int *status_dev,
+                            cudaStream_t stream);
+
+/*
  * Attention for decoding steps (bf16): each of the T_q new query rows of a
  * (b, h) attends to the first cache_lens[b] rows of that sequence's key/value
  * cache,

@@ -143,3 +143,12 @@ def test_mha_add_layernorm_rejects_bad_arguments(lib):
     assert mha_ln(lib, D=192) == lib.MHA_ERR_UNSUPPORTED
     assert mha_ln(lib, D=4096) == lib.MHA_ERR_UNSUPPORTED
     assert mha_ln(lib, x=None) == lib.MHA_ERR_INVALID_ARG
+
+
+def test_sdpa_lse_rejects_bad_arguments(lib):
+    f = lib.lib.sdpa_forward_lse
+    args = lambda dt=1, lse=FAKE, B=1: (dt, FAKE, FAKE, FAKE, FAKE, lse, B, 1, 8, 8, 64, 64, 0.125,
+                                        0, None, None, None)
+    assert f(*args(lse=None)) == lib.MHA_ERR_INVALID_ARG
+    assert f(*args(dt=0)) == lib.MHA_ERR_UNSUPPORTED
+    assert f(*args(lse=None, B=0)) == lib.MHA_OK

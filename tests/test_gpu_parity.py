@@ -331,3 +331,49 @@ def test_mha_add_layernorm_rows_are_normalised(lib):
     y = run_mha_ln(lib, w, x, ln, eps=0.0)
     assert np.abs(y.mean(axis=-1)).max() < 5e-3
     assert np.abs((y ** 2).mean(axis=-1) - 1.0).max() < 1e-2
+
+
+# ------------------------------------------------------- log-sum-exp export
+# lse comes from fp32 sums of ex2.approx terms (relative error ~2^-22 each,
+# fp32 accumulation over up to 8192 keys): 1e-3 absolute covers it.
+LSE_TOL = 1e-3
+
+
+def run_sdpa_lse(lib, w, x, k=None):
+    q = bf16_dev(x["q_bits"])
+    k = bf16_dev(x["k_bits"]) if k is None else k
+    v = bf16_dev(x["v_bits"])
+    out, lse = lib.sdpa_forward_lse(q, k, v, scale=w.scale, mask=w.mask, key_lens=lens_dev(x))
+    torch.cuda.synchronize()
+    return out, lse.double().cpu().numpy()
+
+
+def check_lse(got, ref, what):
+    inf = np.isneginf(ref)
+    assert np.array_equal(np.isneginf(got), inf), what + ": -inf rows differ"
+    err = np.abs(got[~inf] - ref[~inf])
+    assert err.size == 0 or err.max() <= LSE_TOL, "%s: lse max err %.3g" % (what, err.max())
+
+
+@pytest.mark.parametrize("B,h,T_q,T_k,mask", BF16_SHAPES + [(1, 2, 2048, 2048, si.MASK_CAUSAL)])
+def test_bf16_lse_vs_oracle(lib, B, h, T_q, T_k, mask):
+    w = si.WORKLOADS[4].replace(B=B, h=h, T_q=T_q, T_k=T_k, mask=mask, len_lo=0, len_hi=T_k,
+                                seed=91)
+    x = si.make_inputs(w)
+    out, lse = run_sdpa_lse(lib, w, x)
+    ref_o = oracle.sdpa(x["q"], x["k"], x["v"], scale=w.scale, mask=mask, key_lens=x["key_lens"])
+    check_bf16(host(out), ref_o, "lse call output")
+    ref = oracle.sdpa_lse(x["q"], x["k"], scale=w.scale, mask=mask, key_lens=x["key_lens"])
+    check_lse(lse, ref, "B%d h%d Tq%d Tk%d mask%d" % (B, h, T_q, T_k, mask))
+
+
+@pytest.mark.parametrize("profile", ["growing", "jump"])
+def test_bf16_lse_across_reference_updates(lib, profile):
+    w = si.WORKLOADS[4].replace(B=1, h=2, T_q=1024, T_k=1024, mask=si.MASK_CAUSAL, seed=92)
+    x = si.make_inputs(w)
+    f = {"growing": [6 * j + 1 for j in range(8)], "jump": [80 if j in (2, 5) else 1 for j in range(8)]}[profile]
+    k = si.round_bf16(x["k"] * np.repeat(np.array(f, dtype=np.float64), 128)[None, None, :, None])
+    out, lse = run_sdpa_lse(lib, w, x, k=bf16_dev(si.f64_to_bf16_bits(k)))
+    ref = oracle.sdpa_lse(x["q"], k, scale=w.scale, mask=w.mask)
+    # large scores: compare relative to the row's magnitude
+    assert np.all(np.abs(lse - ref) <= LSE_TOL * np.maximum(1.0, np.abs(ref)))

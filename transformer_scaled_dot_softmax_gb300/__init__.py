@@ -16,7 +16,7 @@ from . import _native
 from ._native import (MHA_BF16, MHA_F32, MHA_MASK_CAUSAL, MHA_MASK_CAUSAL_KEY_PADDING,
                       MHA_MASK_KEY_PADDING, MHA_MASK_NONE, MHA_OK, lib)
 
-__all__ = ["sdpa_forward", "sdpa_decode_forward", "mha_forward", "mha_forward_add_layernorm", "mha_workspace_bytes", "status_string", "MhaError",
+__all__ = ["sdpa_forward", "sdpa_forward_lse", "sdpa_decode_forward", "mha_forward", "mha_forward_add_layernorm", "mha_workspace_bytes", "status_string", "MhaError",
            "MASKS", "lib"]
 
 MASKS = {"none": MHA_MASK_NONE, "causal": MHA_MASK_CAUSAL, "key_padding": MHA_MASK_KEY_PADDING,
@@ -93,6 +93,36 @@ def sdpa_forward(q, k, v, out=None, *, scale=None, mask="none", key_lens=None, s
     if rc != MHA_OK:
         raise MhaError(rc, "sdpa_forward")
     return out
+
+
+def sdpa_forward_lse(q, k, v, out=None, lse=None, *, scale=None, mask="none", key_lens=None,
+                     status=None, stream=None):
+    """sdpa_forward for bf16 tensors that also returns the per-row
+    log-sum-exp of the visible scores, lse (B,h,T_q) fp32 (natural log; -inf
+    for a row with no visible key).  Returns (out, lse)."""
+    torch = _torch()
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _check_dev(n, t, torch.bfloat16)
+    B, h, T_q, d_k = q.shape
+    T_k, d_v = k.shape[2], v.shape[3]
+    if out is None:
+        out = torch.empty((B, h, T_q, d_v), dtype=torch.bfloat16, device=q.device)
+    if lse is None:
+        lse = torch.empty((B, h, T_q), dtype=torch.float32, device=q.device)
+    _check_dev("out", out, torch.bfloat16)
+    _check_dev("lse", lse, torch.float32)
+    if key_lens is not None:
+        _check_dev("key_lens", key_lens, torch.int32)
+    if status is not None:
+        _check_dev("status", status, torch.int32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_k)
+    rc = lib.sdpa_forward_lse(MHA_BF16, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, h,
+                              T_q, T_k, d_k, d_v, float(scale), _mask_code(mask), _ptr(key_lens),
+                              _ptr(status), _stream_handle(stream))
+    if rc != MHA_OK:
+        raise MhaError(rc, "sdpa_forward_lse")
+    return out, lse
 
 
 def sdpa_decode_forward(q, k_cache, v_cache, cache_lens=None, out=None, *, scale=None,

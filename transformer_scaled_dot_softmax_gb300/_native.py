@@ -21,6 +21,8 @@ _vp, _ci, _cf, _sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_siz
 SIGNATURES = {
     "sdpa_forward": (_ci, [_ci, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _ci, _cf, _ci, _vp,
                            _vp, _vp]),
+    "sdpa_forward_lse": (_ci, [_ci, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _ci, _cf,
+                               _ci, _vp, _vp, _vp]),
     "sdpa_decode_forward": (_ci, [_vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _ci, _cf, _vp,
                                   _vp]),
     "mha_workspace_bytes": (_sz, [_ci, _ci, _ci, _ci, _ci, _ci]),

@@ -126,7 +126,7 @@ mha_status launch_status(cudaError_t e, const char *what) {
 mha_status run_attention_bf16(const void *q, const void *k, const void *v, void *o,
                               long long o_sb, long long o_sh, long long o_st, int B, int h,
                               int T_q, int T_k, float scale, int mask, const int32_t *key_lens,
-                              int *status_dev, cudaStream_t stream) {
+                              int *status_dev, cudaStream_t stream, float *lse = nullptr) {
     CUtensorMap tq, tk, tv;
     const long long BH = static_cast<long long>(B) * h;
     mha_status s;
@@ -142,6 +142,8 @@ mha_status run_attention_bf16(const void *q, const void *k, const void *v, void 
     p.Tq = T_q;
     p.Tk = T_k;
     p.scale_log2 = scale * 1.4426950408889634f;
+    p.scale = scale;
+    p.lse = lse;
     p.mask = mask;
     p.key_lens = key_lens;
     p.o = static_cast<__nv_bfloat16 *>(o);
@@ -173,16 +175,19 @@ MHA_EXPORT const char *mha_status_string(mha_status status) {
 
 MHA_EXPORT const char *mha_last_error(void) { return g_last_error; }
 
-MHA_EXPORT mha_status sdpa_forward(mha_dtype dt, const void *q, const void *k, const void *v,
-                                   void *o, int B, int h, int T_q, int T_k, int d_k, int d_v,
-                                   float scale, mha_mask mask, const int32_t *key_lens,
-                                   int *status_dev, cudaStream_t stream) {
+namespace {
+
+mha_status sdpa_impl(mha_dtype dt, const void *q, const void *k, const void *v, void *o,
+                     float *lse, int B, int h, int T_q, int T_k, int d_k, int d_v, float scale,
+                     mha_mask mask, const int32_t *key_lens, int *status_dev,
+                     cudaStream_t stream) {
     if (B < 0 || h < 0 || T_q < 0 || T_k < 0 || d_k <= 0 || d_v <= 0) return MHA_ERR_INVALID_ARG;
     if (!valid_mask(mask) || !isfinite(scale)) return MHA_ERR_INVALID_ARG;
     if ((mask & MHA_MASK_KEY_PADDING) && !key_lens) return MHA_ERR_INVALID_ARG;
     if (static_cast<long long>(B) * h >= (1ll << 31)) return MHA_ERR_UNSUPPORTED;
     if (B == 0 || h == 0 || T_q == 0) return MHA_OK;
     if (!q || !o || (T_k > 0 && (!k || !v))) return MHA_ERR_INVALID_ARG;
+    if (lse && dt != MHA_BF16) return dt == MHA_F32 ? MHA_ERR_UNSUPPORTED : MHA_ERR_INVALID_ARG;
     if (dt == MHA_F32) {
         if (d_k > 128 || d_v > 128) return MHA_ERR_UNSUPPORTED;
         if ((T_q + 3) / 4 > 65535) return MHA_ERR_UNSUPPORTED;
@@ -198,7 +203,27 @@ MHA_EXPORT mha_status sdpa_forward(mha_dtype dt, const void *q, const void *k, c
         return MHA_ERR_MISALIGNED;
     const long long so_t = 64, so_h = static_cast<long long>(T_q) * 64, so_b = so_h * h;
     return run_attention_bf16(q, T_k > 0 ? k : q, T_k > 0 ? v : q, o, so_b, so_h, so_t, B, h,
-                              T_q, T_k, scale, mask, key_lens, status_dev, stream);
+                              T_q, T_k, scale, mask, key_lens, status_dev, stream, lse);
+}
+
+}  // namespace
+
+MHA_EXPORT mha_status sdpa_forward(mha_dtype dt, const void *q, const void *k, const void *v,
+                                   void *o, int B, int h, int T_q, int T_k, int d_k, int d_v,
+                                   float scale, mha_mask mask, const int32_t *key_lens,
+                                   int *status_dev, cudaStream_t stream) {
+    return sdpa_impl(dt, q, k, v, o, nullptr, B, h, T_q, T_k, d_k, d_v, scale, mask, key_lens,
+                     status_dev, stream);
+}
+
+MHA_EXPORT mha_status sdpa_forward_lse(mha_dtype dt, const void *q, const void *k, const void *v,
+                                       void *o, float *lse, int B, int h, int T_q, int T_k,
+                                       int d_k, int d_v, float scale, mha_mask mask,
+                                       const int32_t *key_lens, int *status_dev,
+                                       cudaStream_t stream) {
+    if (!lse && B > 0 && h > 0 && T_q > 0) return MHA_ERR_INVALID_ARG;
+    return sdpa_impl(dt, q, k, v, o, lse, B, h, T_q, T_k, d_k, d_v, scale, mask, key_lens,
+                     status_dev, stream);
 }
 
 MHA_EXPORT mha_status sdpa_decode_forward(const void *q, const void *k_cache,

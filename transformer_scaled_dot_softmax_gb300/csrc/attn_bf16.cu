@@ -518,10 +518,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             __nv_bfloat16 *dst = p.o + it.b * p.o_stride_b + it.hh * p.o_stride_h +
                                  static_cast<long long>(row) * p.o_stride_t;
             uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+            float *lse_row = p.lse && row < p.Tq
+                                 ? p.lse + (static_cast<long long>(it.bh) * p.Tq + row)
+                                 : nullptr;
             if (it.n_kv == 0) {
                 if (row < p.Tq) {
 #pragma unroll
                     for (int c = 0; c < 8; ++c) d4[c] = make_uint4(0u, 0u, 0u, 0u);
+                    if (lse_row) *lse_row = -INFINITY;
                 }
                 continue;
             }
@@ -538,6 +542,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float L = la * wa + lb * wb;
             const float inv = L > 0.f ? 1.0f / L : 0.f;
             const float fa = wa * inv, fb = wb * inv;
+            // Log-sum-exp of the row's visible scores: sum_j 2^(s_j c) =
+            // 2^(M c) L with c = scale log2(e), so lse = M scale + ln L.
+            if (lse_row) *lse_row = L > 0.f ? M * p.scale + logf(L) : -INFINITY;
 #pragma unroll
             for (int part = 0; part < 2; ++part) {
                 uint32_t oa[32], ob[32];

@@ -15,6 +15,8 @@ constexpr int kMaskPaddingBit = 2;
 struct AttnParams {
     int B, H, Tq, Tk;
     float scale_log2;  // scale * log2(e): scores are exponentiated with ex2
+    float scale;
+    float *lse;        // optional (B, H, Tq) fp32: log sum_j exp(scale q.k_j); null: not written
     int mask;          // kMaskCausalBit | kMaskPaddingBit
     const int32_t *key_lens;
     __nv_bfloat16 *o;  // output; element (b, h, t, c) at o + b*sb + h*sh + t*st + c
