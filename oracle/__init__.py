@@ -44,6 +44,9 @@ def _load():
         lib.oracle_mha.restype = ci
         lib.oracle_sdpa_lse.argtypes = [dp, dp, dp, ci, ci, ci, ci, ci, cd, ci, ip]
         lib.oracle_sdpa_lse.restype = ci
+        lib.oracle_sdpa_backward.argtypes = [dp, dp, dp, dp, dp, dp, dp, ci, ci, ci, ci, ci, cd,
+                                             ci, ip]
+        lib.oracle_sdpa_backward.restype = ci
         lib.oracle_add_layernorm.argtypes = [dp, dp, dp, dp, cd, dp, cl, ci]
         lib.oracle_add_layernorm.restype = ci
         lib.oracle_num_threads.argtypes = []
@@ -189,3 +192,22 @@ def sdpa_lse(q, k, scale=None, mask=MASK_NONE, key_lens=None):
     if rc:
         raise RuntimeError("oracle_sdpa_lse failed")
     return lse
+
+
+def sdpa_backward(q, k, v, dout, scale=None, mask=MASK_NONE, key_lens=None):
+    """Gradients (dq, dk, dv) of sdpa(q, k, v) for the output gradient dout
+    (same shape as the output); d_k == d_v."""
+    q, k, v, dout = _d(q), _d(k), _d(v), _d(dout)
+    B, H, Tq, d = q.shape
+    Tk = k.shape[2]
+    if k.shape != (B, H, Tk, d) or v.shape != (B, H, Tk, d) or dout.shape != (B, H, Tq, d):
+        raise ValueError("shape mismatch (d_k must equal d_v)")
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    kl = _lens(key_lens, B)
+    dq, dk, dv = np.empty(q.shape), np.empty(k.shape), np.empty(v.shape)
+    rc = _load().oracle_sdpa_backward(_p(q), _p(k), _p(v), _p(dout), _p(dq), _p(dk), _p(dv), B, H,
+                                      Tq, Tk, d, float(scale), int(mask), _p(kl, ctypes.c_int32))
+    if rc:
+        raise RuntimeError("oracle_sdpa_backward failed")
+    return dq, dk, dv

@@ -348,6 +348,92 @@ int oracle_sdpa_lse(const double *q, const double *k, double *lse, int B, int H,
 }
 
 /*
+ * Gradients of scaled dot-product attention, written out from the forward
+ * definition by the chain rule (the pages give the forward only; this is its
+ * derivative, no further reading needed).  Per (b, h), with S = scale Q K^T
+ * (masked entries -inf), P = softmax(S) row-wise, O = P V and an incoming
+ * gradient dO:
+ *   dV = P^T dO,
+ *   dP = dO V^T,
+ *   dS_ij = P_ij (dP_ij - sum_l P_il dP_il)      (softmax Jacobian per row),
+ *   dQ = scale dS K,   dK = scale dS^T Q.
+ * Masked entries have P = 0 and so dS = 0; a row with no visible key has
+ * P = 0 everywhere.  q, do (B,H,Tq,d); k, v (B,H,Tk,d); dq (B,H,Tq,d),
+ * dk, dv (B,H,Tk,d).  The weights are recomputed here from q and k.
+ */
+int oracle_sdpa_backward(const double *q, const double *k, const double *v, const double *dout,
+                         double *dq, double *dk, double *dv, int B, int H, int Tq, int Tk, int d,
+                         double scale, int mask_kind, const int32_t *key_lens)
+{
+    if (B < 0 || H < 0 || Tq < 0 || Tk < 0 || d <= 0)
+        return -1;
+    const long BH = (long)B * H;
+    int failed = 0;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long bh = 0; bh < BH; ++bh) {
+        const int b = (int)(bh / H);
+        const double *qb = q + (size_t)bh * Tq * d, *kb = k + (size_t)bh * Tk * d;
+        const double *vb = v + (size_t)bh * Tk * d, *gb = dout + (size_t)bh * Tq * d;
+        double *dqb = dq + (size_t)bh * Tq * d, *dkb = dk + (size_t)bh * Tk * d;
+        double *dvb = dv + (size_t)bh * Tk * d;
+        double *p = (double *)malloc(sizeof(double) * (size_t)(Tk > 0 ? Tk : 1));
+        double *dp = (double *)malloc(sizeof(double) * (size_t)(Tk > 0 ? Tk : 1));
+        if (!p || !dp) {
+#pragma omp atomic write
+            failed = 1;
+            free(p);
+            free(dp);
+            continue;
+        }
+        for (size_t x = 0; x < (size_t)Tq * d; ++x)
+            dqb[x] = 0.0;
+        for (size_t x = 0; x < (size_t)Tk * d; ++x)
+            dkb[x] = dvb[x] = 0.0;
+        for (int i = 0; i < Tq; ++i) {
+            const double *qi = qb + (size_t)i * d, *gi = gb + (size_t)i * d;
+            /* P_i (the forward's weights) */
+            double m = -INFINITY;
+            for (int j = 0; j < Tk; ++j) {
+                p[j] = key_visible(mask_kind, key_lens, b, i, j) ? scale * qk_dot(qi, kb, j, d)
+                                                                 : -INFINITY;
+                if (p[j] > m)
+                    m = p[j];
+            }
+            if (m == -INFINITY)
+                continue; /* no visible key: P_i = 0, no gradient flows */
+            double den = 0.0;
+            for (int j = 0; j < Tk; ++j) {
+                p[j] = p[j] == -INFINITY ? 0.0 : exp(p[j] - m);
+                den += p[j];
+            }
+            /* dP_ij = dO_i . V_j and the row sum of P dP */
+            double pdp = 0.0;
+            for (int j = 0; j < Tk; ++j) {
+                p[j] /= den;
+                double g = 0.0;
+                for (int c = 0; c < d; ++c)
+                    g += gi[c] * vb[(size_t)j * d + c];
+                dp[j] = g;
+                pdp += p[j] * g;
+            }
+            for (int j = 0; j < Tk; ++j) {
+                if (p[j] == 0.0)
+                    continue;
+                const double ds = p[j] * (dp[j] - pdp);
+                for (int c = 0; c < d; ++c) {
+                    dvb[(size_t)j * d + c] += p[j] * gi[c];
+                    dqb[(size_t)i * d + c] += scale * ds * kb[(size_t)j * d + c];
+                    dkb[(size_t)j * d + c] += scale * ds * qi[c];
+                }
+            }
+        }
+        free(p);
+        free(dp);
+    }
+    return failed ? -1 : 0;
+}
+
+/*
  * Residual connection and layer normalisation around a sublayer, per row:
  *   v = x + s  (the sublayer's input added back to its output),
  *   y = (v - mu) / sigma * gamma + beta,

@@ -37,6 +37,12 @@ MUTATIONS = [
      "yr[c] = (sr[c] - mu)"),
     ("log-sum-exp without its maximum", "lse[r] = m + log(sum);", "lse[r] = log(sum);"),
     ("log-sum-exp sum without the scale", "sum += exp(scale * dot - m);", "sum += exp(dot - m);"),
+    ("backward without the softmax row term", "const double ds = p[j] * (dp[j] - pdp);",
+     "const double ds = p[j] * dp[j];"),
+    ("backward dQ without the scale", "dqb[(size_t)i * d + c] += scale * ds *",
+     "dqb[(size_t)i * d + c] += ds *"),
+    ("backward dV from dP instead of P", "dvb[(size_t)j * d + c] += p[j] * gi[c];",
+     "dvb[(size_t)j * d + c] += dp[j] * gi[c];"),
 ]
 
 

@@ -492,3 +492,73 @@ def test_lse_closed_forms_and_consistency_with_weights():
     # no visible key: -inf
     got = oracle.sdpa_lse(q, k, scale=0.5, mask=MASK_KEY_PADDING, key_lens=np.array([0], np.int32))
     assert np.all(np.isneginf(got))
+
+
+# ------------------------------------------------------------- backward
+def _torch_sdpa_grads(q, k, v, g, scale, mask, lens):
+    torch = pytest.importorskip("torch")
+    tq, tk, tv = (torch.from_numpy(a).requires_grad_(True) for a in (q, k, v))
+    Tq, Tk = q.shape[2], k.shape[2]
+    i = torch.arange(Tq)[:, None]
+    j = torch.arange(Tk)[None, :]
+    vis = torch.ones(q.shape[0], 1, Tq, Tk, dtype=torch.bool)
+    if mask & MASK_CAUSAL:
+        vis = vis & (j <= i)
+    if mask & MASK_KEY_PADDING:
+        vis = vis & (j[None, None] < torch.from_numpy(lens)[:, None, None, None])
+    o = torch.nn.functional.scaled_dot_product_attention(tq, tk, tv, attn_mask=vis, scale=scale)
+    o.backward(torch.from_numpy(g))
+    return tq.grad.numpy(), tk.grad.numpy(), tv.grad.numpy()
+
+
+@pytest.mark.parametrize("mask", [MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING, MASK_CAUSAL_KEY_PADDING])
+def test_backward_matches_torch_autograd(mask):
+    rng = np.random.default_rng(101)
+    B, H, Tq, Tk, d = 2, 2, 7, 9 if not mask & MASK_CAUSAL else 7, 8
+    q, g = rng.normal(size=(B, H, Tq, d)), rng.normal(size=(B, H, Tq, d))
+    k, v = rng.normal(size=(B, H, Tk, d)), rng.normal(size=(B, H, Tk, d))
+    lens = np.array([Tk, 3], dtype=np.int32)
+    got = oracle.sdpa_backward(q, k, v, g, scale=0.4, mask=mask,
+                               key_lens=lens if mask & MASK_KEY_PADDING else None)
+    ref = _torch_sdpa_grads(q, k, v, g, 0.4, mask, lens)
+    for a, r in zip(got, ref):
+        np.testing.assert_allclose(a, r, rtol=0, atol=1e-12)
+
+
+def test_backward_matches_finite_differences_of_the_forward():
+    rng = np.random.default_rng(102)
+    q, g = rng.normal(size=(1, 1, 3, 4)), rng.normal(size=(1, 1, 3, 4))
+    k, v = rng.normal(size=(1, 1, 4, 4)), rng.normal(size=(1, 1, 4, 4))
+    lens = np.array([3], dtype=np.int32)
+    for mask in (MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING):
+        kl = lens if mask & MASK_KEY_PADDING else None
+        grads = oracle.sdpa_backward(q, k, v, g, scale=0.7, mask=mask, key_lens=kl)
+        loss = lambda qq, kk, vv: float(np.sum(g * oracle.sdpa(qq, kk, vv, scale=0.7, mask=mask,
+                                                               key_lens=kl)))
+        h = 1e-6
+        for which, arr in enumerate((q, k, v)):
+            num = np.zeros_like(arr)
+            for idx in np.ndindex(arr.shape):
+                plus, minus = [a.copy() for a in (q, k, v)], [a.copy() for a in (q, k, v)]
+                plus[which][idx] += h
+                minus[which][idx] -= h
+                num[idx] = (loss(*plus) - loss(*minus)) / (2 * h)
+            np.testing.assert_allclose(grads[which], num, rtol=0, atol=1e-7)
+
+
+def test_backward_key_gradients_sum_to_zero_and_masked_keys_get_none():
+    # softmax is shift-invariant per row, so sum_j dS_ij = 0 and hence
+    # sum_j dK_j = 0 for every (b, h)
+    rng = np.random.default_rng(103)
+    q, g = rng.normal(size=(2, 2, 6, 8)), rng.normal(size=(2, 2, 6, 8))
+    k, v = rng.normal(size=(2, 2, 10, 8)), rng.normal(size=(2, 2, 10, 8))
+    lens = np.array([10, 4], dtype=np.int32)
+    dq, dk, dv = oracle.sdpa_backward(q, k, v, g, mask=MASK_KEY_PADDING, key_lens=lens)
+    np.testing.assert_allclose(dk.sum(axis=2), 0.0, atol=1e-12)
+    assert np.all(dk[1, :, 4:] == 0) and np.all(dv[1, :, 4:] == 0)
+    # single visible key: the weight is 1 whatever q and k, so dQ = dK = 0
+    # and dV_0 = sum of the output gradients
+    dq, dk, dv = oracle.sdpa_backward(q, k, v, g, mask=MASK_KEY_PADDING,
+                                      key_lens=np.array([1, 1], dtype=np.int32))
+    assert np.all(dq == 0) and np.all(dk == 0)
+    np.testing.assert_allclose(dv[:, :, 0], g.sum(axis=2), atol=1e-13)
