@@ -367,6 +367,24 @@ def time_other_workloads(dev, stream, flush, iters=20):
             "ms": ms_ln, "tflops": fl / (ms_ln * 1e-3) / 1e12, "flops": fl,
             "kind": "LayerNorm(x + MHA(x)): W^O GEMM with residual add and normalisation "
                     "in its epilogue (cluster per 128-row block)"}
+    # backward of the headline workload (dq, dk, dv from q, k, v, o, lse, dO)
+    w = si.WORKLOADS[4]
+    x = si.make_inputs(w)
+    q, k, v = dv(x["q_bits"]), dv(x["k_bits"]), dv(x["v_bits"])
+    g = dv(si.f64_to_bf16_bits(si.round_bf16(si.normal(w.seed, si.TENSOR_IDS["dout"], q.shape))))
+    o, lse = tsds.sdpa_forward_lse(q, k, v, scale=w.scale, mask="causal", stream=stream)
+    ws = torch.empty(int(tsds.lib.sdpa_backward_workspace_bytes(w.B, w.h, w.T_q, w.T_k, 64, 64)),
+                     dtype=torch.uint8, device=dev)
+    dq, dk, dvv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ms = timed(lambda: tsds.sdpa_backward(q, k, v, o, g, lse, dq, dk, dvv, ws, scale=w.scale,
+                                          mask="causal", stream=stream))
+    fl = 2.5 * attention_flops(w)
+    res[w.name + "_backward"] = {
+        "ms": ms, "tflops": fl / (ms * 1e-3) / 1e12, "flops": fl,
+        "kind": "bf16 attention backward (dq, dk, dv): 5 products per key/query tile pair = "
+                "2.5x the forward's FLOPs; row terms + tcgen05 kernel + dq conversion"}
+    del q, k, v, g, o, lse, ws, dq, dk, dvv
+
     w = si.WORKLOADS[5]
     x = si.make_inputs(w)
     q, k, v = dv(x["q_bits"]), dv(x["k_bits"]), dv(x["v_bits"])

@@ -109,6 +109,29 @@ mha_status sdpa_forward_lse(mha_dtype dt, const void *q, const void *k, const vo
                             cudaStream_t stream);
 
 /*
+ * Gradients of sdpa_forward (bf16): given q, k, v, the forward's output o
+ * and log-sum-exp lse (from sdpa_forward_lse) and the output gradient dout,
+ * writes
+ *   dv = P^T dout,  dq = scale dS k,  dk = scale dS^T q,
+ *   dS = P (.) (dout v^T - rowsum(dout (.) o)),  P = exp(scale q k^T - lse)
+ * (the chain rule of the forward definition; masked entries of P are 0).
+ *   q, o, dout, dq (B, h, T_q, 64); k, v, dk, dv (B, h, T_k, 64); bf16,
+ *   16-byte aligned; lse (B, h, T_q) fp32.  mask / key_lens / scale as the
+ *   forward.  workspace: >= sdpa_backward_workspace_bytes() bytes, 256-byte
+ *   aligned (an fp32 dq accumulator and two per-row vectors).
+ * Three launches (row terms, the tcgen05 kernel -- one CTA per (b, h, block
+ * of 128 keys) that keeps dk and dv in tensor memory and adds its dq
+ * contributions to the fp32 accumulator -- and the dq conversion).  d_k ==
+ * d_v == 64 only; MHA_F32 returns MHA_ERR_UNSUPPORTED.
+ */
+size_t sdpa_backward_workspace_bytes(int B, int h, int T_q, int T_k, int d_k, int d_v);
+mha_status sdpa_backward(mha_dtype dt, const void *q, const void *k, const void *v, const void *o,
+                         const void *dout, const float *lse, void *dq, void *dk, void *dv,
+                         void *workspace, size_t workspace_bytes, int B, int h, int T_q, int T_k,
+                         int d_k, int d_v, float scale, mha_mask mask, const int32_t *key_lens,
+                         int *status_dev, cudaStream_t stream);
+
+/*
  * Attention for decoding steps (bf16): each of the T_q new query rows of a
  * (b, h) attends to the first cache_lens[b] rows of that sequence's key/value
  * cache,

@@ -38,7 +38,7 @@ _M2 = np.uint64(0x94D049BB133111EB)
 
 TENSOR_IDS = {"x_q": 0, "x_kv": 1, "q": 2, "k": 3, "v": 4,
               "w_q": 5, "w_k": 6, "w_v": 7, "w_o": 8, "key_lens": 9,
-              "ln_gamma": 10, "ln_beta": 11}
+              "ln_gamma": 10, "ln_beta": 11, "dout": 12}
 
 MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING, MASK_CAUSAL_KEY_PADDING = 0, 1, 2, 3
 

@@ -152,3 +152,26 @@ def test_sdpa_lse_rejects_bad_arguments(lib):
     assert f(*args(lse=None)) == lib.MHA_ERR_INVALID_ARG
     assert f(*args(dt=0)) == lib.MHA_ERR_UNSUPPORTED
     assert f(*args(lse=None, B=0)) == lib.MHA_OK
+
+
+def bwd(lib, dt=1, p=FAKE, ws=FAKE, ws_bytes=1 << 40, B=1, h=1, Tq=8, Tk=8, d=64, mask=0, lens=None,
+        lse=FAKE):
+    return lib.lib.sdpa_backward(dt, p, p, p, p, p, lse, p, p, p, ws, ws_bytes, B, h, Tq, Tk, d, d,
+                                 0.125, mask, lens, None, None)
+
+
+def test_backward_rejects_bad_arguments(lib):
+    assert bwd(lib, p=None) == lib.MHA_ERR_INVALID_ARG
+    assert bwd(lib, lse=None) == lib.MHA_ERR_INVALID_ARG
+    assert bwd(lib, mask=2, lens=None) == lib.MHA_ERR_INVALID_ARG
+    assert bwd(lib, dt=0) == lib.MHA_ERR_UNSUPPORTED
+    assert bwd(lib, d=128) == lib.MHA_ERR_UNSUPPORTED
+    assert bwd(lib, ws=None) == lib.MHA_ERR_WORKSPACE
+    assert bwd(lib, ws_bytes=16) == lib.MHA_ERR_WORKSPACE
+    assert bwd(lib, ws=FAKE + 64) == lib.MHA_ERR_MISALIGNED
+    assert bwd(lib, p=FAKE + 8) == lib.MHA_ERR_MISALIGNED
+    assert bwd(lib, B=0) == lib.MHA_OK
+    assert bwd(lib, Tq=0, Tk=0) == lib.MHA_OK
+    # fp32 dq accumulator + two per-row vectors over whole 128-row blocks
+    assert lib.lib.sdpa_backward_workspace_bytes(2, 3, 130, 7, 64, 64) == (
+        2 * 3 * 256 * 64 * 4 + 2 * 2 * 3 * 256 * 4)

@@ -16,7 +16,7 @@ from . import _native
 from ._native import (MHA_BF16, MHA_F32, MHA_MASK_CAUSAL, MHA_MASK_CAUSAL_KEY_PADDING,
                       MHA_MASK_KEY_PADDING, MHA_MASK_NONE, MHA_OK, lib)
 
-__all__ = ["sdpa_forward", "sdpa_forward_lse", "sdpa_decode_forward", "mha_forward", "mha_forward_add_layernorm", "mha_workspace_bytes", "status_string", "MhaError",
+__all__ = ["sdpa_forward", "sdpa_forward_lse", "sdpa_backward", "sdpa_decode_forward", "mha_forward", "mha_forward_add_layernorm", "mha_workspace_bytes", "status_string", "MhaError",
            "MASKS", "lib"]
 
 MASKS = {"none": MHA_MASK_NONE, "causal": MHA_MASK_CAUSAL, "key_padding": MHA_MASK_KEY_PADDING,
@@ -123,6 +123,43 @@ def sdpa_forward_lse(q, k, v, out=None, lse=None, *, scale=None, mask="none", ke
     if rc != MHA_OK:
         raise MhaError(rc, "sdpa_forward_lse")
     return out, lse
+
+
+def sdpa_backward(q, k, v, o, dout, lse, dq=None, dk=None, dv=None, workspace=None, *,
+                  scale=None, mask="none", key_lens=None, status=None, stream=None):
+    """Gradients (dq, dk, dv) of sdpa_forward for bf16 tensors, from the
+    forward's output o and log-sum-exp lse (sdpa_forward_lse) and the output
+    gradient dout."""
+    torch = _torch()
+    bf = torch.bfloat16
+    for n, t in (("q", q), ("k", k), ("v", v), ("o", o), ("dout", dout)):
+        _check_dev(n, t, bf)
+    _check_dev("lse", lse, torch.float32)
+    B, h, T_q, d_k = q.shape
+    T_k, d_v = k.shape[2], v.shape[3]
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    for n, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        _check_dev(n, t, bf)
+    need = int(lib.sdpa_backward_workspace_bytes(B, h, T_q, T_k, d_k, d_v))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    _check_dev("workspace", workspace)
+    if key_lens is not None:
+        _check_dev("key_lens", key_lens, torch.int32)
+    if status is not None:
+        _check_dev("status", status, torch.int32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_k)
+    rc = lib.sdpa_backward(MHA_BF16, _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(dout), _ptr(lse),
+                           _ptr(dq), _ptr(dk), _ptr(dv), _ptr(workspace),
+                           workspace.numel() * workspace.element_size(), B, h, T_q, T_k, d_k,
+                           d_v, float(scale), _mask_code(mask), _ptr(key_lens), _ptr(status),
+                           _stream_handle(stream))
+    if rc != MHA_OK:
+        raise MhaError(rc, "sdpa_backward")
+    return dq, dk, dv
 
 
 def sdpa_decode_forward(q, k_cache, v_cache, cache_lens=None, out=None, *, scale=None,

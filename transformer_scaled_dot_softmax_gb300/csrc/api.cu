@@ -226,6 +226,63 @@ MHA_EXPORT mha_status sdpa_forward_lse(mha_dtype dt, const void *q, const void *
                      status_dev, stream);
 }
 
+MHA_EXPORT size_t sdpa_backward_workspace_bytes(int B, int h, int T_q, int T_k, int d_k, int d_v) {
+    if (B < 0 || h < 0 || T_q < 0 || T_k < 0 || d_k < 0 || d_v < 0) return 0;
+    (void)T_k;
+    return mha::bwd_workspace_bytes(static_cast<long long>(B) * h, T_q);
+}
+
+MHA_EXPORT mha_status sdpa_backward(mha_dtype dt, const void *q, const void *k, const void *v,
+                                    const void *o, const void *dout, const float *lse, void *dq,
+                                    void *dk, void *dv, void *workspace, size_t workspace_bytes,
+                                    int B, int h, int T_q, int T_k, int d_k, int d_v, float scale,
+                                    mha_mask mask, const int32_t *key_lens, int *status_dev,
+                                    cudaStream_t stream) {
+    if (B < 0 || h < 0 || T_q < 0 || T_k < 0 || d_k <= 0 || d_v <= 0) return MHA_ERR_INVALID_ARG;
+    if (!valid_mask(mask) || !isfinite(scale)) return MHA_ERR_INVALID_ARG;
+    if ((mask & MHA_MASK_KEY_PADDING) && !key_lens) return MHA_ERR_INVALID_ARG;
+    if (dt != MHA_BF16) return dt == MHA_F32 ? MHA_ERR_UNSUPPORTED : MHA_ERR_INVALID_ARG;
+    if (d_k != 64 || d_v != 64) return MHA_ERR_UNSUPPORTED;
+    const long long BH = static_cast<long long>(B) * h;
+    if (BH >= (1ll << 31) || (T_k + 127) / 128 > 65535) return MHA_ERR_UNSUPPORTED;
+    if (BH == 0 || (T_q == 0 && T_k == 0)) return MHA_OK;
+    if ((T_q > 0 && (!q || !o || !dout || !lse || !dq)) || (T_k > 0 && (!k || !v || !dk || !dv)))
+        return MHA_ERR_INVALID_ARG;
+    if (!workspace || workspace_bytes < mha::bwd_workspace_bytes(BH, T_q)) return MHA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MHA_ERR_MISALIGNED;
+    if ((T_q > 0 && (!aligned16(q) || !aligned16(o) || !aligned16(dout) || !aligned16(dq))) ||
+        (T_k > 0 && (!aligned16(k) || !aligned16(v) || !aligned16(dk) || !aligned16(dv))))
+        return MHA_ERR_MISALIGNED;
+    // A tensor map needs every extent >= 1: describe a one-row tensor for an
+    // empty side (the kernels never load it).
+    const void *q_src = T_q > 0 ? q : k, *g_src = T_q > 0 ? dout : k;
+    const void *k_src = T_k > 0 ? k : q, *v_src = T_k > 0 ? v : q;
+    CUtensorMap tq, tk, tv, tg;
+    mha_status s;
+    if ((s = encode_heads(&tq, q_src, BH, T_q > 0 ? T_q : 1)) != MHA_OK) return s;
+    if ((s = encode_heads(&tg, g_src, BH, T_q > 0 ? T_q : 1)) != MHA_OK) return s;
+    if ((s = encode_heads(&tk, k_src, BH, T_k > 0 ? T_k : 1)) != MHA_OK) return s;
+    if ((s = encode_heads(&tv, v_src, BH, T_k > 0 ? T_k : 1)) != MHA_OK) return s;
+    mha::BwdParams p{};
+    p.B = B;
+    p.H = h;
+    p.Tq = T_q;
+    p.Tk = T_k;
+    p.Tq_pad = (T_q + 127) / 128 * 128;
+    p.scale = scale;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.mask = mask;
+    p.key_lens = key_lens;
+    p.dk = static_cast<__nv_bfloat16 *>(dk);
+    p.dv = static_cast<__nv_bfloat16 *>(dv);
+    p.status = status_dev;
+    return launch_status(
+        mha::launch_attn_bwd_bf16(tq, tk, tv, tg, static_cast<const __nv_bfloat16 *>(o),
+                                  static_cast<const __nv_bfloat16 *>(dout), lse,
+                                  static_cast<__nv_bfloat16 *>(dq), p, workspace, stream),
+        "attention backward launch");
+}
+
 MHA_EXPORT mha_status sdpa_decode_forward(const void *q, const void *k_cache,
                                           const void *v_cache, void *o, int B, int h, int T_q,
                                           int T_k, int d_k, int d_v, float scale,

@@ -1,0 +1,459 @@
+// attn_bwd_bf16.cu -- gradients of scaled dot-product attention for sm_103a.
+//
+// With S = scale Q K^T (masked entries -inf), P = softmax(S) row-wise,
+// O = P V and the output gradient dO, the chain rule gives
+//   dV = P^T dO,  dP = dO V^T,  dS = P (.) (dP - D),  D_i = sum_c dO_ic O_ic,
+//   dQ = scale dS K,  dK = scale dS^T Q
+// (D_i = sum_j P_ij dP_ij, the softmax Jacobian's row term).  The weights are
+// not stored by the forward pass; they are recomputed from the forward's
+// per-row log-sum-exp: P_ij = exp(S_ij - lse_i).
+//
+// Three launches:
+//   attn_bwd_pre   D_i, lse_i in log2 units (+inf for a padded or fully masked
+//                  row, so its weights are 0), and a zeroed fp32 dQ accumulator;
+//   attn_bwd_main  one CTA per (b, h, block of 128 keys): keeps dK and dV of
+//                  its keys in tensor memory and walks the query blocks that
+//                  see them (see the kernel comment);
+//   attn_bwd_post  dQ = bf16(scale * accumulator).
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "sm103_ptx.cuh"
+
+namespace mha {
+namespace {
+
+constexpr int HD = kAttnHeadDim;  // 64
+constexpr int BQ = 128;           // query rows per block
+constexpr int BKB = 128;          // keys per CTA
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ------------------------------------------------------------ pre and post
+// One thread per 8 features of a row; rows past Tq (padding up to a whole
+// query block) get lse = +inf, D = 0.
+__global__ void attn_bwd_pre(const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ dout,
+                             const float *__restrict__ lse, float *__restrict__ lse2,
+                             float *__restrict__ dvec, float *__restrict__ dq_acc, long long BH,
+                             int Tq, int Tq_pad) {
+    const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const long long row = t >> 3;  // over BH * Tq_pad
+    const int part = static_cast<int>(t & 7);
+    // no early return: the row sum below is a full-warp shuffle
+    const bool valid = row < BH * Tq_pad;
+    const long long bh = valid ? row / Tq_pad : 0;
+    const int i = valid ? static_cast<int>(row - bh * Tq_pad) : Tq;
+    float acc = 0.f;
+    if (i < Tq) {
+        const long long src = (bh * Tq + i) * HD + part * 8;
+        const uint4 a = *reinterpret_cast<const uint4 *>(o + src);
+        const uint4 g = *reinterpret_cast<const uint4 *>(dout + src);
+        const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            acc = fmaf(__uint_as_float(aw[e] << 16), __uint_as_float(gw[e] << 16), acc);
+            acc = fmaf(__uint_as_float(aw[e] & 0xffff0000u), __uint_as_float(gw[e] & 0xffff0000u), acc);
+        }
+    }
+    // reduce over the 8 threads of the row (consecutive lanes)
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+    if (!valid) return;
+    float4 *z = reinterpret_cast<float4 *>(dq_acc + row * HD + part * 8);
+    z[0] = make_float4(0.f, 0.f, 0.f, 0.f);
+    z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (part == 0) {
+        dvec[row] = acc;
+        float l = INFINITY;
+        if (i < Tq) {
+            const float x = lse[bh * Tq + i];
+            l = x == -INFINITY ? INFINITY : x * kLog2e;
+        }
+        lse2[row] = l;
+    }
+}
+
+__global__ void attn_bwd_post(const float *__restrict__ dq_acc, __nv_bfloat16 *__restrict__ dq,
+                              long long BH, int Tq, int Tq_pad, float scale) {
+    const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const long long row = t >> 3;  // over BH * Tq
+    const int part = static_cast<int>(t & 7);
+    if (row >= BH * Tq) return;
+    const long long bh = row / Tq;
+    const int i = static_cast<int>(row - bh * Tq);
+    const float4 *src = reinterpret_cast<const float4 *>(dq_acc + (bh * Tq_pad + i) * HD + part * 8);
+    const float4 a = src[0], b = src[1];
+    const uint4 w = make_uint4(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale),
+                               pack_bf16x2(b.x * scale, b.y * scale), pack_bf16x2(b.z * scale, b.w * scale));
+    *reinterpret_cast<uint4 *>(dq + row * HD + part * 8) = w;
+}
+
+// ------------------------------------------------------------------- main
+// One CTA = one (b, h) and a block of 128 keys; it walks the query blocks j
+// that see any of its keys (all of them, or j >= kb under the causal mask).
+// Warp roles (10 warps):
+//
+//   warp 0      TMA: the K and V blocks once; per query block Q_j, dO_j (3-D
+//               tensor maps) and its 128 lse and D values (bulk copies) into
+//               a 2-stage ring.
+//   warp 1      MMA issuer (whole warp, elected lane), per query block:
+//                 (1) S^T  = K Q_j^T     M=128 keys, N=128 queries, K=64
+//                 (2) dP^T = V dO_j^T    same shape
+//                 (3) dV  += P^T dO_j    M=128 keys, N=64, K=128 queries, A = P^T in
+//                                        tensor memory
+//                 (4) dK  += dS^T Q_j    same, A = dS^T in tensor memory
+//                 (5) dQ_j = dS K        M=128 queries, N=64, K=128 keys, A = dS from
+//                                        shared memory (queries contiguous)
+//               Computing S and dP transposed puts the keys on the
+//               tensor-memory lanes, so P^T and dS^T feed (3) and (4) straight
+//               from tensor memory.
+//   warps 2-5   one thread per key (tensor-memory lane): P^T = 2^(S^T c - lse_j)
+//               (masked: 0), dS^T = P^T (dP^T - D_j); P^T and dS^T written back
+//               over S^T and dP^T (bf16), dS^T also into shared memory for (5).
+//               At the end: dK (times scale) and dV out of tensor memory, bf16.
+//   warps 6-9   one thread per query row: dQ_j partial out of tensor memory,
+//               added to the fp32 accumulator in global memory (other key
+//               blocks add theirs).
+//
+// Tensor memory: S^T [0,128) (P^T over [0,64)), dP^T [128,256) (dS^T over
+// [128,192)), dV [256,320), dK [320,384), dQ_j [384,448).
+constexpr uint32_t kTile = BQ * HD * 2;  // 16 KiB
+constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kColDQ = 384;
+constexpr int kBwdThreads = 320;
+
+struct __align__(1024) SmemBwd {
+    uint8_t k[kTile];
+    uint8_t v[kTile];
+    uint8_t q[2][kTile];
+    uint8_t g[2][kTile];   // dO
+    uint8_t ds[2 * kTile]; // dS as the A operand of (5): 2 blocks of 64 queries x 128 key rows
+    float lse2[2][BQ];
+    float dvec[2][BQ];
+    uint64_t kv_full;
+    uint64_t stage_full[2];
+    uint64_t stage_empty[2];
+    uint64_t sdp_full;   // (1), (2) complete
+    uint64_t pds_full;   // P^T, dS^T written (4 warps)
+    uint64_t tmem_free;  // (3), (4) complete: S^T / dP^T columns reusable
+    uint64_t ds_free;    // (5) complete: the shared dS tile reusable
+    uint64_t dq_full;    // (5) complete
+    uint64_t dq_free;    // dQ_j read (4 warps)
+    uint64_t acc_done;   // every product complete
+    uint64_t drain;
+    uint32_t tmem_base;
+    int abort_flag;
+};
+
+__global__ void __launch_bounds__(kBwdThreads, 1)
+    attn_bwd_main(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                  const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_g,
+                  const BwdParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    SmemBwd &sm = *reinterpret_cast<SmemBwd *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int bh = static_cast<int>(blockIdx.x);
+    const int kb = static_cast<int>(blockIdx.y);  // key block 0 (most query blocks when causal) first
+    const int b = bh / p.H;
+    const int k0 = kb * BKB;
+    const bool causal = (p.mask & kMaskCausalBit) != 0;
+    int key_hi = p.Tk;  // keys [0, key_hi) exist and are not padding
+    if ((p.mask & kMaskPaddingBit) && p.key_lens) key_hi = min(max(p.key_lens[b], 0), p.Tk);
+    const int n_qb = (p.Tq + BQ - 1) / BQ;
+    // Query i sees key k iff k <= i (causal, top-left aligned): query blocks
+    // from k0 / BQ on.
+    const int j_begin = causal ? k0 / BQ : 0;
+    const int n_j = k0 < key_hi ? max(0, n_qb - j_begin) : 0;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&sm.kv_full, 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sm.stage_full[i], 1);
+            mbar_init(&sm.stage_empty[i], 1);
+        }
+        mbar_init(&sm.sdp_full, 1);
+        mbar_init(&sm.pds_full, 4);
+        mbar_init(&sm.tmem_free, 1);
+        mbar_init(&sm.ds_free, 1);
+        mbar_init(&sm.dq_full, 1);
+        mbar_init(&sm.dq_free, 4);
+        mbar_init(&sm.acc_done, 1);
+        mbar_init(&sm.drain, 1);
+        sm.abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&sm.tmem_base, 512);
+        tmem_relinquish();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&tmap_q);
+        prefetch_tensormap(&tmap_k);
+        prefetch_tensormap(&tmap_v);
+        prefetch_tensormap(&tmap_g);
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = sm.tmem_base;
+    const AbortState ab{&sm.abort_flag, p.status};
+
+    if (warp == 0) {
+        // -------------------------------------------------------------- TMA
+        if (lane == 0 && n_j > 0) {
+            mbar_arrive_expect_tx(&sm.kv_full, 2 * kTile);
+            tma_load_3d(&tmap_k, &sm.kv_full, sm.k, 0, k0, bh);
+            tma_load_3d(&tmap_v, &sm.kv_full, sm.v, 0, k0, bh);
+            int issued = 0;
+            for (int t = 0; t < n_j; ++t) {
+                const int st = t & 1;
+                if (t >= 2 && !mbar_wait(&sm.stage_empty[st], ((t >> 1) - 1) & 1, ab)) break;
+                const int j = j_begin + t;
+                const long long vrow = static_cast<long long>(bh) * p.Tq_pad + j * BQ;
+                mbar_arrive_expect_tx(&sm.stage_full[st], 2 * kTile + 2 * BQ * 4);
+                tma_load_3d(&tmap_q, &sm.stage_full[st], sm.q[st], 0, j * BQ, bh);
+                tma_load_3d(&tmap_g, &sm.stage_full[st], sm.g[st], 0, j * BQ, bh);
+                bulk_load_1d(sm.lse2[st], p.lse2 + vrow, BQ * 4, &sm.stage_full[st]);
+                bulk_load_1d(sm.dvec[st], p.dvec + vrow, BQ * 4, &sm.stage_full[st]);
+                issued = t + 1;
+            }
+            mbar_wait_drain(&sm.kv_full, 0);
+            for (int x = max(0, issued - 2); x < issued; ++x)
+                mbar_wait_drain(&sm.stage_full[x & 1], (x >> 1) & 1);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------- MMA
+        if (n_j > 0) {
+            constexpr uint32_t id_s = idesc_bf16_f32(128, 128, false, false);  // (1), (2)
+            constexpr uint32_t id_kv = idesc_bf16_f32(128, HD, false, true);   // (3), (4)
+            constexpr uint32_t id_q = idesc_bf16_f32(128, HD, true, true);     // (5)
+            constexpr uint64_t kT = kTile >> 4;
+            // K-major operands (a K step of 16 = 32 bytes = 2), MN-major
+            // operands (16 rows of 128 bytes = 2 KiB = 128 per K step).
+            const uint64_t k_km = smem_desc_sw128(smem_u32(sm.k), 16, 1024);
+            const uint64_t v_km = smem_desc_sw128(smem_u32(sm.v), 16, 1024);
+            const uint64_t q_km = smem_desc_sw128(smem_u32(sm.q[0]), 16, 1024);
+            const uint64_t g_km = smem_desc_sw128(smem_u32(sm.g[0]), 16, 1024);
+            const uint64_t q_mn = smem_desc_sw128(smem_u32(sm.q[0]), 1024, 1024);
+            const uint64_t g_mn = smem_desc_sw128(smem_u32(sm.g[0]), 1024, 1024);
+            const uint64_t k_mn = smem_desc_sw128(smem_u32(sm.k), 1024, 1024);
+            // dS: two 64-query blocks 16 KiB apart (leading byte offset)
+            const uint64_t ds_mn = smem_desc_sw128(smem_u32(sm.ds), kTile, 1024);
+            bool ok = warp_wait(&sm.kv_full, 0, ab);
+            for (int t = 0; ok && t < n_j; ++t) {
+                const int st = t & 1;
+                const uint64_t so = static_cast<uint64_t>(st) * kT;  // q[st], g[st] stage offset
+                if (!(ok = warp_wait(&sm.stage_full[st], (t >> 1) & 1, ab))) break;
+                if (t >= 1 && !(ok = warp_wait(&sm.tmem_free, (t - 1) & 1, ab))) break;
+                tc_fence_after_sync();
+#pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk)
+                    warp_mma_bf16_ss(tmem + kColS, k_km + 2 * kk, q_km + so + 2 * kk, id_s, kk > 0 ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk)
+                    warp_mma_bf16_ss(tmem + kColDP, v_km + 2 * kk, g_km + so + 2 * kk, id_s, kk > 0 ? 1u : 0u);
+                warp_commit(&sm.sdp_full);
+                if (!(ok = warp_wait(&sm.pds_full, t & 1, ab))) break;
+                tc_fence_after_sync();
+#pragma unroll
+                for (int kk = 0; kk < BQ / 16; ++kk)
+                    warp_mma_bf16_ts(tmem + kColDV, tmem + kColS + 8 * kk, g_mn + so + 128 * kk, id_kv,
+                                     (t > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+                for (int kk = 0; kk < BQ / 16; ++kk)
+                    warp_mma_bf16_ts(tmem + kColDK, tmem + kColDP + 8 * kk, q_mn + so + 128 * kk, id_kv,
+                                     (t > 0 || kk > 0) ? 1u : 0u);
+                warp_commit(&sm.tmem_free);
+                if (t >= 1 && !(ok = warp_wait(&sm.dq_free, (t - 1) & 1, ab))) break;
+                tc_fence_after_sync();
+#pragma unroll
+                for (int kk = 0; kk < BKB / 16; ++kk)
+                    warp_mma_bf16_ss(tmem + kColDQ, ds_mn + 128 * kk, k_mn + 128 * kk, id_q, kk > 0 ? 1u : 0u);
+                warp_commit(&sm.dq_full);
+                warp_commit(&sm.ds_free);
+                warp_commit(&sm.stage_empty[st]);
+            }
+            if (ok) warp_commit(&sm.acc_done);
+        }
+        warp_commit(&sm.drain);
+        mbar_wait_drain(&sm.drain, 0);
+    } else if (warp < 6) {
+        // ------------------------------------------- per-key softmax terms
+        const uint32_t lane_base = static_cast<uint32_t>(warp & 3) * 32;
+        const int r = static_cast<int>(lane_base) + lane;  // key row in the block
+        const int key = k0 + r;
+        const bool key_ok = key < key_hi;
+        const uint32_t tl = tmem_addr(tmem, lane_base, 0);
+        const float C = p.scale_log2;
+        bool ok = true;
+        for (int t = 0; t < n_j; ++t) {
+            const int st = t & 1;
+            const int q0 = (j_begin + t) * BQ;
+            ok = __all_sync(0xffffffffu, mbar_wait(&sm.sdp_full, t & 1, ab)) &&
+                 __all_sync(0xffffffffu, mbar_wait(&sm.stage_full[st], (t >> 1) & 1, ab));
+            if (ok && t >= 1) ok = __all_sync(0xffffffffu, mbar_wait(&sm.ds_free, (t - 1) & 1, ab));
+            if (!ok) break;
+            tc_fence_after_sync();
+#pragma unroll 1
+            for (int c = 0; c < BQ / 32; ++c) {
+                uint32_t sv[32], dp[32];
+                tmem_ld32(tl + kColS + 32u * c, sv);
+                tmem_ld32(tl + kColDP + 32u * c, dp);
+                tmem_ld_wait(sv);
+                reg_fence32(dp);
+                uint32_t pk[16], dsk[16];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    float pp[2], dd[2];
+#pragma unroll
+                    for (int h2 = 0; h2 < 2; ++h2) {
+                        const int qi = 32 * c + 2 * e + h2;  // query column in the block
+                        const bool vis = key_ok && (!causal || key <= q0 + qi);
+                        const float pv = vis ? ex2_approx(__uint_as_float(sv[2 * e + h2]) * C - sm.lse2[st][qi]) : 0.f;
+                        pp[h2] = pv;
+                        dd[h2] = pv * (__uint_as_float(dp[2 * e + h2]) - sm.dvec[st][qi]);
+                    }
+                    pk[e] = pack_bf16x2(pp[0], pp[1]);
+                    dsk[e] = pack_bf16x2(dd[0], dd[1]);
+                }
+                // P^T and dS^T over the scores already read (columns
+                // [16c, 16c+16) of each region were read by chunks <= c).
+                tmem_st16(tl + kColS + 16u * c, pk);
+                tmem_st16(tl + kColDP + 16u * c, dsk);
+                // dS into shared memory as the A operand of (5): queries
+                // contiguous, 128-byte swizzled rows (16-byte chunk x of key
+                // row r at x ^ (r % 8)), 64 queries per 16 KiB block.
+                uint8_t *blk = sm.ds + (c >> 1) * kTile + r * 128;
+#pragma unroll
+                for (int x = 0; x < 4; ++x) {
+                    const int chunk = 4 * (c & 1) + x;
+                    *reinterpret_cast<uint4 *>(blk + ((chunk ^ (r & 7)) << 4)) =
+                        make_uint4(dsk[4 * x], dsk[4 * x + 1], dsk[4 * x + 2], dsk[4 * x + 3]);
+                }
+            }
+            tmem_st_wait();
+            fence_proxy_async_smem();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.pds_full);
+        }
+        // dK = scale dS^T Q and dV = P^T dO of this block's keys.
+        if (ok && n_j > 0) ok = __all_sync(0xffffffffu, mbar_wait(&sm.acc_done, 0, ab));
+        // `ok` and n_j are warp-uniform: every lane issues the tensor-memory
+        // loads; only the stores depend on the key row.
+        if (ok) {
+            const long long rowo = (static_cast<long long>(bh) * p.Tk + key) * HD;
+#pragma unroll 1
+            for (int which = 0; which < 2; ++which) {
+                uint32_t a[32], a2[32];
+                if (n_j > 0) {
+                    tc_fence_after_sync();
+                    __syncwarp();
+                    tmem_ld32(tl + (which ? kColDV : kColDK), a);
+                    tmem_ld32(tl + (which ? kColDV : kColDK) + 32, a2);
+                    tmem_ld_wait(a);
+                    reg_fence32(a2);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) a[e] = a2[e] = 0u;
+                }
+                if (key >= p.Tk) continue;
+                const float f = which ? 1.f : p.scale;
+                __nv_bfloat16 *dst = (which ? p.dv : p.dk) + rowo;
+                uint32_t w[32];
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    w[e] = pack_bf16x2(__uint_as_float(a[2 * e]) * f, __uint_as_float(a[2 * e + 1]) * f);
+                    w[16 + e] = pack_bf16x2(__uint_as_float(a2[2 * e]) * f, __uint_as_float(a2[2 * e + 1]) * f);
+                }
+#pragma unroll
+                for (int x = 0; x < 8; ++x)
+                    reinterpret_cast<uint4 *>(dst)[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+            }
+        }
+        if (!ok) tmem_st_wait();
+    } else {
+        // ------------------------------------------------- dQ accumulation
+        const uint32_t lane_base = static_cast<uint32_t>(warp & 3) * 32;
+        const int r = static_cast<int>(lane_base) + lane;  // query row in the block
+        const uint32_t tl = tmem_addr(tmem, lane_base, 0);
+        for (int t = 0; t < n_j; ++t) {
+            if (!__all_sync(0xffffffffu, mbar_wait(&sm.dq_full, t & 1, ab))) break;
+            tc_fence_after_sync();
+            uint32_t a[32], a2[32];
+            tmem_ld32(tl + kColDQ, a);
+            tmem_ld32(tl + kColDQ + 32, a2);
+            tmem_ld_wait(a);
+            reg_fence32(a2);
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.dq_free);
+            // rows past Tq carry zeros (their weights are 0) and stay inside
+            // the padded accumulator
+            float *dst = p.dq_acc + (static_cast<long long>(bh) * p.Tq_pad + (j_begin + t) * BQ + r) * HD;
+#pragma unroll
+            for (int x = 0; x < 8; ++x)
+                red_add_v4(dst + 4 * x, __uint_as_float(a[4 * x]), __uint_as_float(a[4 * x + 1]),
+                           __uint_as_float(a[4 * x + 2]), __uint_as_float(a[4 * x + 3]));
+#pragma unroll
+            for (int x = 0; x < 8; ++x)
+                red_add_v4(dst + 32 + 4 * x, __uint_as_float(a2[4 * x]), __uint_as_float(a2[4 * x + 1]),
+                           __uint_as_float(a2[4 * x + 2]), __uint_as_float(a2[4 * x + 3]));
+        }
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+}  // namespace
+
+size_t bwd_workspace_bytes(long long BH, int Tq) {
+    const long long Tq_pad = (Tq + BQ - 1) / BQ * BQ;
+    const size_t rows = static_cast<size_t>(BH) * Tq_pad;
+    auto r256 = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+    return r256(rows * HD * 4) + 2 * r256(rows * 4);
+}
+
+cudaError_t launch_attn_bwd_bf16(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                                 const CUtensorMap &tg, const __nv_bfloat16 *o,
+                                 const __nv_bfloat16 *dout, const float *lse, __nv_bfloat16 *dq,
+                                 BwdParams p, void *workspace, cudaStream_t stream) {
+    const long long BH = static_cast<long long>(p.B) * p.H;
+    const size_t rows = static_cast<size_t>(BH) * p.Tq_pad;
+    auto r256 = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    float *lse2 = reinterpret_cast<float *>(ws + r256(rows * HD * 4));
+    float *dvec = reinterpret_cast<float *>(ws + r256(rows * HD * 4) + r256(rows * 4));
+    p.dq_acc = reinterpret_cast<float *>(ws);
+    p.lse2 = lse2;
+    p.dvec = dvec;
+    cudaError_t e = cudaSuccess;
+    const long long pre_threads = static_cast<long long>(rows) * 8;
+    if (pre_threads > 0) {
+        attn_bwd_pre<<<static_cast<unsigned>((pre_threads + 255) / 256), 256, 0, stream>>>(
+            o, dout, lse, lse2, dvec, p.dq_acc, BH, p.Tq, p.Tq_pad);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    if (p.Tk > 0) {
+        const size_t smem = sizeof(SmemBwd) + 1024;
+        e = cudaFuncSetAttribute(attn_bwd_main, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        dim3 grid(static_cast<unsigned>(BH), static_cast<unsigned>((p.Tk + BKB - 1) / BKB));
+        attn_bwd_main<<<grid, kBwdThreads, smem, stream>>>(tq, tk, tv, tg, p);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    const long long post_threads = BH * p.Tq * 8;
+    if (post_threads == 0) return cudaSuccess;
+    attn_bwd_post<<<static_cast<unsigned>((post_threads + 255) / 256), 256, 0, stream>>>(
+        p.dq_acc, dq, BH, p.Tq, p.Tq_pad, p.scale);
+    return cudaGetLastError();
+}
+
+}  // namespace mha

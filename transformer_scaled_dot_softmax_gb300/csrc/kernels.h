@@ -46,6 +46,28 @@ cudaError_t launch_decode_bf16(const __nv_bfloat16 *q, const __nv_bfloat16 *k,
                                const __nv_bfloat16 *v, __nv_bfloat16 *o, const DecodeParams &p,
                                cudaStream_t stream);
 
+// ------------------------------------------------ bf16 attention backward
+struct BwdParams {
+    int B, H, Tq, Tk, Tq_pad;   // Tq_pad: Tq rounded up to whole 128-row blocks
+    float scale, scale_log2;
+    int mask;
+    const int32_t *key_lens;
+    const float *lse2;          // (B, H, Tq_pad) lse * log2(e), +inf for padded / empty rows
+    const float *dvec;          // (B, H, Tq_pad) rowsum(dO * O)
+    float *dq_acc;              // (B, H, Tq_pad, 64) fp32
+    __nv_bfloat16 *dk, *dv;     // (B, H, Tk, 64)
+    int *status;
+};
+// Bytes of workspace the backward needs (fp32 dQ accumulator, lse, D).
+size_t bwd_workspace_bytes(long long BH, int Tq);
+// q, k, v, dout: 3-D TMA maps like the forward's; o, dout, lse as device
+// arrays; fills dq (bf16), p.dk, p.dv.  `workspace`: bwd_workspace_bytes(),
+// 256-byte aligned.
+cudaError_t launch_attn_bwd_bf16(const CUtensorMap &tq, const CUtensorMap &tk, const CUtensorMap &tv,
+                                 const CUtensorMap &tg, const __nv_bfloat16 *o,
+                                 const __nv_bfloat16 *dout, const float *lse, __nv_bfloat16 *dq,
+                                 BwdParams p, void *workspace, cudaStream_t stream);
+
 // ------------------------------------------------ fp32 SIMT attention
 cudaError_t launch_sdpa_f32(const float *q, const float *k, const float *v, float *o, int B,
                             int H, int Tq, int Tk, int dk, int dv, float scale, int mask,
