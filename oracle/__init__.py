@@ -47,6 +47,10 @@ def _load():
         lib.oracle_sdpa_backward.argtypes = [dp, dp, dp, dp, dp, dp, dp, ci, ci, ci, ci, ci, cd,
                                              ci, ip]
         lib.oracle_sdpa_backward.restype = ci
+        lib.oracle_positional_encoding.argtypes = [dp, ci, ci, ci]
+        lib.oracle_positional_encoding.restype = ci
+        lib.oracle_ffn.argtypes = [dp, dp, dp, dp, dp, dp, cl, ci, ci]
+        lib.oracle_ffn.restype = ci
         lib.oracle_add_layernorm.argtypes = [dp, dp, dp, dp, cd, dp, cl, ci]
         lib.oracle_add_layernorm.restype = ci
         lib.oracle_num_threads.argtypes = []
@@ -211,3 +215,34 @@ def sdpa_backward(q, k, v, dout, scale=None, mask=MASK_NONE, key_lens=None):
     if rc:
         raise RuntimeError("oracle_sdpa_backward failed")
     return dq, dk, dv
+
+
+def positional_encoding(T, D, pos0=0):
+    """(T, D) table: PE(pos, 2i) = sin(pos / 10000^(2i/D)), PE(pos, 2i+1) =
+    cos(pos / 10000^(2i/D)) for pos = pos0 .. pos0+T-1."""
+    pe = np.empty((T, D))
+    if _load().oracle_positional_encoding(_p(pe), int(T), int(D), int(pos0)):
+        raise RuntimeError("oracle_positional_encoding failed")
+    return pe
+
+
+def ffn(x, w1, b1, w2, b2):
+    """max(0, x W1 + b1) W2 + b2 over the last axis of x."""
+    x, w1, b1, w2, b2 = _d(x), _d(w1), _d(b1), _d(w2), _d(b2)
+    D = x.shape[-1]
+    F = w1.shape[1]
+    if w1.shape != (D, F) or b1.shape != (F,) or w2.shape != (F, D) or b2.shape != (D,):
+        raise ValueError("shape mismatch")
+    y = np.empty(x.shape)
+    if _load().oracle_ffn(_p(x), _p(w1), _p(b1), _p(w2), _p(b2), _p(y), x.size // D, D, F):
+        raise RuntimeError("oracle_ffn failed")
+    return y
+
+
+def encoder_layer(x, p, h, eps=1e-5, scale=None, mask=MASK_NONE, key_lens=None):
+    """One encoder layer with post-normalisation:
+    y = LayerNorm1(x + MultiHead(x, x)), out = LayerNorm2(y + FFN(y)).
+    p: dict with w_q, w_k, w_v, w_o, gamma1, beta1, w1, b1, w2, b2, gamma2, beta2."""
+    y = mha_add_layernorm(x, x, p["w_q"], p["w_k"], p["w_v"], p["w_o"], p["gamma1"], p["beta1"],
+                          h=h, eps=eps, scale=scale, mask=mask, key_lens=key_lens)
+    return add_layernorm(y, ffn(y, p["w1"], p["b1"], p["w2"], p["b2"]), p["gamma2"], p["beta2"], eps)

@@ -468,6 +468,56 @@ int oracle_add_layernorm(const double *x, const double *s, const double *gamma,
     return 0;
 }
 
+/*
+ * Sinusoidal positional encoding of positions pos0 .. pos0+T-1 over D
+ * features ("Attention is All You Need" notebook chapter and aiany.app Step 8):
+ *   PE(pos, 2i)   = sin(pos / 10000^(2i/D)),
+ *   PE(pos, 2i+1) = cos(pos / 10000^(2i/D)).
+ * pe (T, D).
+ */
+int oracle_positional_encoding(double *pe, int T, int D, int pos0)
+{
+    if (T < 0 || D <= 0)
+        return -1;
+    for (int t = 0; t < T; ++t)
+        for (int c = 0; c < D; ++c) {
+            const int i2 = c - (c % 2); /* 2i */
+            const double angle = (double)(pos0 + t) / pow(10000.0, (double)i2 / D);
+            pe[(size_t)t * D + c] = (c % 2 == 0) ? sin(angle) : cos(angle);
+        }
+    return 0;
+}
+
+/*
+ * Position-wise feed-forward network, applied to every row independently
+ * (aiany.app Step 9; notebook chapter "Feed-Forward Network"):
+ *   FFN(x) = max(0, x W1 + b1) W2 + b2.
+ * x (M, D), W1 (D, F), b1 (F), W2 (F, D), b2 (D), y (M, D).
+ */
+int oracle_ffn(const double *x, const double *W1, const double *b1, const double *W2,
+               const double *b2, double *y, long M, int D, int F)
+{
+    if (M < 0 || D <= 0 || F <= 0)
+        return -1;
+    double *hid = (double *)malloc(sizeof(double) * (size_t)(M > 0 ? M : 1) * F);
+    if (!hid)
+        return -1;
+    matmul(x, W1, hid, M, D, F);
+#pragma omp parallel for schedule(static)
+    for (long r = 0; r < M; ++r)
+        for (int f = 0; f < F; ++f) {
+            const double a = hid[(size_t)r * F + f] + b1[f];
+            hid[(size_t)r * F + f] = a > 0.0 ? a : 0.0;
+        }
+    matmul(hid, W2, y, M, F, D);
+#pragma omp parallel for schedule(static)
+    for (long r = 0; r < M; ++r)
+        for (int c = 0; c < D; ++c)
+            y[(size_t)r * D + c] += b2[c];
+    free(hid);
+    return 0;
+}
+
 /* Number of host threads OpenMP will use (for reporting). */
 int oracle_num_threads(void)
 {

@@ -43,6 +43,14 @@ MUTATIONS = [
      "dqb[(size_t)i * d + c] += ds *"),
     ("backward dV from dP instead of P", "dvb[(size_t)j * d + c] += p[j] * gi[c];",
      "dvb[(size_t)j * d + c] += dp[j] * gi[c];"),
+    ("positional encoding sin and cos swapped", "(c % 2 == 0) ? sin(angle) : cos(angle)",
+     "(c % 2 == 0) ? cos(angle) : sin(angle)"),
+    ("positional encoding exponent i instead of 2i", "const int i2 = c - (c % 2); /* 2i */",
+     "const int i2 = c / 2; /* 2i */"),
+    ("feed-forward network without the ReLU", "hid[(size_t)r * F + f] = a > 0.0 ? a : 0.0;",
+     "hid[(size_t)r * F + f] = a;"),
+    ("feed-forward network output bias dropped", "y[(size_t)r * D + c] += b2[c];",
+     "y[(size_t)r * D + c] += 0.0;"),
 ]
 
 

@@ -562,3 +562,86 @@ def test_backward_key_gradients_sum_to_zero_and_masked_keys_get_none():
                                       key_lens=np.array([1, 1], dtype=np.int32))
     assert np.all(dq == 0) and np.all(dk == 0)
     np.testing.assert_allclose(dv[:, :, 0], g.sum(axis=2), atol=1e-13)
+
+
+# ------------------------------------------ encoder layer: PE, FFN, composition
+def test_positional_encoding_toy_table_from_the_pages():
+    g = GOLDEN["positional_encoding_toy"]
+    pe = oracle.positional_encoding(len(g["positions"]), g["d_model"])
+    np.testing.assert_allclose(pe, g["values"], rtol=0, atol=g["tolerance"])
+
+
+def test_positional_encoding_offsets_are_rotations():
+    # the pages: for a fixed offset k, PE(pos + k) is a linear function of
+    # PE(pos) -- per frequency w the pair (sin, cos) turns by the angle k w
+    D, k = 16, 5
+    pe = oracle.positional_encoding(40, D)
+    shifted = oracle.positional_encoding(40, D, pos0=k)
+    for i in range(D // 2):
+        w = 1.0 / 10000.0 ** (2 * i / D)
+        c, s = math.cos(k * w), math.sin(k * w)
+        sin_p, cos_p = pe[:, 2 * i], pe[:, 2 * i + 1]
+        np.testing.assert_allclose(shifted[:, 2 * i], sin_p * c + cos_p * s, atol=1e-12)
+        np.testing.assert_allclose(shifted[:, 2 * i + 1], cos_p * c - sin_p * s, atol=1e-12)
+    np.testing.assert_allclose(pe[:, 0::2] ** 2 + pe[:, 1::2] ** 2, 1.0, atol=1e-14)
+
+
+def test_ffn_matches_torch_linear_relu_linear():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(121)
+    x = rng.normal(size=(3, 5, 8))
+    w1, b1 = rng.normal(size=(8, 12)), rng.normal(size=12)
+    w2, b2 = rng.normal(size=(12, 8)), rng.normal(size=8)
+    t = torch.from_numpy
+    ref = (torch.relu(t(x) @ t(w1) + t(b1)) @ t(w2) + t(b2)).numpy()
+    np.testing.assert_allclose(oracle.ffn(x, w1, b1, w2, b2), ref, rtol=0, atol=1e-12)
+    # the ReLU is there: with every pre-activation negative the output is b2
+    np.testing.assert_allclose(oracle.ffn(np.abs(x), -np.abs(w1), -np.ones(12), w2, b2),
+                               np.broadcast_to(b2, x.shape), atol=1e-15)
+
+
+def encoder_params(rng, D, F):
+    return {"w_q": rng.normal(size=(D, D)) * 0.2, "w_k": rng.normal(size=(D, D)) * 0.2,
+            "w_v": rng.normal(size=(D, D)) * 0.2, "w_o": rng.normal(size=(D, D)) * 0.2,
+            "gamma1": 1 + rng.normal(size=D) * 0.1, "beta1": rng.normal(size=D) * 0.1,
+            "w1": rng.normal(size=(D, F)) * 0.2, "b1": rng.normal(size=F) * 0.1,
+            "w2": rng.normal(size=(F, D)) * 0.2, "b2": rng.normal(size=D) * 0.1,
+            "gamma2": 1 + rng.normal(size=D) * 0.1, "beta2": rng.normal(size=D) * 0.1}
+
+
+@pytest.mark.parametrize("mask", [MASK_NONE, MASK_KEY_PADDING])
+def test_encoder_layer_matches_torch_transformer_encoder_layer(mask):
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(122)
+    B, T, D, h, F = 2, 6, 16, 2, 24
+    x = rng.normal(size=(B, T, D))
+    p = encoder_params(rng, D, F)
+    lens = np.array([6, 3], dtype=np.int32)
+    layer = torch.nn.TransformerEncoderLayer(D, h, dim_feedforward=F, dropout=0.0,
+                                             activation="relu", batch_first=True,
+                                             norm_first=False, dtype=torch.float64)
+    t = torch.from_numpy
+    with torch.no_grad():
+        # row-vector weights (y = x W) map to torch's (out, in) matrices
+        layer.self_attn.in_proj_weight.copy_(t(np.concatenate([p["w_q"], p["w_k"], p["w_v"]], 1).T))
+        layer.self_attn.in_proj_bias.zero_()
+        layer.self_attn.out_proj.weight.copy_(t(p["w_o"].T))
+        layer.self_attn.out_proj.bias.zero_()
+        layer.linear1.weight.copy_(t(p["w1"].T))
+        layer.linear1.bias.copy_(t(p["b1"]))
+        layer.linear2.weight.copy_(t(p["w2"].T))
+        layer.linear2.bias.copy_(t(p["b2"]))
+        layer.norm1.weight.copy_(t(p["gamma1"]))
+        layer.norm1.bias.copy_(t(p["beta1"]))
+        layer.norm2.weight.copy_(t(p["gamma2"]))
+        layer.norm2.bias.copy_(t(p["beta2"]))
+    layer.norm1.eps = layer.norm2.eps = 1e-5
+    layer.eval()
+    pad = None
+    if mask == MASK_KEY_PADDING:
+        pad = torch.arange(T)[None, :] >= t(lens)[:, None]
+    with torch.no_grad():
+        ref = layer(t(x), src_key_padding_mask=pad).numpy()
+    got = oracle.encoder_layer(x, p, h=h, eps=1e-5, mask=mask,
+                               key_lens=lens if mask == MASK_KEY_PADDING else None)
+    np.testing.assert_allclose(got, ref, rtol=0, atol=1e-10)
