@@ -132,6 +132,42 @@ mha_status sdpa_backward(mha_dtype dt, const void *q, const void *k, const void 
                          int *status_dev, cudaStream_t stream);
 
 /*
+ * Adds the sinusoidal positional encoding to embedding rows (bf16):
+ *   out[b, t, 2i]   = x[b, t, 2i]   + sin(pos / 10000^(2i/d_model)),
+ *   out[b, t, 2i+1] = x[b, t, 2i+1] + cos(pos / 10000^(2i/d_model)),
+ * pos = pos0 + t ("Attention is All You Need" notebook chapter, Positional
+ * Encoding; aiany.app Step 8).  x, out (B, T, d_model), 16-byte aligned, may
+ * be the same buffer; d_model % 8 == 0; pos0 + T < 2^24.
+ */
+mha_status positional_encoding_add(const void *x, void *out, int B, int T, int d_model, int pos0,
+                                   cudaStream_t stream);
+
+/*
+ * One encoder layer with post-normalisation (bf16), the Transformer's
+ * "self-attention -> add & normalise -> feed-forward -> add & normalise"
+ * block (aiany.app Steps 9-10; notebook chapter "Feed-Forward Network"):
+ *   y   = LayerNorm1(x + MultiHead(x, x)),
+ *   out = LayerNorm2(y + FFN(y)),  FFN(y) = max(0, y W1 + b1) W2 + b2.
+ *   x, out (B, T, d_model); W^Q, W^K, W^V, W^O (d_model, d_model) with h heads
+ *   of 64 (d_model == 64 h); W1 (d_model, d_ff), b1 (d_ff), W2 (d_ff,
+ *   d_model), b2, gamma1/beta1, gamma2/beta2 (d_model); all bf16 device
+ *   arrays, 16-byte aligned.  d_ff % 64 == 0; d_model as
+ *   mha_forward_add_layernorm.  mask, key_lens, scale, eps, status_dev as there.
+ *   workspace: >= encoder_layer_workspace_bytes() bytes, 256-byte aligned.
+ * Five launches: the three of the attention sublayer (its output projection
+ * normalises), the first FFN GEMM with a bias + ReLU epilogue, the second FFN
+ * GEMM with the bias, residual and normalisation in its epilogue.
+ */
+size_t encoder_layer_workspace_bytes(int B, int T, int d_model, int h, int d_ff);
+mha_status encoder_layer_forward(const void *x, const void *w_q, const void *w_k, const void *w_v,
+                                 const void *w_o, const void *gamma1, const void *beta1,
+                                 const void *w1, const void *b1, const void *w2, const void *b2,
+                                 const void *gamma2, const void *beta2, float eps, void *out,
+                                 void *workspace, size_t workspace_bytes, int B, int T, int d_model,
+                                 int h, int d_ff, float scale, mha_mask mask,
+                                 const int32_t *key_lens, int *status_dev, cudaStream_t stream);
+
+/*
  * Attention for decoding steps (bf16): each of the T_q new query rows of a
  * (b, h) attends to the first cache_lens[b] rows of that sequence's key/value
  * cache,

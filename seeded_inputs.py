@@ -38,7 +38,9 @@ _M2 = np.uint64(0x94D049BB133111EB)
 
 TENSOR_IDS = {"x_q": 0, "x_kv": 1, "q": 2, "k": 3, "v": 4,
               "w_q": 5, "w_k": 6, "w_v": 7, "w_o": 8, "key_lens": 9,
-              "ln_gamma": 10, "ln_beta": 11, "dout": 12}
+              "ln_gamma": 10, "ln_beta": 11, "dout": 12,
+              "ffn_w1": 13, "ffn_b1": 14, "ffn_w2": 15, "ffn_b2": 16, "ln2_gamma": 17,
+              "ln2_beta": 18}
 
 MASK_NONE, MASK_CAUSAL, MASK_KEY_PADDING, MASK_CAUSAL_KEY_PADDING = 0, 1, 2, 3
 
@@ -104,6 +106,27 @@ def layernorm_params(seed: int, d_model: int) -> dict:
     return out
 
 
+def encoder_params(seed: int, d_model: int, d_ff: int) -> dict:
+    """Parameters of one encoder layer beyond the attention projections
+    (which make_inputs draws): layer-norm gains and shifts of both sublayers
+    (as layernorm_params) and the feed-forward network W1 (d_model, d_ff),
+    b1, W2 (d_ff, d_model), b2 -- Xavier-uniform matrices, N(0,1)/8 biases --
+    all rounded to bf16.  Float64 values and raw bits under '*_bits'."""
+    out = {}
+    ln1 = layernorm_params(seed, d_model)
+    out.update({"gamma1": ln1["gamma"], "beta1": ln1["beta"]})
+    for name, base in (("gamma2", 1.0), ("beta2", 0.0)):
+        tid = TENSOR_IDS["ln2_" + name[:-1]]
+        out[name] = round_bf16(base + normal(seed, tid, (d_model,)) / 8.0)
+    out["w1"] = round_bf16(xavier_uniform(seed, TENSOR_IDS["ffn_w1"], (d_model, d_ff), d_model, d_ff))
+    out["w2"] = round_bf16(xavier_uniform(seed, TENSOR_IDS["ffn_w2"], (d_ff, d_model), d_ff, d_model))
+    out["b1"] = round_bf16(normal(seed, TENSOR_IDS["ffn_b1"], (d_ff,)) / 8.0)
+    out["b2"] = round_bf16(normal(seed, TENSOR_IDS["ffn_b2"], (d_model,)) / 8.0)
+    for name in list(out):
+        out[name + "_bits"] = f64_to_bf16_bits(out[name])
+    return out
+
+
 def f64_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """Round (via fp32, RNE) to bf16 and return the raw uint16 bits."""
     b = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
@@ -163,7 +186,13 @@ WORKLOADS = [
     # 8192 slots, of which the first len_b (uniform in [2048, 8192]) hold keys.
     Workload("decode_bf16_B16_h16_Tq1_cache8192", "sdpa", "bf16", B=16, h=16, T_q=1,
              T_k=8192, mask=MASK_KEY_PADDING, len_lo=2048, len_hi=8192, seed=5),
+    # One encoder layer of the base model (d_model 512, 8 heads, d_ff 2048):
+    # attention sublayer + feed-forward sublayer, each with residual and
+    # layer normalisation; inputs as the MHA workloads, d_ff in ENCODER_D_FF.
+    Workload("encoder_layer_D512_h8_ff2048_B16_T512", "mha", "bf16", B=16, h=8, T_q=512,
+             T_k=512, d_model=512, mask=MASK_KEY_PADDING, len_lo=256, len_hi=512, seed=6),
 ]
+ENCODER_D_FF = 2048
 
 
 def make_inputs(w: Workload) -> dict:

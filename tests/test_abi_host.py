@@ -175,3 +175,33 @@ def test_backward_rejects_bad_arguments(lib):
     # fp32 dq accumulator + two per-row vectors over whole 128-row blocks
     assert lib.lib.sdpa_backward_workspace_bytes(2, 3, 130, 7, 64, 64) == (
         2 * 3 * 256 * 64 * 4 + 2 * 2 * 3 * 256 * 4)
+
+
+def enc(lib, x=FAKE, ws=FAKE, ws_bytes=1 << 40, B=1, T=8, D=128, h=2, F=256, eps=1e-5, w1=FAKE):
+    return lib.lib.encoder_layer_forward(x, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, w1, FAKE, FAKE, FAKE,
+                                         FAKE, FAKE, eps, FAKE, ws, ws_bytes, B, T, D, h, F, 0.125, 0,
+                                         None, None, None)
+
+
+def test_encoder_layer_rejects_bad_arguments(lib):
+    assert enc(lib, x=None) == lib.MHA_ERR_INVALID_ARG
+    assert enc(lib, w1=None) == lib.MHA_ERR_INVALID_ARG
+    assert enc(lib, eps=-1.0) == lib.MHA_ERR_INVALID_ARG
+    assert enc(lib, F=100) == lib.MHA_ERR_UNSUPPORTED          # d_ff % 64
+    assert enc(lib, D=192, h=2) == lib.MHA_ERR_UNSUPPORTED     # d_model != 64 h
+    assert enc(lib, ws=None) == lib.MHA_ERR_WORKSPACE
+    assert enc(lib, ws_bytes=1000) == lib.MHA_ERR_WORKSPACE
+    assert enc(lib, w1=FAKE + 2) == lib.MHA_ERR_MISALIGNED
+    assert enc(lib, B=0) == lib.MHA_OK
+    # attention workspace + the sublayer output + the hidden activations
+    assert lib.lib.encoder_layer_workspace_bytes(2, 8, 128, 2, 256) == (
+        lib.lib.mha_workspace_bytes(2, 2, 8, 8, 64, 64) + 2 * 8 * 128 * 2 + 2 * 8 * 256 * 2)
+
+
+def test_positional_encoding_rejects_bad_arguments(lib):
+    f = lib.lib.positional_encoding_add
+    assert f(None, FAKE, 1, 4, 64, 0, None) == lib.MHA_ERR_INVALID_ARG
+    assert f(FAKE, FAKE, 1, 4, 60, 0, None) == lib.MHA_ERR_UNSUPPORTED
+    assert f(FAKE, FAKE, 1, 4, 64, -1, None) == lib.MHA_ERR_INVALID_ARG
+    assert f(FAKE + 4, FAKE, 1, 4, 64, 0, None) == lib.MHA_ERR_MISALIGNED
+    assert f(FAKE, FAKE, 0, 4, 64, 0, None) == lib.MHA_OK

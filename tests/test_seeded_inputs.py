@@ -62,7 +62,7 @@ def test_bf16_rounding_matches_torch():
 
 def test_workload_table_matches_stated_shapes():
     w = si.WORKLOADS
-    assert [x.seed for x in w] == [0, 1, 2, 3, 4, 5]
+    assert [x.seed for x in w] == [0, 1, 2, 3, 4, 5, 6]
     assert (w[0].B, w[0].h, w[0].T_q, w[0].dtype, w[0].scale) == (1, 8, 16, "f32", 0.125)
     assert (w[1].d_model, w[1].B, w[1].T_q, w[1].len_lo, w[1].len_hi) == (512, 32, 128, 64, 128)
     assert (w[2].B, w[2].T_q, w[2].mask) == (16, 512, si.MASK_CAUSAL)
@@ -70,6 +70,7 @@ def test_workload_table_matches_stated_shapes():
     assert (w[4].B, w[4].h, w[4].T_q, w[4].mask) == (2, 16, 8192, si.MASK_CAUSAL)
     assert (w[5].B, w[5].h, w[5].T_q, w[5].T_k, w[5].mask, w[5].len_lo, w[5].len_hi) == (
         16, 16, 1, 8192, si.MASK_KEY_PADDING, 2048, 8192)
+    assert (w[6].d_model, w[6].h, w[6].B, w[6].T_q, si.ENCODER_D_FF) == (512, 8, 16, 512, 2048)
 
 
 def test_make_inputs_small():

@@ -16,7 +16,8 @@ from . import _native
 from ._native import (MHA_BF16, MHA_F32, MHA_MASK_CAUSAL, MHA_MASK_CAUSAL_KEY_PADDING,
                       MHA_MASK_KEY_PADDING, MHA_MASK_NONE, MHA_OK, lib)
 
-__all__ = ["sdpa_forward", "sdpa_forward_lse", "sdpa_backward", "sdpa_decode_forward", "mha_forward", "mha_forward_add_layernorm", "mha_workspace_bytes", "status_string", "MhaError",
+__all__ = ["sdpa_forward", "sdpa_forward_lse", "sdpa_backward", "positional_encoding_add",
+           "encoder_layer_forward", "ENCODER_PARAMS", "sdpa_decode_forward", "mha_forward", "mha_forward_add_layernorm", "mha_workspace_bytes", "status_string", "MhaError",
            "MASKS", "lib"]
 
 MASKS = {"none": MHA_MASK_NONE, "causal": MHA_MASK_CAUSAL, "key_padding": MHA_MASK_KEY_PADDING,
@@ -160,6 +161,57 @@ def sdpa_backward(q, k, v, o, dout, lse, dq=None, dk=None, dv=None, workspace=No
     if rc != MHA_OK:
         raise MhaError(rc, "sdpa_backward")
     return dq, dk, dv
+
+
+def positional_encoding_add(x, out=None, *, pos0=0, stream=None):
+    """x + PE(pos0 + t) for bf16 embedding rows x (B, T, d_model); out may be x."""
+    torch = _torch()
+    _check_dev("x", x, torch.bfloat16)
+    B, T, D = x.shape
+    out = torch.empty_like(x) if out is None else out
+    _check_dev("out", out, torch.bfloat16)
+    rc = lib.positional_encoding_add(_ptr(x), _ptr(out), B, T, D, int(pos0), _stream_handle(stream))
+    if rc != MHA_OK:
+        raise MhaError(rc, "positional_encoding_add")
+    return out
+
+
+ENCODER_PARAMS = ("w_q", "w_k", "w_v", "w_o", "gamma1", "beta1", "w1", "b1", "w2", "b2", "gamma2",
+                  "beta2")
+
+
+def encoder_layer_forward(x, params, h, out=None, workspace=None, *, eps=1e-5, scale=None,
+                          mask="none", key_lens=None, status=None, stream=None):
+    """One post-LN encoder layer: y = LN1(x + MHA(x, x)), out = LN2(y + FFN(y)).
+    params: dict of bf16 CUDA tensors named as ENCODER_PARAMS (W^Q..W^O
+    (D, D), gamma/beta (D), w1 (D, F), b1 (F), w2 (F, D), b2 (D))."""
+    torch = _torch()
+    bf = torch.bfloat16
+    _check_dev("x", x, bf)
+    for n in ENCODER_PARAMS:
+        _check_dev(n, params[n], bf)
+    B, T, D = x.shape
+    F = params["w1"].shape[1]
+    out = torch.empty_like(x) if out is None else out
+    _check_dev("out", out, bf)
+    need = int(lib.encoder_layer_workspace_bytes(B, T, D, h, F))
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=x.device)
+    _check_dev("workspace", workspace)
+    if key_lens is not None:
+        _check_dev("key_lens", key_lens, torch.int32)
+    if status is not None:
+        _check_dev("status", status, torch.int32)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D // h)
+    rc = lib.encoder_layer_forward(_ptr(x), *[_ptr(params[n]) for n in ENCODER_PARAMS], float(eps),
+                                   _ptr(out), _ptr(workspace),
+                                   workspace.numel() * workspace.element_size(), B, T, D, h, F,
+                                   float(scale), _mask_code(mask), _ptr(key_lens), _ptr(status),
+                                   _stream_handle(stream))
+    if rc != MHA_OK:
+        raise MhaError(rc, "encoder_layer_forward")
+    return out
 
 
 def sdpa_decode_forward(q, k_cache, v_cache, cache_lens=None, out=None, *, scale=None,

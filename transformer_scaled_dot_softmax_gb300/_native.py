@@ -26,6 +26,10 @@ SIGNATURES = {
     "sdpa_backward_workspace_bytes": (_sz, [_ci, _ci, _ci, _ci, _ci, _ci]),
     "sdpa_backward": (_ci, [_ci, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _ci, _ci,
                             _ci, _ci, _ci, _ci, _cf, _ci, _vp, _vp, _vp]),
+    "positional_encoding_add": (_ci, [_vp, _vp, _ci, _ci, _ci, _ci, _vp]),
+    "encoder_layer_workspace_bytes": (_sz, [_ci, _ci, _ci, _ci, _ci]),
+    "encoder_layer_forward": (_ci, [_vp] * 13 + [_cf, _vp, _vp, _sz, _ci, _ci, _ci, _ci, _ci, _cf,
+                                                _ci, _vp, _vp, _vp]),
     "sdpa_decode_forward": (_ci, [_vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _ci, _cf, _vp,
                                   _vp]),
     "mha_workspace_bytes": (_sz, [_ci, _ci, _ci, _ci, _ci, _ci]),

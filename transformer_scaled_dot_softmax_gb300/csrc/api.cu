@@ -478,6 +478,108 @@ MHA_EXPORT mha_status mha_forward(mha_dtype dt, const void *x_q, const void *x_k
                     nullptr);
 }
 
+MHA_EXPORT mha_status positional_encoding_add(const void *x, void *out, int B, int T, int d_model,
+                                              int pos0, cudaStream_t stream) {
+    if (B < 0 || T < 0 || d_model <= 0 || pos0 < 0) return MHA_ERR_INVALID_ARG;
+    if (d_model % 8 != 0) return MHA_ERR_UNSUPPORTED;
+    if (static_cast<long long>(pos0) + T >= (1ll << 24)) return MHA_ERR_UNSUPPORTED;  // exact fp32 positions
+    if (B == 0 || T == 0) return MHA_OK;
+    if (!x || !out) return MHA_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(out)) return MHA_ERR_MISALIGNED;
+    return launch_status(mha::launch_posenc_add_bf16(static_cast<const __nv_bfloat16 *>(x),
+                                                     static_cast<__nv_bfloat16 *>(out),
+                                                     static_cast<long long>(B) * T, T, d_model,
+                                                     pos0, stream),
+                         "positional encoding launch");
+}
+
+MHA_EXPORT size_t encoder_layer_workspace_bytes(int B, int T, int d_model, int h, int d_ff) {
+    if (B < 0 || T < 0 || d_model < 0 || h < 0 || d_ff < 0) return 0;
+    const size_t rows = static_cast<size_t>(B) * T;
+    return round256(mha_workspace_bytes(B, h, T, T, 64, 64)) + round256(rows * d_model * 2) +
+           round256(rows * d_ff * 2);
+}
+
+MHA_EXPORT mha_status encoder_layer_forward(
+    const void *x, const void *w_q, const void *w_k, const void *w_v, const void *w_o,
+    const void *gamma1, const void *beta1, const void *w1, const void *b1, const void *w2,
+    const void *b2, const void *gamma2, const void *beta2, float eps, void *out, void *workspace,
+    size_t workspace_bytes, int B, int T, int d_model, int h, int d_ff, float scale, mha_mask mask,
+    const int32_t *key_lens, int *status_dev, cudaStream_t stream) {
+    if (B < 0 || T < 0 || d_model <= 0 || h <= 0 || d_ff <= 0) return MHA_ERR_INVALID_ARG;
+    if (d_ff % 64 != 0 || d_model != h * 64) return MHA_ERR_UNSUPPORTED;
+    if (B == 0 || T == 0) return MHA_OK;
+    if (!x || !out || !w1 || !b1 || !w2 || !b2 || !gamma2 || !beta2) return MHA_ERR_INVALID_ARG;
+    if (!(eps >= 0.f && isfinite(eps))) return MHA_ERR_INVALID_ARG;
+    if (!aligned16(w1) || !aligned16(b1) || !aligned16(w2) || !aligned16(b2) || !aligned16(gamma2) ||
+        !aligned16(beta2))
+        return MHA_ERR_MISALIGNED;
+    if (!workspace || workspace_bytes < encoder_layer_workspace_bytes(B, T, d_model, h, d_ff))
+        return MHA_ERR_WORKSPACE;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MHA_ERR_MISALIGNED;
+    const size_t rows = static_cast<size_t>(B) * T;
+    const size_t mha_ws = round256(mha_workspace_bytes(B, h, T, T, 64, 64));
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    void *y1 = ws + mha_ws;
+    void *hid = ws + mha_ws + round256(rows * d_model * 2);
+    // 1. y1 = LayerNorm1(x + MultiHead(x, x)): the attention sublayer (checks
+    //    the remaining arguments, including d_model's support by the fused
+    //    normalisation).
+    const LnArgs ln1{gamma1, beta1, eps};
+    mha_status s = mha_impl(MHA_BF16, x, x, w_q, w_k, w_v, w_o, y1, ws, mha_ws, B, h, T, T,
+                            d_model, 64, 64, scale, mask, key_lens, status_dev, stream, &ln1);
+    if (s != MHA_OK) return s;
+    int sms = 0;
+    if (mha::sm_count(&sms) != cudaSuccess || sms <= 0)
+        return cuda_fail("cudaDeviceGetAttribute", "SM count");
+    const long long M = static_cast<long long>(rows);
+    // 2. hid = max(0, y1 W1 + b1): projection GEMM with a bias + ReLU epilogue.
+    CUtensorMap ta[mha::kGemmMaxProblems], tb[mha::kGemmMaxProblems];
+    mha::GemmParams gp{};
+    gp.status = status_dev;
+    gp.bn = choose_bn(&M, 1, d_ff, sms);
+    if ((s = encode_act(&ta[0], y1, M, d_model)) != MHA_OK) return s;
+    if ((s = encode_weight(&tb[0], w1, d_model, d_ff, gp.bn)) != MHA_OK) return s;
+    for (int i = 1; i < mha::kGemmMaxProblems; ++i) {
+        ta[i] = ta[0];
+        tb[i] = tb[0];
+    }
+    mha::GemmProblem &pr = gp.prob[0];
+    pr.M = static_cast<int>(M);
+    pr.N = d_ff;
+    pr.K = d_model;
+    pr.tiles_n = (d_ff + gp.bn - 1) / gp.bn;
+    pr.tile_start = 0;
+    pr.tile_count = pr.tiles_n * static_cast<int>((M + mha::kGemmBM - 1) / mha::kGemmBM);
+    pr.out = static_cast<__nv_bfloat16 *>(hid);
+    pr.out_mode = mha::kOutRowMajor;
+    pr.bias = static_cast<const __nv_bfloat16 *>(b1);
+    pr.relu = 1;
+    gp.num_problems = 1;
+    gp.total_tiles = pr.tile_count;
+    if ((s = launch_status(mha::launch_gemm_bf16(ta, tb, gp, stream), "feed-forward GEMM launch")) !=
+        MHA_OK)
+        return s;
+    // 3. out = LayerNorm2(y1 + hid W2 + b2): the normalising GEMM with a bias.
+    mha::LnParams lp{};
+    lp.M = static_cast<int>(M);
+    lp.D = d_model;
+    lp.K = d_ff;
+    lp.bn = mha::ln_tile_width(d_model, M, sms);
+    lp.resid = static_cast<const __nv_bfloat16 *>(y1);
+    lp.bias = static_cast<const __nv_bfloat16 *>(b2);
+    lp.gamma = static_cast<const __nv_bfloat16 *>(gamma2);
+    lp.beta = static_cast<const __nv_bfloat16 *>(beta2);
+    lp.eps = eps;
+    lp.out = static_cast<__nv_bfloat16 *>(out);
+    lp.status = status_dev;
+    CUtensorMap la, lb;
+    if ((s = encode_act(&la, hid, M, d_ff)) != MHA_OK) return s;
+    if ((s = encode_weight(&lb, w2, d_ff, d_model, lp.bn)) != MHA_OK) return s;
+    return launch_status(mha::launch_gemm_ln_bf16(la, lb, lp, stream),
+                         "feed-forward output + layer norm launch");
+}
+
 MHA_EXPORT mha_status mha_forward_add_layernorm(
     mha_dtype dt, const void *x_q, const void *x_kv, const void *w_q, const void *w_k,
     const void *w_v, const void *w_o, const void *gamma, const void *beta, float eps, void *out,

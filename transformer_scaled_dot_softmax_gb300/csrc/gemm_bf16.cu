@@ -23,7 +23,8 @@
 //               output columns (96 instead of 128 bytes per cycle at the
 //               tensor rate).
 //   warps 2-5   epilogue: tensor memory -> registers (the buffer is handed
-//               back as soon as it is read) -> bf16 -> global.  In head-split
+//               back as soon as it is read) -> [+ bias, ReLU] -> bf16 ->
+//               global.  In head-split
 //               mode column n = head*64 + c of row m = b*T + t is stored at
 //               ((b*H + head)*T + t)*64 + c, i.e. straight into the
 //               (B, H, T, 64) layout attention reads -- the view/transpose of
@@ -235,10 +236,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int n0 = t.tn * BN + grp * 128 + c * 32;
                     if (n0 < pr.N) {
                         uint32_t packed[16];
+                        if (pr.bias) {
+                            // bias (+ ReLU): the feed-forward network's first layer
 #pragma unroll
-                        for (int q = 0; q < 16; ++q)
-                            packed[q] = pack_bf16x2(__uint_as_float(r[c][2 * q]),
-                                                    __uint_as_float(r[c][2 * q + 1]));
+                            for (int q = 0; q < 4; ++q) {
+                                const uint4 bw = *reinterpret_cast<const uint4 *>(pr.bias + n0 + 8 * q);
+                                const uint32_t bb[4] = {bw.x, bw.y, bw.z, bw.w};
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    float y0 = __uint_as_float(r[c][8 * q + 2 * e]) + __uint_as_float(bb[e] << 16);
+                                    float y1 = __uint_as_float(r[c][8 * q + 2 * e + 1]) +
+                                               __uint_as_float(bb[e] & 0xffff0000u);
+                                    if (pr.relu) {
+                                        y0 = fmaxf(y0, 0.f);
+                                        y1 = fmaxf(y1, 0.f);
+                                    }
+                                    packed[4 * q + e] = pack_bf16x2(y0, y1);
+                                }
+                            }
+                        } else {
+#pragma unroll
+                            for (int q = 0; q < 16; ++q)
+                                packed[q] = pack_bf16x2(__uint_as_float(r[c][2 * q]),
+                                                        __uint_as_float(r[c][2 * q + 1]));
+                        }
                         __nv_bfloat16 *dst;
                         if (pr.out_mode == kOutHeadSplit) {
                             const int head = n0 >> 6, c0 = n0 & 63;

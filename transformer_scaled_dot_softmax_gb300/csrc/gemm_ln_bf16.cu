@@ -1,7 +1,8 @@
 // gemm_ln_bf16.cu -- output projection fused with the residual connection and
 // layer normalisation that wrap the attention sublayer, for sm_103a:
 //
-//   out = LayerNorm(x + Concat(heads) W^O),
+//   out = LayerNorm(x + Concat(heads) W^O),  or, for the feed-forward
+//   sublayer, LayerNorm(x + H W_2 + b_2) (the same kernel with a bias),
 //   LayerNorm(v) = (v - mu) / sqrt(var + eps) * gamma + beta per row,
 //
 // ("Attention Is All You Need" (aiany.app) Step 9, LayerNorm(x + Sublayer(x));
@@ -86,6 +87,16 @@ __device__ __forceinline__ void bf16x8(const uint4 &u, float (&f)[8]) {
         f[2 * i] = __uint_as_float(w[i] << 16);
         f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
     }
+}
+
+// x[0..7] += bias[n .. n+7] (bf16), if there is a bias: the residual and the
+// sublayer's output bias enter the row together.
+__device__ __forceinline__ void add_bias(float (&x)[8], const __nv_bfloat16 *bias, int n) {
+    if (!bias) return;
+    float b[8];
+    bf16x8(*reinterpret_cast<const uint4 *>(bias + n), b);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] += b[e];
 }
 
 template <int BN>
@@ -192,6 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int q = 0; q < 4; ++q) {
                         float xf[8];
                         bf16x8(*reinterpret_cast<const uint4 *>(xr + 32 * c + 8 * q), xf);
+                        add_bias(xf, p.bias, n_base + 32 * c + 8 * q);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) s1 += __uint_as_float(acc[8 * q + e]) + xf[e];
                     }
@@ -224,6 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int q = 0; q < 4; ++q) {
                         float xf[8];
                         bf16x8(*reinterpret_cast<const uint4 *>(xr + 32 * c + 8 * q), xf);
+                        add_bias(xf, p.bias, n_base + 32 * c + 8 * q);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
                             const float d = __uint_as_float(acc[8 * q + e]) + xf[e] - mu;
@@ -257,6 +270,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int q = 0; q < 4; ++q) {
                     float xf[8], gf[8], bf[8];
                     bf16x8(*reinterpret_cast<const uint4 *>(xr + 32 * c + 8 * q), xf);
+                    add_bias(xf, p.bias, n_base + 32 * c + 8 * q);
                     bf16x8(*reinterpret_cast<const uint4 *>(p.gamma + n_base + 32 * c + 8 * q), gf);
                     bf16x8(*reinterpret_cast<const uint4 *>(p.beta + n_base + 32 * c + 8 * q), bf);
                     uint32_t packed[4];

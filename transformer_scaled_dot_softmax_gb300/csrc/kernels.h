@@ -68,6 +68,11 @@ cudaError_t launch_attn_bwd_bf16(const CUtensorMap &tq, const CUtensorMap &tk, c
                                  const __nv_bfloat16 *dout, const float *lse, __nv_bfloat16 *dq,
                                  BwdParams p, void *workspace, cudaStream_t stream);
 
+// ------------------------------------------------ positional encoding
+// out (rows, D) = x + PE(pos0 + row % T); D % 8 == 0; x and out may alias.
+cudaError_t launch_posenc_add_bf16(const __nv_bfloat16 *x, __nv_bfloat16 *out, long long rows, int T,
+                                   int D, int pos0, cudaStream_t stream);
+
 // ------------------------------------------------ fp32 SIMT attention
 cudaError_t launch_sdpa_f32(const float *q, const float *k, const float *v, float *o, int B,
                             int H, int Tq, int Tk, int dk, int dv, float scale, int mask,
@@ -83,6 +88,8 @@ struct GemmProblem {
     int out_mode;  // kOutRowMajor: out (M, N); kOutHeadSplit: row m = b*T + t,
                    // column n = head*64 + c -> out ((b*H + head)*T + t)*64 + c
     int T, H;
+    const __nv_bfloat16 *bias;  // optional (N): added to every row
+    int relu;                   // nonzero: max(0, .) after the bias
 };
 struct GemmParams {
     int num_problems;
@@ -105,9 +112,10 @@ cudaError_t sm_count(int *sms);
 // ------------------------------------ output projection + residual + LayerNorm
 constexpr int kLnMaxCluster = 8;  // CTAs per 128-row block (portable cluster size)
 struct LnParams {
-    int M, D, K;                  // out (M, D) = LN(resid + A (M, K) W (K, D))
+    int M, D, K;                  // out (M, D) = LN(resid + A (M, K) W (K, D) [+ bias])
     int bn;                       // columns per CTA: ln_tile_width(D)
     const __nv_bfloat16 *resid;   // (M, D)
+    const __nv_bfloat16 *bias;    // optional (D): added to the product before the residual
     const __nv_bfloat16 *gamma;   // (D)
     const __nv_bfloat16 *beta;    // (D)
     float eps;
