@@ -367,6 +367,28 @@ def time_other_workloads(dev, stream, flush, iters=20):
             "ms": ms_ln, "tflops": fl / (ms_ln * 1e-3) / 1e12, "flops": fl,
             "kind": "LayerNorm(x + MHA(x)): W^O GEMM with residual add and normalisation "
                     "in its epilogue (cluster per 128-row block)"}
+    # one encoder layer of the base model (attention + FFN sublayers, both normalised)
+    w = si.WORKLOADS[6]
+    x = si.make_inputs(w)
+    F = si.ENCODER_D_FF
+    ep = si.encoder_params(w.seed, w.d_model, F)
+    params = {n: dv(ep[n + "_bits"]) for n in ("gamma1", "beta1", "w1", "b1", "w2", "b2", "gamma2",
+                                               "beta2")}
+    for n in ("w_q", "w_k", "w_v", "w_o"):
+        params[n] = dv(x[n + "_bits"])
+    xe = dv(x["x_q_bits"])
+    lens = torch.from_numpy(x["key_lens"]).to(dev)
+    oute = torch.empty_like(xe)
+    wse = torch.empty(int(tsds.lib.encoder_layer_workspace_bytes(w.B, w.T_q, w.d_model, w.h, F)),
+                      dtype=torch.uint8, device=dev)
+    ms = timed(lambda: tsds.encoder_layer_forward(xe, params, w.h, oute, wse, scale=w.scale,
+                                                  mask=w.mask, key_lens=lens, stream=stream))
+    fl = mha_flops(w, x["key_lens"]) + 4.0 * w.B * w.T_q * w.d_model * F
+    res[w.name] = {"ms": ms, "tflops": fl / (ms * 1e-3) / 1e12, "flops": fl,
+                   "kind": "one post-LN encoder layer: MHA + FFN (d_ff 2048), 5 launches; "
+                           "FLOPs = projections + visible-pair attention + the two FFN GEMMs"}
+    del xe, oute, wse, params
+
     # backward of the headline workload (dq, dk, dv from q, k, v, o, lse, dO)
     w = si.WORKLOADS[4]
     x = si.make_inputs(w)
