@@ -91,7 +91,7 @@ __global__ void attn_bwd_post(const float *__restrict__ dq_acc, __nv_bfloat16 *_
 // ------------------------------------------------------------------- main
 // One CTA = one (b, h) and a block of 128 keys; it walks the query blocks j
 // that see any of its keys (all of them, or j >= kb under the causal mask).
-// Warp roles (10 warps):
+// Warp roles (14 warps):
 //
 //   warp 0      TMA: the K and V blocks once; per query block Q_j, dO_j (3-D
 //               tensor maps) and its 128 lse and D values (bulk copies) into
@@ -107,19 +107,26 @@ __global__ void attn_bwd_post(const float *__restrict__ dq_acc, __nv_bfloat16 *_
 //               Computing S and dP transposed puts the keys on the
 //               tensor-memory lanes, so P^T and dS^T feed (3) and (4) straight
 //               from tensor memory.
-//   warps 2-5   one thread per key (tensor-memory lane): P^T = 2^(S^T c - lse_j)
-//               (masked: 0), dS^T = P^T (dP^T - D_j); P^T and dS^T written back
-//               over S^T and dP^T (bf16), dS^T also into shared memory for (5).
-//               At the end: dK (times scale) and dV out of tensor memory, bf16.
-//   warps 6-9   one thread per query row: dQ_j partial out of tensor memory,
+//   warps 2-9   one thread per (key, half of the query block) -- warps w and
+//               w+4 share the keys of lane quadrant w%4 and take queries
+//               [0,64) and [64,128): P^T = 2^(S^T c - lse_j) (masked: 0),
+//               dS^T = P^T (dP^T - D_j), elementwise (lse and D are per-query
+//               inputs, no row reduction); P^T and dS^T written as bf16, dS^T
+//               also into shared memory for (5).  At the end the first half
+//               writes dK (times scale), the second dV.
+//   warps 10-13 one thread per query row: dQ_j partial out of tensor memory,
 //               added to the fp32 accumulator in global memory (other key
 //               blocks add theirs).
 //
-// Tensor memory: S^T [0,128) (P^T over [0,64)), dP^T [128,256) (dS^T over
-// [128,192)), dV [256,320), dK [320,384), dQ_j [384,448).
+// Tensor memory: S^T [0,128), dP^T [128,256), dV [256,320), dK [320,384),
+// dQ_j [384,448).  P^T and dS^T of queries [0,64) go over S^T [0,32) and
+// dP^T [128,160) -- columns only the warp of that half has read -- and those of
+// queries [64,128) into [448,480) and [480,512): a warp never writes columns
+// the other half still reads.
 constexpr uint32_t kTile = BQ * HD * 2;  // 16 KiB
 constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kColDQ = 384;
-constexpr int kBwdThreads = 320;
+constexpr uint32_t kColP2 = 448, kColDS2 = 480;  // P^T, dS^T of queries [64,128)
+constexpr int kBwdThreads = 448;
 
 struct __align__(1024) SmemBwd {
     uint8_t k[kTile];
@@ -133,7 +140,7 @@ struct __align__(1024) SmemBwd {
     uint64_t stage_full[2];
     uint64_t stage_empty[2];
     uint64_t sdp_full;   // (1), (2) complete
-    uint64_t pds_full;   // P^T, dS^T written (4 warps)
+    uint64_t pds_full;   // P^T, dS^T written (8 warps)
     uint64_t tmem_free;  // (3), (4) complete: S^T / dP^T columns reusable
     uint64_t ds_free;    // (5) complete: the shared dS tile reusable
     uint64_t dq_full;    // (5) complete
@@ -173,7 +180,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_init(&sm.stage_empty[i], 1);
         }
         mbar_init(&sm.sdp_full, 1);
-        mbar_init(&sm.pds_full, 4);
+        mbar_init(&sm.pds_full, 8);
         mbar_init(&sm.tmem_free, 1);
         mbar_init(&sm.ds_free, 1);
         mbar_init(&sm.dq_full, 1);
@@ -258,12 +265,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tc_fence_after_sync();
 #pragma unroll
                 for (int kk = 0; kk < BQ / 16; ++kk)
-                    warp_mma_bf16_ts(tmem + kColDV, tmem + kColS + 8 * kk, g_mn + so + 128 * kk, id_kv,
-                                     (t > 0 || kk > 0) ? 1u : 0u);
+                    warp_mma_bf16_ts(tmem + kColDV, tmem + (kk < 4 ? kColS + 8 * kk : kColP2 + 8 * (kk - 4)),
+                                     g_mn + so + 128 * kk, id_kv, (t > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
                 for (int kk = 0; kk < BQ / 16; ++kk)
-                    warp_mma_bf16_ts(tmem + kColDK, tmem + kColDP + 8 * kk, q_mn + so + 128 * kk, id_kv,
-                                     (t > 0 || kk > 0) ? 1u : 0u);
+                    warp_mma_bf16_ts(tmem + kColDK, tmem + (kk < 4 ? kColDP + 8 * kk : kColDS2 + 8 * (kk - 4)),
+                                     q_mn + so + 128 * kk, id_kv, (t > 0 || kk > 0) ? 1u : 0u);
                 warp_commit(&sm.tmem_free);
                 if (t >= 1 && !(ok = warp_wait(&sm.dq_free, (t - 1) & 1, ab))) break;
                 tc_fence_after_sync();
@@ -278,8 +285,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         warp_commit(&sm.drain);
         mbar_wait_drain(&sm.drain, 0);
-    } else if (warp < 6) {
+    } else if (warp < 10) {
         // ------------------------------------------- per-key softmax terms
+        const int half = (warp - 2) >> 2;  // queries [64 half, 64 half + 64)
+        const uint32_t p_col = half ? kColP2 : kColS, ds_col = half ? kColDS2 : kColDP;
         const uint32_t lane_base = static_cast<uint32_t>(warp & 3) * 32;
         const int r = static_cast<int>(lane_base) + lane;  // key row in the block
         const int key = k0 + r;
@@ -296,7 +305,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             if (!ok) break;
             tc_fence_after_sync();
 #pragma unroll 1
-            for (int c = 0; c < BQ / 32; ++c) {
+            for (int c = 2 * half; c < 2 * half + 2; ++c) {
                 uint32_t sv[32], dp[32];
                 tmem_ld32(tl + kColS + 32u * c, sv);
                 tmem_ld32(tl + kColDP + 32u * c, dp);
@@ -317,10 +326,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     pk[e] = pack_bf16x2(pp[0], pp[1]);
                     dsk[e] = pack_bf16x2(dd[0], dd[1]);
                 }
-                // P^T and dS^T over the scores already read (columns
-                // [16c, 16c+16) of each region were read by chunks <= c).
-                tmem_st16(tl + kColS + 16u * c, pk);
-                tmem_st16(tl + kColDP + 16u * c, dsk);
+                // P^T and dS^T: the first half writes over S^T / dP^T columns
+                // [16c, 16c+16) it has already read (chunks <= c); the second
+                // half into its own columns.
+                tmem_st16(tl + p_col + 16u * (c - 2 * half), pk);
+                tmem_st16(tl + ds_col + 16u * (c - 2 * half), dsk);
                 // dS into shared memory as the A operand of (5): queries
                 // contiguous, 128-byte swizzled rows (16-byte chunk x of key
                 // row r at x ^ (r % 8)), 64 queries per 16 KiB block.
@@ -344,8 +354,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // loads; only the stores depend on the key row.
         if (ok) {
             const long long rowo = (static_cast<long long>(bh) * p.Tk + key) * HD;
-#pragma unroll 1
-            for (int which = 0; which < 2; ++which) {
+            {
+                const int which = half;  // the first half writes dK, the second dV
                 uint32_t a[32], a2[32];
                 if (n_j > 0) {
                     tc_fence_after_sync();
@@ -358,7 +368,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) a[e] = a2[e] = 0u;
                 }
-                if (key >= p.Tk) continue;
+                if (key < p.Tk) {
                 const float f = which ? 1.f : p.scale;
                 __nv_bfloat16 *dst = (which ? p.dv : p.dk) + rowo;
                 uint32_t w[32];
@@ -370,6 +380,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                 for (int x = 0; x < 8; ++x)
                     reinterpret_cast<uint4 *>(dst)[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
+                }
             }
         }
         if (!ok) tmem_st_wait();
