@@ -73,19 +73,59 @@ __global__ void attn_bwd_pre(const __nv_bfloat16 *__restrict__ o, const __nv_bfl
     }
 }
 
+// The dQ accumulator of a query block j of head bh is 128 rows x 64 fp32 at
+// (bh Tq_pad + 128 j) 64, stored as four 8 KiB quarters (rows 32w .. 32w+31),
+// each ordered [16-byte chunk x of the row][row within the quarter][4 floats]:
+// the order in which a dQ warp stages its rows without shared-memory bank
+// conflicts, so that one untiled bulk reduction adds the whole quarter.
+__device__ __forceinline__ long long dq_acc_index(long long bh, int Tq_pad, int i, int chunk) {
+    return (bh * Tq_pad + (i & ~31)) * HD + chunk * 128 + (i & 31) * 4;
+}
+
+// One thread per 8 features of a row; a warp takes 32 consecutive rows of one
+// feature group (coalesced accumulator reads).
 __global__ void attn_bwd_post(const float *__restrict__ dq_acc, __nv_bfloat16 *__restrict__ dq,
                               long long BH, int Tq, int Tq_pad, float scale) {
     const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const long long row = t >> 3;  // over BH * Tq
-    const int part = static_cast<int>(t & 7);
-    if (row >= BH * Tq) return;
-    const long long bh = row / Tq;
-    const int i = static_cast<int>(row - bh * Tq);
-    const float4 *src = reinterpret_cast<const float4 *>(dq_acc + (bh * Tq_pad + i) * HD + part * 8);
-    const float4 a = src[0], b = src[1];
+    const long long grp = t >> 8;  // 32-row group over BH * Tq_pad / 32
+    const int part = static_cast<int>((t >> 5) & 7);
+    const int groups = Tq_pad >> 5;
+    if (grp >= BH * groups) return;
+    const long long bh = grp / groups;
+    const int i = static_cast<int>(grp - bh * groups) * 32 + static_cast<int>(t & 31);
+    if (i >= Tq) return;
+    const float4 a = *reinterpret_cast<const float4 *>(dq_acc + dq_acc_index(bh, Tq_pad, i, 2 * part));
+    const float4 b = *reinterpret_cast<const float4 *>(dq_acc + dq_acc_index(bh, Tq_pad, i, 2 * part + 1));
     const uint4 w = make_uint4(pack_bf16x2(a.x * scale, a.y * scale), pack_bf16x2(a.z * scale, a.w * scale),
                                pack_bf16x2(b.x * scale, b.y * scale), pack_bf16x2(b.z * scale, b.w * scale));
-    *reinterpret_cast<uint4 *>(dq + row * HD + part * 8) = w;
+    *reinterpret_cast<uint4 *>(dq + (bh * Tq + i) * HD + part * 8) = w;
+}
+
+// P^T and dS^T of one thread's 32 query columns for its key: p = 2^(s c - lse2),
+// ds = p (dp - D), as bf16 pairs.  kMasked: column e counts iff e >= lim.
+template <bool kMasked>
+__device__ __forceinline__ void softmax_terms(const uint32_t (&sv)[32], const uint32_t (&dp)[32],
+                                              const float *lse2, const float *dvec, float C, int lim,
+                                              uint32_t (&pk)[16], uint32_t (&dsk)[16]) {
+#pragma unroll
+    for (int g = 0; g < 8; ++g) {
+        const float4 l4 = reinterpret_cast<const float4 *>(lse2)[g];
+        const float4 d4 = reinterpret_cast<const float4 *>(dvec)[g];
+        const float l[4] = {l4.x, l4.y, l4.z, l4.w}, d[4] = {d4.x, d4.y, d4.z, d4.w};
+        float pp[4], dd[4];
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
+            const int e = 4 * g + h;
+            float pv = ex2_approx(__uint_as_float(sv[e]) * C - l[h]);
+            if (kMasked && e < lim) pv = 0.f;
+            pp[h] = pv;
+            dd[h] = pv * (__uint_as_float(dp[e]) - d[h]);
+        }
+        pk[2 * g] = pack_bf16x2(pp[0], pp[1]);
+        pk[2 * g + 1] = pack_bf16x2(pp[2], pp[3]);
+        dsk[2 * g] = pack_bf16x2(dd[0], dd[1]);
+        dsk[2 * g + 1] = pack_bf16x2(dd[2], dd[3]);
+    }
 }
 
 // ------------------------------------------------------------------- main
@@ -106,17 +146,22 @@ __global__ void attn_bwd_post(const float *__restrict__ dq_acc, __nv_bfloat16 *_
 //                                        shared memory (queries contiguous)
 //               Computing S and dP transposed puts the keys on the
 //               tensor-memory lanes, so P^T and dS^T feed (3) and (4) straight
-//               from tensor memory.
+//               from tensor memory.  Issue order: (3)(4) of block j, (1)(2)
+//               of block j+1, then (5) of block j -- the tensor pipe runs in
+//               issue order, so (5) does not delay the next block's scores.
 //   warps 2-9   one thread per (key, half of the query block) -- warps w and
 //               w+4 share the keys of lane quadrant w%4 and take queries
 //               [0,64) and [64,128): P^T = 2^(S^T c - lse_j) (masked: 0),
 //               dS^T = P^T (dP^T - D_j), elementwise (lse and D are per-query
 //               inputs, no row reduction); P^T and dS^T written as bf16, dS^T
-//               also into shared memory for (5).  At the end the first half
-//               writes dK (times scale), the second dV.
-//   warps 10-13 one thread per query row: dQ_j partial out of tensor memory,
-//               added to the fp32 accumulator in global memory (other key
-//               blocks add theirs).
+//               also into shared memory for (5) (two buffers: block j+2
+//               reuses block j's, whose (5) the commit of block j+1's scores
+//               already covers).  At the end the first half writes dK (times
+//               scale), the second dV.
+//   warps 10-13 one thread per query row: the dQ_j partial out of tensor
+//               memory, staged in shared memory and added to the fp32
+//               accumulator in global memory by one bulk reduction per warp
+//               (other key blocks add theirs).
 //
 // Tensor memory: S^T [0,128), dP^T [128,256), dV [256,320), dK [320,384),
 // dQ_j [384,448).  P^T and dS^T of queries [0,64) go over S^T [0,32) and
@@ -132,8 +177,9 @@ struct __align__(1024) SmemBwd {
     uint8_t k[kTile];
     uint8_t v[kTile];
     uint8_t q[2][kTile];
-    uint8_t g[2][kTile];   // dO
-    uint8_t ds[2 * kTile]; // dS as the A operand of (5): 2 blocks of 64 queries x 128 key rows
+    uint8_t g[2][kTile];      // dO
+    uint8_t ds[2][2 * kTile]; // dS as the A operand of (5): 2 blocks of 64 queries x 128 key rows
+    float4 dq_stage[4][16 * 32];  // per dQ warp: [16-byte chunk][row of the warp]
     float lse2[2][BQ];
     float dvec[2][BQ];
     uint64_t kv_full;
@@ -142,7 +188,6 @@ struct __align__(1024) SmemBwd {
     uint64_t sdp_full;   // (1), (2) complete
     uint64_t pds_full;   // P^T, dS^T written (8 warps)
     uint64_t tmem_free;  // (3), (4) complete: S^T / dP^T columns reusable
-    uint64_t ds_free;    // (5) complete: the shared dS tile reusable
     uint64_t dq_full;    // (5) complete
     uint64_t dq_free;    // dQ_j read (4 warps)
     uint64_t acc_done;   // every product complete
@@ -182,7 +227,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(&sm.sdp_full, 1);
         mbar_init(&sm.pds_full, 8);
         mbar_init(&sm.tmem_free, 1);
-        mbar_init(&sm.ds_free, 1);
         mbar_init(&sm.dq_full, 1);
         mbar_init(&sm.dq_free, 4);
         mbar_init(&sm.acc_done, 1);
@@ -246,14 +290,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const uint64_t g_mn = smem_desc_sw128(smem_u32(sm.g[0]), 1024, 1024);
             const uint64_t k_mn = smem_desc_sw128(smem_u32(sm.k), 1024, 1024);
             // dS: two 64-query blocks 16 KiB apart (leading byte offset)
-            const uint64_t ds_mn = smem_desc_sw128(smem_u32(sm.ds), kTile, 1024);
-            bool ok = warp_wait(&sm.kv_full, 0, ab);
-            for (int t = 0; ok && t < n_j; ++t) {
-                const int st = t & 1;
-                const uint64_t so = static_cast<uint64_t>(st) * kT;  // q[st], g[st] stage offset
-                if (!(ok = warp_wait(&sm.stage_full[st], (t >> 1) & 1, ab))) break;
-                if (t >= 1 && !(ok = warp_wait(&sm.tmem_free, (t - 1) & 1, ab))) break;
-                tc_fence_after_sync();
+            const uint64_t ds_mn = smem_desc_sw128(smem_u32(sm.ds[0]), kTile, 1024);
+            // (1), (2) of the block in stage s
+            auto scores = [&](int s) {
+                const uint64_t so = static_cast<uint64_t>(s) * kT;
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk)
                     warp_mma_bf16_ss(tmem + kColS, k_km + 2 * kk, q_km + so + 2 * kk, id_s, kk > 0 ? 1u : 0u);
@@ -261,6 +301,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 for (int kk = 0; kk < HD / 16; ++kk)
                     warp_mma_bf16_ss(tmem + kColDP, v_km + 2 * kk, g_km + so + 2 * kk, id_s, kk > 0 ? 1u : 0u);
                 warp_commit(&sm.sdp_full);
+            };
+            bool ok = warp_wait(&sm.kv_full, 0, ab) && warp_wait(&sm.stage_full[0], 0, ab);
+            if (ok) {
+                tc_fence_after_sync();
+                scores(0);
+            }
+            for (int t = 0; ok && t < n_j; ++t) {
+                const int st = t & 1;
+                const uint64_t so = static_cast<uint64_t>(st) * kT;  // q[st], g[st] stage offset
                 if (!(ok = warp_wait(&sm.pds_full, t & 1, ab))) break;
                 tc_fence_after_sync();
 #pragma unroll
@@ -271,15 +320,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 for (int kk = 0; kk < BQ / 16; ++kk)
                     warp_mma_bf16_ts(tmem + kColDK, tmem + (kk < 4 ? kColDP + 8 * kk : kColDS2 + 8 * (kk - 4)),
                                      q_mn + so + 128 * kk, id_kv, (t > 0 || kk > 0) ? 1u : 0u);
-                warp_commit(&sm.tmem_free);
+                warp_commit(&sm.stage_empty[st]);  // (1)-(4) were the stage's last readers
+                if (t + 1 < n_j) {
+                    // the next block's scores overwrite the columns (3), (4) read
+                    warp_commit(&sm.tmem_free);
+                    if (!(ok = warp_wait(&sm.stage_full[st ^ 1], ((t + 1) >> 1) & 1, ab))) break;
+                    if (!(ok = warp_wait(&sm.tmem_free, t & 1, ab))) break;
+                    tc_fence_after_sync();
+                    scores(st ^ 1);
+                }
                 if (t >= 1 && !(ok = warp_wait(&sm.dq_free, (t - 1) & 1, ab))) break;
                 tc_fence_after_sync();
+                const uint64_t dso = static_cast<uint64_t>(st) * (2 * kT);
 #pragma unroll
                 for (int kk = 0; kk < BKB / 16; ++kk)
-                    warp_mma_bf16_ss(tmem + kColDQ, ds_mn + 128 * kk, k_mn + 128 * kk, id_q, kk > 0 ? 1u : 0u);
+                    warp_mma_bf16_ss(tmem + kColDQ, ds_mn + dso + 128 * kk, k_mn + 128 * kk, id_q,
+                                     kk > 0 ? 1u : 0u);
                 warp_commit(&sm.dq_full);
-                warp_commit(&sm.ds_free);
-                warp_commit(&sm.stage_empty[st]);
             }
             if (ok) warp_commit(&sm.acc_done);
         }
@@ -301,7 +358,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const int q0 = (j_begin + t) * BQ;
             ok = __all_sync(0xffffffffu, mbar_wait(&sm.sdp_full, t & 1, ab)) &&
                  __all_sync(0xffffffffu, mbar_wait(&sm.stage_full[st], (t >> 1) & 1, ab));
-            if (ok && t >= 1) ok = __all_sync(0xffffffffu, mbar_wait(&sm.ds_free, (t - 1) & 1, ab));
             if (!ok) break;
             tc_fence_after_sync();
 #pragma unroll 1
@@ -309,23 +365,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 uint32_t sv[32], dp[32];
                 tmem_ld32(tl + kColS + 32u * c, sv);
                 tmem_ld32(tl + kColDP + 32u * c, dp);
+                // query column e of the chunk sees the key iff e >= lim
+                const int lim = key_ok ? (causal ? key - (q0 + 32 * c) : 0) : 32;
                 tmem_ld_wait(sv);
                 reg_fence32(dp);
                 uint32_t pk[16], dsk[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    float pp[2], dd[2];
-#pragma unroll
-                    for (int h2 = 0; h2 < 2; ++h2) {
-                        const int qi = 32 * c + 2 * e + h2;  // query column in the block
-                        const bool vis = key_ok && (!causal || key <= q0 + qi);
-                        const float pv = vis ? ex2_approx(__uint_as_float(sv[2 * e + h2]) * C - sm.lse2[st][qi]) : 0.f;
-                        pp[h2] = pv;
-                        dd[h2] = pv * (__uint_as_float(dp[2 * e + h2]) - sm.dvec[st][qi]);
-                    }
-                    pk[e] = pack_bf16x2(pp[0], pp[1]);
-                    dsk[e] = pack_bf16x2(dd[0], dd[1]);
-                }
+                if (__all_sync(0xffffffffu, lim <= 0))
+                    softmax_terms<false>(sv, dp, sm.lse2[st] + 32 * c, sm.dvec[st] + 32 * c, C, 0, pk, dsk);
+                else
+                    softmax_terms<true>(sv, dp, sm.lse2[st] + 32 * c, sm.dvec[st] + 32 * c, C, lim, pk, dsk);
                 // P^T and dS^T: the first half writes over S^T / dP^T columns
                 // [16c, 16c+16) it has already read (chunks <= c); the second
                 // half into its own columns.
@@ -334,7 +382,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 // dS into shared memory as the A operand of (5): queries
                 // contiguous, 128-byte swizzled rows (16-byte chunk x of key
                 // row r at x ^ (r % 8)), 64 queries per 16 KiB block.
-                uint8_t *blk = sm.ds + (c >> 1) * kTile + r * 128;
+                uint8_t *blk = sm.ds[st] + (c >> 1) * kTile + r * 128;
 #pragma unroll
                 for (int x = 0; x < 4; ++x) {
                     const int chunk = 4 * (c & 1) + x;
@@ -386,9 +434,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         if (!ok) tmem_st_wait();
     } else {
         // ------------------------------------------------- dQ accumulation
-        const uint32_t lane_base = static_cast<uint32_t>(warp & 3) * 32;
-        const int r = static_cast<int>(lane_base) + lane;  // query row in the block
+        const int wq = warp & 3;
+        const uint32_t lane_base = static_cast<uint32_t>(wq) * 32;
         const uint32_t tl = tmem_addr(tmem, lane_base, 0);
+        float4 *stage = sm.dq_stage[wq];
         for (int t = 0; t < n_j; ++t) {
             if (!__all_sync(0xffffffffu, mbar_wait(&sm.dq_full, t & 1, ab))) break;
             tc_fence_after_sync();
@@ -399,19 +448,33 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             reg_fence32(a2);
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&sm.dq_free);
-            // rows past Tq carry zeros (their weights are 0) and stay inside
-            // the padded accumulator
-            float *dst = p.dq_acc + (static_cast<long long>(bh) * p.Tq_pad + (j_begin + t) * BQ + r) * HD;
+            if (lane == 0) {
+                mbar_arrive(&sm.dq_free);
+                bulk_wait_read();  // the previous block's reduction has read the stage
+            }
+            __syncwarp();
+            // [chunk][row]: a warp's stores cover 512 contiguous bytes
 #pragma unroll
             for (int x = 0; x < 8; ++x)
-                red_add_v4(dst + 4 * x, __uint_as_float(a[4 * x]), __uint_as_float(a[4 * x + 1]),
-                           __uint_as_float(a[4 * x + 2]), __uint_as_float(a[4 * x + 3]));
+                stage[x * 32 + lane] = make_float4(__uint_as_float(a[4 * x]), __uint_as_float(a[4 * x + 1]),
+                                                   __uint_as_float(a[4 * x + 2]), __uint_as_float(a[4 * x + 3]));
 #pragma unroll
             for (int x = 0; x < 8; ++x)
-                red_add_v4(dst + 32 + 4 * x, __uint_as_float(a2[4 * x]), __uint_as_float(a2[4 * x + 1]),
-                           __uint_as_float(a2[4 * x + 2]), __uint_as_float(a2[4 * x + 3]));
+                stage[(8 + x) * 32 + lane] =
+                    make_float4(__uint_as_float(a2[4 * x]), __uint_as_float(a2[4 * x + 1]),
+                                __uint_as_float(a2[4 * x + 2]), __uint_as_float(a2[4 * x + 3]));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                // rows past Tq carry zeros (their weights are 0) and stay
+                // inside the padded accumulator
+                float *dst = p.dq_acc +
+                             (static_cast<long long>(bh) * p.Tq_pad + (j_begin + t) * BQ + lane_base) * HD;
+                bulk_reduce_add_f32(dst, stage, 32 * HD * 4);
+                bulk_commit_group();
+            }
         }
+        if (lane == 0) bulk_wait_all();
     }
 
     tc_fence_before_sync();
@@ -460,7 +523,7 @@ cudaError_t launch_attn_bwd_bf16(const CUtensorMap &tq, const CUtensorMap &tk, c
         attn_bwd_main<<<grid, kBwdThreads, smem, stream>>>(tq, tk, tv, tg, p);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
-    const long long post_threads = BH * p.Tq * 8;
+    const long long post_threads = p.Tq > 0 ? BH * p.Tq_pad * 8 : 0;
     if (post_threads == 0) return cudaSuccess;
     attn_bwd_post<<<static_cast<unsigned>((post_threads + 255) / 256), 256, 0, stream>>>(
         p.dq_acc, dq, BH, p.Tq, p.Tq_pad, p.scale);
