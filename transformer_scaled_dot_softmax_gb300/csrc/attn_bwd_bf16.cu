@@ -101,14 +101,15 @@ __global__ void attn_bwd_post(const float *__restrict__ dq_acc, __nv_bfloat16 *_
     *reinterpret_cast<uint4 *>(dq + (bh * Tq + i) * HD + part * 8) = w;
 }
 
-// P^T and dS^T of one thread's 32 query columns for its key: p = 2^(s c - lse2),
-// ds = p (dp - D), as bf16 pairs.  kMasked: column e counts iff e >= lim.
-template <bool kMasked>
-__device__ __forceinline__ void softmax_terms(const uint32_t (&sv)[32], const uint32_t (&dp)[32],
+// P^T and dS^T of N of one thread's query columns for its key:
+// p = 2^(s c - lse2), ds = p (dp - D), as bf16 pairs.  kMasked: column e
+// counts iff e >= lim.
+template <int N, bool kMasked>
+__device__ __forceinline__ void softmax_terms(const uint32_t (&sv)[N], const uint32_t (&dp)[N],
                                               const float *lse2, const float *dvec, float C, int lim,
-                                              uint32_t (&pk)[16], uint32_t (&dsk)[16]) {
+                                              uint32_t (&pk)[N / 2], uint32_t (&dsk)[N / 2]) {
 #pragma unroll
-    for (int g = 0; g < 8; ++g) {
+    for (int g = 0; g < N / 4; ++g) {
         const float4 l4 = reinterpret_cast<const float4 *>(lse2)[g];
         const float4 d4 = reinterpret_cast<const float4 *>(dvec)[g];
         const float l[4] = {l4.x, l4.y, l4.z, l4.w}, d[4] = {d4.x, d4.y, d4.z, d4.w};
@@ -131,7 +132,7 @@ __device__ __forceinline__ void softmax_terms(const uint32_t (&sv)[32], const ui
 // ------------------------------------------------------------------- main
 // One CTA = one (b, h) and a block of 128 keys; it walks the query blocks j
 // that see any of its keys (all of them, or j >= kb under the causal mask).
-// Warp roles (14 warps):
+// Warp roles (18 warps):
 //
 //   warp 0      TMA: the K and V blocks once; per query block Q_j, dO_j (3-D
 //               tensor maps) and its 128 lse and D values (bulk copies) into
@@ -146,32 +147,33 @@ __device__ __forceinline__ void softmax_terms(const uint32_t (&sv)[32], const ui
 //                                        shared memory (queries contiguous)
 //               Computing S and dP transposed puts the keys on the
 //               tensor-memory lanes, so P^T and dS^T feed (3) and (4) straight
-//               from tensor memory.  Issue order: (3)(4) of block j, (1)(2)
-//               of block j+1, then (5) of block j -- the tensor pipe runs in
-//               issue order, so (5) does not delay the next block's scores.
-//   warps 2-9   one thread per (key, half of the query block) -- warps w and
-//               w+4 share the keys of lane quadrant w%4 and take queries
-//               [0,64) and [64,128): P^T = 2^(S^T c - lse_j) (masked: 0),
-//               dS^T = P^T (dP^T - D_j), elementwise (lse and D are per-query
-//               inputs, no row reduction); P^T and dS^T written as bf16, dS^T
-//               also into shared memory for (5) (two buffers: block j+2
-//               reuses block j's, whose (5) the commit of block j+1's scores
-//               already covers).  At the end the first half writes dK (times
-//               scale), the second dV.
-//   warps 10-13 one thread per query row: the dQ_j partial out of tensor
-//               memory, staged in shared memory and added to the fp32
-//               accumulator in global memory by one bulk reduction per warp
-//               (other key blocks add theirs).
+//               from tensor memory.  Issue order: (4) (3) of block j, (1) of
+//               block j+1, (2) of block j+1 once (4) has read dS^T, then (5)
+//               of block j -- the tensor pipe runs in issue order, so (5)
+//               does not delay the next block's scores.
+//   warps 2-17  one thread per (key, chunk of 32 queries) -- warp w takes the
+//               keys of lane quadrant w%4 and chunk (w-2)/4:
+//               P^T = 2^(S^T c - lse_j) (masked: 0), dS^T = P^T (dP^T - D_j),
+//               elementwise (lse and D are per-query inputs, no row
+//               reduction); P^T and dS^T written as bf16, dS^T also into
+//               shared memory for (5) (two buffers: block j+2 reuses block
+//               j's, whose (5) the commit of block j+1's scores already
+//               covers).  After block j's terms, the same warps move the
+//               dQ_{j-1} partial out of tensor memory (warp w: the rows of
+//               quadrant w%4, features [16c, 16c+16)), stage it in shared
+//               memory and add it to the fp32 accumulator in global memory
+//               by one bulk reduction per warp (other key blocks add theirs).
+//               At the end chunks 0, 1 write dK (times scale) and chunks 2, 3
+//               dV, 32 features each.
 //
-// Tensor memory: S^T [0,128), dP^T [128,256), dV [256,320), dK [320,384),
-// dQ_j [384,448).  P^T and dS^T of queries [0,64) go over S^T [0,32) and
-// dP^T [128,160) -- columns only the warp of that half has read -- and those of
-// queries [64,128) into [448,480) and [480,512): a warp never writes columns
-// the other half still reads.
+// Tensor memory: S^T [0,128), dP^T [128,256), P^T [256,320), dV [320,384),
+// dK [384,448), dQ_j [448,512).  dS^T of chunk c goes over dP^T columns
+// [128+32c, 128+32c+16), which only chunk c's warp reads; P^T has columns of
+// its own so that (1) of the next block need not wait for (3).
 constexpr uint32_t kTile = BQ * HD * 2;  // 16 KiB
-constexpr uint32_t kColS = 0, kColDP = 128, kColDV = 256, kColDK = 320, kColDQ = 384;
-constexpr uint32_t kColP2 = 448, kColDS2 = 480;  // P^T, dS^T of queries [64,128)
-constexpr int kBwdThreads = 448;
+constexpr uint32_t kColS = 0, kColDP = 128, kColP = 256, kColDV = 320, kColDK = 384, kColDQ = 448;
+constexpr int kBwdThreads = 576;
+constexpr int kSoftmaxWarps = 16;
 
 struct __align__(1024) SmemBwd {
     uint8_t k[kTile];
@@ -179,17 +181,17 @@ struct __align__(1024) SmemBwd {
     uint8_t q[2][kTile];
     uint8_t g[2][kTile];      // dO
     uint8_t ds[2][2 * kTile]; // dS as the A operand of (5): 2 blocks of 64 queries x 128 key rows
-    float4 dq_stage[4][16 * 32];  // per dQ warp: [16-byte chunk][row of the warp]
+    float4 dq_stage[4][16 * 32];  // per lane quadrant: [16-byte chunk][row of the quadrant]
     float lse2[2][BQ];
     float dvec[2][BQ];
     uint64_t kv_full;
     uint64_t stage_full[2];
     uint64_t stage_empty[2];
     uint64_t sdp_full;   // (1), (2) complete
-    uint64_t pds_full;   // P^T, dS^T written (8 warps)
-    uint64_t tmem_free;  // (3), (4) complete: S^T / dP^T columns reusable
+    uint64_t pds_full;   // P^T, dS^T written (16 warps)
+    uint64_t tmem_free;  // (4) complete: the dP^T columns reusable
     uint64_t dq_full;    // (5) complete
-    uint64_t dq_free;    // dQ_j read (4 warps)
+    uint64_t dq_free;    // dQ_j read (16 warps)
     uint64_t acc_done;   // every product complete
     uint64_t drain;
     uint32_t tmem_base;
@@ -225,10 +227,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             mbar_init(&sm.stage_empty[i], 1);
         }
         mbar_init(&sm.sdp_full, 1);
-        mbar_init(&sm.pds_full, 8);
+        mbar_init(&sm.pds_full, kSoftmaxWarps);
         mbar_init(&sm.tmem_free, 1);
         mbar_init(&sm.dq_full, 1);
-        mbar_init(&sm.dq_free, 4);
+        mbar_init(&sm.dq_free, kSoftmaxWarps);
         mbar_init(&sm.acc_done, 1);
         mbar_init(&sm.drain, 1);
         sm.abort_flag = 0;
@@ -291,43 +293,51 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             const uint64_t k_mn = smem_desc_sw128(smem_u32(sm.k), 1024, 1024);
             // dS: two 64-query blocks 16 KiB apart (leading byte offset)
             const uint64_t ds_mn = smem_desc_sw128(smem_u32(sm.ds[0]), kTile, 1024);
-            // (1), (2) of the block in stage s
-            auto scores = [&](int s) {
+            // (1) and (2) of the block in stage s
+            auto score_s = [&](int s) {
                 const uint64_t so = static_cast<uint64_t>(s) * kT;
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk)
                     warp_mma_bf16_ss(tmem + kColS, k_km + 2 * kk, q_km + so + 2 * kk, id_s, kk > 0 ? 1u : 0u);
+            };
+            auto score_dp = [&](int s) {
+                const uint64_t so = static_cast<uint64_t>(s) * kT;
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk)
                     warp_mma_bf16_ss(tmem + kColDP, v_km + 2 * kk, g_km + so + 2 * kk, id_s, kk > 0 ? 1u : 0u);
-                warp_commit(&sm.sdp_full);
             };
             bool ok = warp_wait(&sm.kv_full, 0, ab) && warp_wait(&sm.stage_full[0], 0, ab);
             if (ok) {
                 tc_fence_after_sync();
-                scores(0);
+                score_s(0);
+                score_dp(0);
+                warp_commit(&sm.sdp_full);
             }
             for (int t = 0; ok && t < n_j; ++t) {
                 const int st = t & 1;
                 const uint64_t so = static_cast<uint64_t>(st) * kT;  // q[st], g[st] stage offset
                 if (!(ok = warp_wait(&sm.pds_full, t & 1, ab))) break;
                 tc_fence_after_sync();
+                // (4): the 16 queries of K step kk are chunk kk/2, half kk%2
 #pragma unroll
                 for (int kk = 0; kk < BQ / 16; ++kk)
-                    warp_mma_bf16_ts(tmem + kColDV, tmem + (kk < 4 ? kColS + 8 * kk : kColP2 + 8 * (kk - 4)),
-                                     g_mn + so + 128 * kk, id_kv, (t > 0 || kk > 0) ? 1u : 0u);
-#pragma unroll
-                for (int kk = 0; kk < BQ / 16; ++kk)
-                    warp_mma_bf16_ts(tmem + kColDK, tmem + (kk < 4 ? kColDP + 8 * kk : kColDS2 + 8 * (kk - 4)),
+                    warp_mma_bf16_ts(tmem + kColDK, tmem + kColDP + 32 * (kk >> 1) + 8 * (kk & 1),
                                      q_mn + so + 128 * kk, id_kv, (t > 0 || kk > 0) ? 1u : 0u);
+                warp_commit(&sm.tmem_free);
+#pragma unroll
+                for (int kk = 0; kk < BQ / 16; ++kk)
+                    warp_mma_bf16_ts(tmem + kColDV, tmem + kColP + 8 * kk, g_mn + so + 128 * kk, id_kv,
+                                     (t > 0 || kk > 0) ? 1u : 0u);
                 warp_commit(&sm.stage_empty[st]);  // (1)-(4) were the stage's last readers
                 if (t + 1 < n_j) {
-                    // the next block's scores overwrite the columns (3), (4) read
-                    warp_commit(&sm.tmem_free);
                     if (!(ok = warp_wait(&sm.stage_full[st ^ 1], ((t + 1) >> 1) & 1, ab))) break;
+                    tc_fence_after_sync();
+                    score_s(st ^ 1);
+                    // dP^T of the next block overwrites the dS^T that (4) reads
                     if (!(ok = warp_wait(&sm.tmem_free, t & 1, ab))) break;
                     tc_fence_after_sync();
-                    scores(st ^ 1);
+                    score_dp(st ^ 1);
+                    warp_commit(&sm.sdp_full);
                 }
                 if (t >= 1 && !(ok = warp_wait(&sm.dq_free, (t - 1) & 1, ab))) break;
                 tc_fence_after_sync();
@@ -342,50 +352,81 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         warp_commit(&sm.drain);
         mbar_wait_drain(&sm.drain, 0);
-    } else if (warp < 10) {
+    } else if (warp < 2 + kSoftmaxWarps) {
         // ------------------------------------------- per-key softmax terms
-        const int half = (warp - 2) >> 2;  // queries [64 half, 64 half + 64)
-        const uint32_t p_col = half ? kColP2 : kColS, ds_col = half ? kColDS2 : kColDP;
+        const int c = (warp - 2) >> 2;  // query chunk [32c, 32c + 32)
         const uint32_t lane_base = static_cast<uint32_t>(warp & 3) * 32;
         const int r = static_cast<int>(lane_base) + lane;  // key row in the block
         const int key = k0 + r;
         const bool key_ok = key < key_hi;
         const uint32_t tl = tmem_addr(tmem, lane_base, 0);
         const float C = p.scale_log2;
+        // dQ_u of this warp's rows and features [16c, 16c+16): chunks
+        // [4c, 4c+4) of the quadrant's accumulator quarter.
+        float4 *stage = sm.dq_stage[warp & 3] + 4 * c * 32;
+        auto add_dq = [&](int u) -> bool {
+            if (!__all_sync(0xffffffffu, mbar_wait(&sm.dq_full, u & 1, ab))) return false;
+            if (lane == 0) bulk_wait_read();  // the previous reduction has read the stage
+            __syncwarp();
+            tc_fence_after_sync();
+            uint32_t a[16];
+            tmem_ld16(tl + kColDQ + 16u * c, a);
+            tmem_ld_wait(a);
+#pragma unroll
+            for (int x = 0; x < 4; ++x)
+                stage[x * 32 + lane] = make_float4(__uint_as_float(a[4 * x]), __uint_as_float(a[4 * x + 1]),
+                                                   __uint_as_float(a[4 * x + 2]), __uint_as_float(a[4 * x + 3]));
+            tc_fence_before_sync();
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&sm.dq_free);
+                // rows past Tq carry zeros (their weights are 0) and stay
+                // inside the padded accumulator
+                float *dst = p.dq_acc +
+                             (static_cast<long long>(bh) * p.Tq_pad + (j_begin + u) * BQ + lane_base) * HD +
+                             512 * c;
+                bulk_reduce_add_f32(dst, stage, 4 * 32 * 16);
+                bulk_commit_group();
+            }
+            return true;
+        };
         bool ok = true;
         for (int t = 0; t < n_j; ++t) {
             const int st = t & 1;
-            const int q0 = (j_begin + t) * BQ;
+            const int q0 = (j_begin + t) * BQ + 32 * c;
             ok = __all_sync(0xffffffffu, mbar_wait(&sm.sdp_full, t & 1, ab)) &&
                  __all_sync(0xffffffffu, mbar_wait(&sm.stage_full[st], (t >> 1) & 1, ab));
             if (!ok) break;
             tc_fence_after_sync();
+            // two halves of 16 query columns, 32 registers in flight each
+            uint8_t *blk = sm.ds[st] + (c >> 1) * kTile + r * 128;
 #pragma unroll 1
-            for (int c = 2 * half; c < 2 * half + 2; ++c) {
-                uint32_t sv[32], dp[32];
-                tmem_ld32(tl + kColS + 32u * c, sv);
-                tmem_ld32(tl + kColDP + 32u * c, dp);
-                // query column e of the chunk sees the key iff e >= lim
-                const int lim = key_ok ? (causal ? key - (q0 + 32 * c) : 0) : 32;
+            for (int h = 0; h < 2; ++h) {
+                const uint32_t col = 32u * c + 16u * h;
+                uint32_t sv[16], dp[16];
+                tmem_ld16(tl + kColS + col, sv);
+                tmem_ld16(tl + kColDP + col, dp);
+                // query column e of the half sees the key iff e >= lim
+                const int lim = key_ok ? (causal ? key - (q0 + 16 * h) : 0) : 16;
                 tmem_ld_wait(sv);
-                reg_fence32(dp);
-                uint32_t pk[16], dsk[16];
+                tmem_ld_wait(dp);
+                uint32_t pk[8], dsk[8];
+                const float *l2 = sm.lse2[st] + 32 * c + 16 * h, *dv = sm.dvec[st] + 32 * c + 16 * h;
                 if (__all_sync(0xffffffffu, lim <= 0))
-                    softmax_terms<false>(sv, dp, sm.lse2[st] + 32 * c, sm.dvec[st] + 32 * c, C, 0, pk, dsk);
+                    softmax_terms<16, false>(sv, dp, l2, dv, C, 0, pk, dsk);
                 else
-                    softmax_terms<true>(sv, dp, sm.lse2[st] + 32 * c, sm.dvec[st] + 32 * c, C, lim, pk, dsk);
-                // P^T and dS^T: the first half writes over S^T / dP^T columns
-                // [16c, 16c+16) it has already read (chunks <= c); the second
-                // half into its own columns.
-                tmem_st16(tl + p_col + 16u * (c - 2 * half), pk);
-                tmem_st16(tl + ds_col + 16u * (c - 2 * half), dsk);
+                    softmax_terms<16, true>(sv, dp, l2, dv, C, lim, pk, dsk);
+                // P^T into its own columns, dS^T over dP^T columns this warp
+                // has read
+                tmem_st8(tl + kColP + 16u * c + 8u * h, pk);
+                tmem_st8(tl + kColDP + 32u * c + 8u * h, dsk);
                 // dS into shared memory as the A operand of (5): queries
                 // contiguous, 128-byte swizzled rows (16-byte chunk x of key
                 // row r at x ^ (r % 8)), 64 queries per 16 KiB block.
-                uint8_t *blk = sm.ds[st] + (c >> 1) * kTile + r * 128;
 #pragma unroll
-                for (int x = 0; x < 4; ++x) {
-                    const int chunk = 4 * (c & 1) + x;
+                for (int x = 0; x < 2; ++x) {
+                    const int chunk = 4 * (c & 1) + 2 * h + x;
                     *reinterpret_cast<uint4 *>(blk + ((chunk ^ (r & 7)) << 4)) =
                         make_uint4(dsk[4 * x], dsk[4 * x + 1], dsk[4 * x + 2], dsk[4 * x + 3]);
                 }
@@ -395,85 +436,40 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&sm.pds_full);
+            if (t >= 1 && !(ok = add_dq(t - 1))) break;
         }
-        // dK = scale dS^T Q and dV = P^T dO of this block's keys.
+        if (ok && n_j > 0) ok = add_dq(n_j - 1);
+        // dK = scale dS^T Q (chunks 0, 1) and dV = P^T dO (chunks 2, 3) of
+        // this block's keys, 32 features per warp.
         if (ok && n_j > 0) ok = __all_sync(0xffffffffu, mbar_wait(&sm.acc_done, 0, ab));
         // `ok` and n_j are warp-uniform: every lane issues the tensor-memory
-        // loads; only the stores depend on the key row.
+        // load; only the stores depend on the key row.
         if (ok) {
-            const long long rowo = (static_cast<long long>(bh) * p.Tk + key) * HD;
-            {
-                const int which = half;  // the first half writes dK, the second dV
-                uint32_t a[32], a2[32];
-                if (n_j > 0) {
-                    tc_fence_after_sync();
-                    __syncwarp();
-                    tmem_ld32(tl + (which ? kColDV : kColDK), a);
-                    tmem_ld32(tl + (which ? kColDV : kColDK) + 32, a2);
-                    tmem_ld_wait(a);
-                    reg_fence32(a2);
-                } else {
+            const bool is_dv = c >= 2;
+            const int f0 = 32 * (c & 1);  // first feature
+            uint32_t a[32];
+            if (n_j > 0) {
+                tc_fence_after_sync();
+                __syncwarp();
+                tmem_ld32(tl + (is_dv ? kColDV : kColDK) + f0, a);
+                tmem_ld_wait(a);
+            } else {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) a[e] = a2[e] = 0u;
-                }
-                if (key < p.Tk) {
-                const float f = which ? 1.f : p.scale;
-                __nv_bfloat16 *dst = (which ? p.dv : p.dk) + rowo;
-                uint32_t w[32];
+                for (int e = 0; e < 32; ++e) a[e] = 0u;
+            }
+            if (key < p.Tk) {
+                const float f = is_dv ? 1.f : p.scale;
+                __nv_bfloat16 *dst = (is_dv ? p.dv : p.dk) + (static_cast<long long>(bh) * p.Tk + key) * HD + f0;
+                uint32_t w[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
+                for (int e = 0; e < 16; ++e)
                     w[e] = pack_bf16x2(__uint_as_float(a[2 * e]) * f, __uint_as_float(a[2 * e + 1]) * f);
-                    w[16 + e] = pack_bf16x2(__uint_as_float(a2[2 * e]) * f, __uint_as_float(a2[2 * e + 1]) * f);
-                }
 #pragma unroll
-                for (int x = 0; x < 8; ++x)
+                for (int x = 0; x < 4; ++x)
                     reinterpret_cast<uint4 *>(dst)[x] = make_uint4(w[4 * x], w[4 * x + 1], w[4 * x + 2], w[4 * x + 3]);
-                }
             }
         }
         if (!ok) tmem_st_wait();
-    } else {
-        // ------------------------------------------------- dQ accumulation
-        const int wq = warp & 3;
-        const uint32_t lane_base = static_cast<uint32_t>(wq) * 32;
-        const uint32_t tl = tmem_addr(tmem, lane_base, 0);
-        float4 *stage = sm.dq_stage[wq];
-        for (int t = 0; t < n_j; ++t) {
-            if (!__all_sync(0xffffffffu, mbar_wait(&sm.dq_full, t & 1, ab))) break;
-            tc_fence_after_sync();
-            uint32_t a[32], a2[32];
-            tmem_ld32(tl + kColDQ, a);
-            tmem_ld32(tl + kColDQ + 32, a2);
-            tmem_ld_wait(a);
-            reg_fence32(a2);
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&sm.dq_free);
-                bulk_wait_read();  // the previous block's reduction has read the stage
-            }
-            __syncwarp();
-            // [chunk][row]: a warp's stores cover 512 contiguous bytes
-#pragma unroll
-            for (int x = 0; x < 8; ++x)
-                stage[x * 32 + lane] = make_float4(__uint_as_float(a[4 * x]), __uint_as_float(a[4 * x + 1]),
-                                                   __uint_as_float(a[4 * x + 2]), __uint_as_float(a[4 * x + 3]));
-#pragma unroll
-            for (int x = 0; x < 8; ++x)
-                stage[(8 + x) * 32 + lane] =
-                    make_float4(__uint_as_float(a2[4 * x]), __uint_as_float(a2[4 * x + 1]),
-                                __uint_as_float(a2[4 * x + 2]), __uint_as_float(a2[4 * x + 3]));
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                // rows past Tq carry zeros (their weights are 0) and stay
-                // inside the padded accumulator
-                float *dst = p.dq_acc +
-                             (static_cast<long long>(bh) * p.Tq_pad + (j_begin + t) * BQ + lane_base) * HD;
-                bulk_reduce_add_f32(dst, stage, 32 * HD * 4);
-                bulk_commit_group();
-            }
-        }
         if (lane == 0) bulk_wait_all();
     }
 
