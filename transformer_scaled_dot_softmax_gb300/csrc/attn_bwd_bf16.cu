@@ -9,7 +9,7 @@
 // per-row log-sum-exp: P_ij = exp(S_ij - lse_i).
 //
 // Three launches:
-//   attn_bwd_pre   D_i, lse_i in log2 units (+inf for a padded or fully masked
+//   attn_bwd_pre   D_i, -lse_i in log2 units (-inf for a padded or fully masked
 //                  row, so its weights are 0), and a zeroed fp32 dQ accumulator;
 //   attn_bwd_main  one CTA per (b, h, block of 128 keys): keeps dK and dV of
 //                  its keys in tensor memory and walks the query blocks that
@@ -32,7 +32,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 // One thread per 8 features of a row; rows past Tq (padding up to a whole
 // query block) get lse = +inf, D = 0.
 __global__ void attn_bwd_pre(const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ dout,
-                             const float *__restrict__ lse, float *__restrict__ lse2,
+                             const float *__restrict__ lse, float *__restrict__ nlse2,
                              float *__restrict__ dvec, float *__restrict__ dq_acc, long long BH,
                              int Tq, int Tq_pad) {
     const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -64,12 +64,12 @@ __global__ void attn_bwd_pre(const __nv_bfloat16 *__restrict__ o, const __nv_bfl
     z[1] = make_float4(0.f, 0.f, 0.f, 0.f);
     if (part == 0) {
         dvec[row] = acc;
-        float l = INFINITY;
+        float l = -INFINITY;
         if (i < Tq) {
             const float x = lse[bh * Tq + i];
-            l = x == -INFINITY ? INFINITY : x * kLog2e;
+            l = x == -INFINITY ? -INFINITY : -x * kLog2e;
         }
-        lse2[row] = l;
+        nlse2[row] = l;
     }
 }
 
@@ -102,30 +102,36 @@ __global__ void attn_bwd_post(const float *__restrict__ dq_acc, __nv_bfloat16 *_
 }
 
 // P^T and dS^T of N of one thread's query columns for its key:
-// p = 2^(s c - lse2), ds = p (dp - D), as bf16 pairs.  kMasked: column e
-// counts iff e >= lim.
+// p = 2^(s c - lse2) (nlse2 = -lse2), ds = p (dp - D), as bf16 pairs, in
+// packed fp32 pair arithmetic.  kMasked: column e counts iff e >= lim.
 template <int N, bool kMasked>
 __device__ __forceinline__ void softmax_terms(const uint32_t (&sv)[N], const uint32_t (&dp)[N],
-                                              const float *lse2, const float *dvec, float C, int lim,
+                                              const float *nlse2, const float *dvec, float C, int lim,
                                               uint32_t (&pk)[N / 2], uint32_t (&dsk)[N / 2]) {
+    const uint64_t C2 = f32x2_pack(C, C);
 #pragma unroll
     for (int g = 0; g < N / 4; ++g) {
-        const float4 l4 = reinterpret_cast<const float4 *>(lse2)[g];
+        const float4 l4 = reinterpret_cast<const float4 *>(nlse2)[g];
         const float4 d4 = reinterpret_cast<const float4 *>(dvec)[g];
-        const float l[4] = {l4.x, l4.y, l4.z, l4.w}, d[4] = {d4.x, d4.y, d4.z, d4.w};
-        float pp[4], dd[4];
+        const uint64_t nl[2] = {f32x2_pack(l4.x, l4.y), f32x2_pack(l4.z, l4.w)};
+        const uint64_t d[2] = {f32x2_pack(d4.x, d4.y), f32x2_pack(d4.z, d4.w)};
 #pragma unroll
-        for (int h = 0; h < 4; ++h) {
-            const int e = 4 * g + h;
-            float pv = ex2_approx(__uint_as_float(sv[e]) * C - l[h]);
-            if (kMasked && e < lim) pv = 0.f;
-            pp[h] = pv;
-            dd[h] = pv * (__uint_as_float(dp[e]) - d[h]);
+        for (int h = 0; h < 2; ++h) {
+            const int e = 4 * g + 2 * h;
+            float x0, x1;
+            f32x2_unpack(fma_f32x2(f32x2_pack(__uint_as_float(sv[e]), __uint_as_float(sv[e + 1])), C2, nl[h]), x0, x1);
+            float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+            if (kMasked) {
+                if (e < lim) p0 = 0.f;
+                if (e + 1 < lim) p1 = 0.f;
+            }
+            const uint64_t dd =
+                mul_f32x2(f32x2_pack(p0, p1), sub_f32x2(f32x2_pack(__uint_as_float(dp[e]), __uint_as_float(dp[e + 1])), d[h]));
+            float ds0, ds1;
+            f32x2_unpack(dd, ds0, ds1);
+            pk[2 * g + h] = pack_bf16x2(p0, p1);
+            dsk[2 * g + h] = pack_bf16x2(ds0, ds1);
         }
-        pk[2 * g] = pack_bf16x2(pp[0], pp[1]);
-        pk[2 * g + 1] = pack_bf16x2(pp[2], pp[3]);
-        dsk[2 * g] = pack_bf16x2(dd[0], dd[1]);
-        dsk[2 * g + 1] = pack_bf16x2(dd[2], dd[3]);
     }
 }
 
@@ -147,10 +153,11 @@ __device__ __forceinline__ void softmax_terms(const uint32_t (&sv)[N], const uin
 //                                        shared memory (queries contiguous)
 //               Computing S and dP transposed puts the keys on the
 //               tensor-memory lanes, so P^T and dS^T feed (3) and (4) straight
-//               from tensor memory.  Issue order: (4) (3) of block j, (1) of
-//               block j+1, (2) of block j+1 once (4) has read dS^T, then (5)
-//               of block j -- the tensor pipe runs in issue order, so (5)
-//               does not delay the next block's scores.
+//               from tensor memory.  Issue order: (4) of block j, (1) of
+//               block j+1, (2) of block j+1 once (4) has read dS^T, then (3)
+//               and (5) of block j -- the tensor pipe runs in issue order, so
+//               only (4) stands between block j's softmax terms and block
+//               j+1's scores.
 //   warps 2-17  one thread per (key, chunk of 32 queries) -- warp w takes the
 //               keys of lane quadrant w%4 and chunk (w-2)/4:
 //               P^T = 2^(S^T c - lse_j) (masked: 0), dS^T = P^T (dP^T - D_j),
@@ -158,18 +165,18 @@ __device__ __forceinline__ void softmax_terms(const uint32_t (&sv)[N], const uin
 //               reduction); P^T and dS^T written as bf16, dS^T also into
 //               shared memory for (5) (two buffers: block j+2 reuses block
 //               j's, whose (5) the commit of block j+1's scores already
-//               covers).  After block j's terms, the same warps move the
-//               dQ_{j-1} partial out of tensor memory (warp w: the rows of
-//               quadrant w%4, features [16c, 16c+16)), stage it in shared
-//               memory and add it to the fp32 accumulator in global memory
-//               by one bulk reduction per warp (other key blocks add theirs).
-//               At the end chunks 0, 1 write dK (times scale) and chunks 2, 3
-//               dV, 32 features each.
+//               covers).  After block j's terms, the same warps add the
+//               dQ_{j-1} partial (warp w: the rows of quadrant w%4, features
+//               [16c, 16c+16)) to the fp32 accumulator in global memory with
+//               vector reductions, each warp instruction covering 512
+//               contiguous bytes of the accumulator's layout (other key blocks
+//               add theirs).  At the end chunks 0, 1 write dK (times scale) and
+//               chunks 2, 3 dV, 32 features each.
 //
 // Tensor memory: S^T [0,128), dP^T [128,256), P^T [256,320), dV [320,384),
 // dK [384,448), dQ_j [448,512).  dS^T of chunk c goes over dP^T columns
 // [128+32c, 128+32c+16), which only chunk c's warp reads; P^T has columns of
-// its own so that (1) of the next block need not wait for (3).
+// its own so that the next block's scores need not wait for (3).
 constexpr uint32_t kTile = BQ * HD * 2;  // 16 KiB
 constexpr uint32_t kColS = 0, kColDP = 128, kColP = 256, kColDV = 320, kColDK = 384, kColDQ = 448;
 constexpr int kBwdThreads = 576;
@@ -181,15 +188,16 @@ struct __align__(1024) SmemBwd {
     uint8_t q[2][kTile];
     uint8_t g[2][kTile];      // dO
     uint8_t ds[2][2 * kTile]; // dS as the A operand of (5): 2 blocks of 64 queries x 128 key rows
-    float4 dq_stage[4][16 * 32];  // per lane quadrant: [16-byte chunk][row of the quadrant]
-    float lse2[2][BQ];
+    float nlse2[2][BQ];
     float dvec[2][BQ];
     uint64_t kv_full;
     uint64_t stage_full[2];
-    uint64_t stage_empty[2];
+    uint64_t q_empty[2];  // (1), (4) have read Q_j (and the softmax lse_j, D_j)
+    uint64_t g_empty[2];  // (2), (3) have read dO_j
     uint64_t sdp_full;   // (1), (2) complete
     uint64_t pds_full;   // P^T, dS^T written (16 warps)
     uint64_t tmem_free;  // (4) complete: the dP^T columns reusable
+    uint64_t p_free;     // (3) complete: the P^T columns reusable
     uint64_t dq_full;    // (5) complete
     uint64_t dq_free;    // dQ_j read (16 warps)
     uint64_t acc_done;   // every product complete
@@ -224,8 +232,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         mbar_init(&sm.kv_full, 1);
         for (int i = 0; i < 2; ++i) {
             mbar_init(&sm.stage_full[i], 1);
-            mbar_init(&sm.stage_empty[i], 1);
+            mbar_init(&sm.q_empty[i], 1);
+            mbar_init(&sm.g_empty[i], 1);
         }
+        mbar_init(&sm.p_free, 1);
         mbar_init(&sm.sdp_full, 1);
         mbar_init(&sm.pds_full, kSoftmaxWarps);
         mbar_init(&sm.tmem_free, 1);
@@ -261,15 +271,17 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             int issued = 0;
             for (int t = 0; t < n_j; ++t) {
                 const int st = t & 1;
-                if (t >= 2 && !mbar_wait(&sm.stage_empty[st], ((t >> 1) - 1) & 1, ab)) break;
+                if (t >= 2 && !mbar_wait(&sm.q_empty[st], ((t >> 1) - 1) & 1, ab)) break;
                 const int j = j_begin + t;
                 const long long vrow = static_cast<long long>(bh) * p.Tq_pad + j * BQ;
                 mbar_arrive_expect_tx(&sm.stage_full[st], 2 * kTile + 2 * BQ * 4);
                 tma_load_3d(&tmap_q, &sm.stage_full[st], sm.q[st], 0, j * BQ, bh);
-                tma_load_3d(&tmap_g, &sm.stage_full[st], sm.g[st], 0, j * BQ, bh);
-                bulk_load_1d(sm.lse2[st], p.lse2 + vrow, BQ * 4, &sm.stage_full[st]);
+                bulk_load_1d(sm.nlse2[st], p.nlse2 + vrow, BQ * 4, &sm.stage_full[st]);
                 bulk_load_1d(sm.dvec[st], p.dvec + vrow, BQ * 4, &sm.stage_full[st]);
                 issued = t + 1;
+                // dO_j last: its slot frees later (after (3))
+                if (t >= 2 && !mbar_wait(&sm.g_empty[st], ((t >> 1) - 1) & 1, ab)) break;
+                tma_load_3d(&tmap_g, &sm.stage_full[st], sm.g[st], 0, j * BQ, bh);
             }
             mbar_wait_drain(&sm.kv_full, 0);
             for (int x = max(0, issued - 2); x < issued; ++x)
@@ -324,21 +336,26 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     warp_mma_bf16_ts(tmem + kColDK, tmem + kColDP + 32 * (kk >> 1) + 8 * (kk & 1),
                                      q_mn + so + 128 * kk, id_kv, (t > 0 || kk > 0) ? 1u : 0u);
                 warp_commit(&sm.tmem_free);
-#pragma unroll
-                for (int kk = 0; kk < BQ / 16; ++kk)
-                    warp_mma_bf16_ts(tmem + kColDV, tmem + kColP + 8 * kk, g_mn + so + 128 * kk, id_kv,
-                                     (t > 0 || kk > 0) ? 1u : 0u);
-                warp_commit(&sm.stage_empty[st]);  // (1)-(4) were the stage's last readers
+                warp_commit(&sm.q_empty[st]);
                 if (t + 1 < n_j) {
+                    // the next block's scores; (1) runs while (4)'s completion
+                    // comes back, (2) overwrites the dS^T that (4) reads
                     if (!(ok = warp_wait(&sm.stage_full[st ^ 1], ((t + 1) >> 1) & 1, ab))) break;
                     tc_fence_after_sync();
                     score_s(st ^ 1);
-                    // dP^T of the next block overwrites the dS^T that (4) reads
                     if (!(ok = warp_wait(&sm.tmem_free, t & 1, ab))) break;
                     tc_fence_after_sync();
                     score_dp(st ^ 1);
                     warp_commit(&sm.sdp_full);
                 }
+                // (3) after the next block's scores: P^T has columns of its
+                // own, which the softmax warps rewrite only after p_free
+#pragma unroll
+                for (int kk = 0; kk < BQ / 16; ++kk)
+                    warp_mma_bf16_ts(tmem + kColDV, tmem + kColP + 8 * kk, g_mn + so + 128 * kk, id_kv,
+                                     (t > 0 || kk > 0) ? 1u : 0u);
+                warp_commit(&sm.p_free);
+                warp_commit(&sm.g_empty[st]);
                 if (t >= 1 && !(ok = warp_wait(&sm.dq_free, (t - 1) & 1, ab))) break;
                 tc_fence_after_sync();
                 const uint64_t dso = static_cast<uint64_t>(st) * (2 * kT);
@@ -363,32 +380,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         const float C = p.scale_log2;
         // dQ_u of this warp's rows and features [16c, 16c+16): chunks
         // [4c, 4c+4) of the quadrant's accumulator quarter.
-        float4 *stage = sm.dq_stage[warp & 3] + 4 * c * 32;
         auto add_dq = [&](int u) -> bool {
             if (!__all_sync(0xffffffffu, mbar_wait(&sm.dq_full, u & 1, ab))) return false;
-            if (lane == 0) bulk_wait_read();  // the previous reduction has read the stage
-            __syncwarp();
             tc_fence_after_sync();
             uint32_t a[16];
             tmem_ld16(tl + kColDQ + 16u * c, a);
             tmem_ld_wait(a);
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.dq_free);
+            // chunks [4c, 4c+4) of the quadrant's quarter: per chunk the 32
+            // lanes' vectors are 512 contiguous bytes
+            float *dst = p.dq_acc + (static_cast<long long>(bh) * p.Tq_pad + (j_begin + u) * BQ + lane_base) * HD +
+                         512 * c + 4 * lane;
 #pragma unroll
             for (int x = 0; x < 4; ++x)
-                stage[x * 32 + lane] = make_float4(__uint_as_float(a[4 * x]), __uint_as_float(a[4 * x + 1]),
-                                                   __uint_as_float(a[4 * x + 2]), __uint_as_float(a[4 * x + 3]));
-            tc_fence_before_sync();
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&sm.dq_free);
-                // rows past Tq carry zeros (their weights are 0) and stay
-                // inside the padded accumulator
-                float *dst = p.dq_acc +
-                             (static_cast<long long>(bh) * p.Tq_pad + (j_begin + u) * BQ + lane_base) * HD +
-                             512 * c;
-                bulk_reduce_add_f32(dst, stage, 4 * 32 * 16);
-                bulk_commit_group();
-            }
+                red_add_v4(dst + 128 * x, __uint_as_float(a[4 * x]), __uint_as_float(a[4 * x + 1]),
+                           __uint_as_float(a[4 * x + 2]), __uint_as_float(a[4 * x + 3]));
             return true;
         };
         bool ok = true;
@@ -412,13 +420,15 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 tmem_ld_wait(sv);
                 tmem_ld_wait(dp);
                 uint32_t pk[8], dsk[8];
-                const float *l2 = sm.lse2[st] + 32 * c + 16 * h, *dv = sm.dvec[st] + 32 * c + 16 * h;
+                const float *l2 = sm.nlse2[st] + 32 * c + 16 * h, *dv = sm.dvec[st] + 32 * c + 16 * h;
                 if (__all_sync(0xffffffffu, lim <= 0))
                     softmax_terms<16, false>(sv, dp, l2, dv, C, 0, pk, dsk);
                 else
                     softmax_terms<16, true>(sv, dp, l2, dv, C, lim, pk, dsk);
-                // P^T into its own columns, dS^T over dP^T columns this warp
-                // has read
+                // P^T into its own columns once (3) of the previous block has
+                // read them, dS^T over dP^T columns this warp has read
+                if (h == 0 && t >= 1 && !(ok = __all_sync(0xffffffffu, mbar_wait(&sm.p_free, (t - 1) & 1, ab))))
+                    break;
                 tmem_st8(tl + kColP + 16u * c + 8u * h, pk);
                 tmem_st8(tl + kColDP + 32u * c + 8u * h, dsk);
                 // dS into shared memory as the A operand of (5): queries
@@ -431,6 +441,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                         make_uint4(dsk[4 * x], dsk[4 * x + 1], dsk[4 * x + 2], dsk[4 * x + 3]);
                 }
             }
+            if (!ok) break;
             tmem_st_wait();
             fence_proxy_async_smem();
             tc_fence_before_sync();
@@ -470,7 +481,6 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
         }
         if (!ok) tmem_st_wait();
-        if (lane == 0) bulk_wait_all();
     }
 
     tc_fence_before_sync();
@@ -498,16 +508,16 @@ cudaError_t launch_attn_bwd_bf16(const CUtensorMap &tq, const CUtensorMap &tk, c
     const size_t rows = static_cast<size_t>(BH) * p.Tq_pad;
     auto r256 = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
     uint8_t *ws = static_cast<uint8_t *>(workspace);
-    float *lse2 = reinterpret_cast<float *>(ws + r256(rows * HD * 4));
+    float *nlse2 = reinterpret_cast<float *>(ws + r256(rows * HD * 4));
     float *dvec = reinterpret_cast<float *>(ws + r256(rows * HD * 4) + r256(rows * 4));
     p.dq_acc = reinterpret_cast<float *>(ws);
-    p.lse2 = lse2;
+    p.nlse2 = nlse2;
     p.dvec = dvec;
     cudaError_t e = cudaSuccess;
     const long long pre_threads = static_cast<long long>(rows) * 8;
     if (pre_threads > 0) {
         attn_bwd_pre<<<static_cast<unsigned>((pre_threads + 255) / 256), 256, 0, stream>>>(
-            o, dout, lse, lse2, dvec, p.dq_acc, BH, p.Tq, p.Tq_pad);
+            o, dout, lse, nlse2, dvec, p.dq_acc, BH, p.Tq, p.Tq_pad);
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     if (p.Tk > 0) {

@@ -52,7 +52,7 @@ struct BwdParams {
     float scale, scale_log2;
     int mask;
     const int32_t *key_lens;
-    const float *lse2;          // (B, H, Tq_pad) lse * log2(e), +inf for padded / empty rows
+    const float *nlse2;         // (B, H, Tq_pad) -lse * log2(e), -inf for padded / empty rows
     const float *dvec;          // (B, H, Tq_pad) rowsum(dO * O)
     float *dq_acc;              // (B, H, Tq_pad, 64) fp32
     __nv_bfloat16 *dk, *dv;     // (B, H, Tk, 64)
