@@ -163,28 +163,6 @@ __device__ __forceinline__ void bulk_load_1d(void *dst, const void *src, uint32_
         : "memory");
 }
 
-// dst[0 .. bytes/4) += src[0 .. bytes/4) (fp32), an untiled bulk reduction
-// from shared to global memory in the calling thread's bulk group (bytes a
-// multiple of 16; both addresses 16-byte aligned).  The shared source must
-// not be rewritten before bulk_wait_read() returns.
-__device__ __forceinline__ void bulk_reduce_add_f32(float *dst, const void *src, uint32_t bytes) {
-    asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(
-                     reinterpret_cast<uint64_t>(dst)),
-                 "r"(smem_u32(src)), "r"(bytes)
-                 : "memory");
-}
-__device__ __forceinline__ void bulk_commit_group() {
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-// The sources of this thread's bulk groups have been read.
-__device__ __forceinline__ void bulk_wait_read() {
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-// This thread's bulk groups have completed.
-__device__ __forceinline__ void bulk_wait_all() {
-    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
-}
-
 // Makes this thread's generic-proxy writes to shared memory visible to the
 // async proxy (a tcgen05.mma that reads them as an operand).
 __device__ __forceinline__ void fence_proxy_async_smem() {
