@@ -109,6 +109,37 @@ mha_status sdpa_forward_lse(mha_dtype dt, const void *q, const void *k, const vo
                             cudaStream_t stream);
 
 /*
+ * sdpa_forward with HOST buffers: q, k, v (and key_lens) are read from, and o
+ * written to, caller-owned HOST memory with the layouts, types and limits of
+ * sdpa_forward.  Page-locked memory (cudaHostAlloc / cudaHostRegister) lets
+ * the copies run asynchronously; pageable memory works but every copy then
+ * completes before the call goes on.  workspace: DEVICE memory of at least
+ * sdpa_forward_host_workspace_bytes() bytes, 256-byte aligned, owned by the
+ * caller (the device copies of q, k, v, o and key_lens).  key_lens: HOST
+ * int32 array of B entries (key-padding masks only).
+ *
+ * The heads are taken in up to 8 chunks (groups of heads of one batch item,
+ * or whole batch items): chunk i's host-to-device copies, its attention launch
+ * on `stream` and its device-to-host copy of o are chained by events, the
+ * copies run on two internal copy streams (created on first use, one pair per
+ * device, kept for the life of the process), so the copies of one chunk
+ * overlap the attention of another.  The whole sequence is ordered after the
+ * work enqueued on `stream` before the call and before the work enqueued on
+ * it afterwards: synchronise `stream` before reading o, and keep the host
+ * buffers valid and unchanged until then.  Calls are serialised per device by
+ * a mutex while they enqueue.  Errors as sdpa_forward; a workspace that is
+ * missing or too small is MHA_ERR_INVALID_ARG, a misaligned one
+ * MHA_ERR_MISALIGNED (both detected before anything is enqueued).
+ */
+size_t sdpa_forward_host_workspace_bytes(mha_dtype dt, int B, int h, int T_q, int T_k, int d_k,
+                                         int d_v);
+mha_status sdpa_forward_host(mha_dtype dt, const void *q_host, const void *k_host,
+                             const void *v_host, void *o_host, void *workspace,
+                             size_t workspace_bytes, int B, int h, int T_q, int T_k, int d_k,
+                             int d_v, float scale, mha_mask mask, const int32_t *key_lens_host,
+                             int *status_dev, cudaStream_t stream);
+
+/*
  * Gradients of sdpa_forward (bf16): given q, k, v, the forward's output o
  * and log-sum-exp lse (from sdpa_forward_lse) and the output gradient dout,
  * writes

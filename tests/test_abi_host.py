@@ -205,3 +205,35 @@ def test_positional_encoding_rejects_bad_arguments(lib):
     assert f(FAKE, FAKE, 1, 4, 64, -1, None) == lib.MHA_ERR_INVALID_ARG
     assert f(FAKE + 4, FAKE, 1, 4, 64, 0, None) == lib.MHA_ERR_MISALIGNED
     assert f(FAKE, FAKE, 0, 4, 64, 0, None) == lib.MHA_OK
+
+
+def host(lib, dt=1, p=FAKE, ws=FAKE, ws_bytes=1 << 40, B=1, h=1, Tq=8, Tk=8, dk=64, dv=64, mask=0,
+         lens=None, scale=0.125):
+    return lib.lib.sdpa_forward_host(dt, p, p, p, p, ws, ws_bytes, B, h, Tq, Tk, dk, dv, scale, mask,
+                                     lens, None, None)
+
+
+def test_host_path_rejects_bad_arguments(lib):
+    # every rejection happens before the library touches CUDA
+    assert host(lib, ws=None) == 1
+    assert host(lib, ws_bytes=1024) == 1                      # smaller than the device copies
+    assert host(lib, ws=FAKE + 16) == 4                       # workspace not 256-byte aligned
+    assert host(lib, dk=32, dv=32) == 2                       # bf16 path needs d = 64
+    assert host(lib, dt=0, dk=160, dv=160) == 2               # fp32 path: d <= 128
+    assert host(lib, dt=7) == 1
+    assert host(lib, mask=2, lens=None) == 1                  # key padding needs key_lens
+    assert host(lib, mask=9) == 1
+    assert host(lib, B=-1) == 1
+    assert host(lib, scale=float("nan")) == 1
+    assert host(lib, p=None) == 1
+    assert host(lib, B=0) == 0 and host(lib, Tq=0) == 0       # empty problems: no-ops
+
+
+def test_host_workspace_bytes(lib):
+    r = lambda x: (x + 255) // 256 * 256
+    B, h, Tq, Tk = 2, 3, 130, 7
+    bf = lib.lib.sdpa_forward_host_workspace_bytes(1, B, h, Tq, Tk, 64, 64)
+    assert bf == r(B * h * Tq * 128) + 2 * r(B * h * Tk * 128) + r(B * h * Tq * 128) + r(B * 4)
+    f32 = lib.lib.sdpa_forward_host_workspace_bytes(0, B, h, Tq, Tk, 32, 48)
+    assert f32 == r(B * h * Tq * 128) + r(B * h * Tk * 128) + r(B * h * Tk * 192) + r(B * h * Tq * 192) + r(B * 4)
+    assert lib.lib.sdpa_forward_host_workspace_bytes(1, -1, h, Tq, Tk, 64, 64) == 0

@@ -16,7 +16,7 @@ from . import _native
 from ._native import (MHA_BF16, MHA_F32, MHA_MASK_CAUSAL, MHA_MASK_CAUSAL_KEY_PADDING,
                       MHA_MASK_KEY_PADDING, MHA_MASK_NONE, MHA_OK, lib)
 
-__all__ = ["sdpa_forward", "sdpa_forward_lse", "sdpa_backward", "positional_encoding_add",
+__all__ = ["sdpa_forward", "sdpa_forward_lse", "sdpa_forward_host", "sdpa_forward_host_workspace_bytes", "sdpa_backward", "positional_encoding_add",
            "encoder_layer_forward", "ENCODER_PARAMS", "sdpa_decode_forward", "mha_forward", "mha_forward_add_layernorm", "mha_workspace_bytes", "status_string", "MhaError",
            "MASKS", "lib"]
 
@@ -124,6 +124,59 @@ def sdpa_forward_lse(q, k, v, out=None, lse=None, *, scale=None, mask="none", ke
     if rc != MHA_OK:
         raise MhaError(rc, "sdpa_forward_lse")
     return out, lse
+
+
+def _check_host(name, t, dtype=None):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor) or t.device.type != "cpu":
+        raise ValueError("%s must be a CPU tensor" % name)
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError("%s must be %s" % (name, dtype))
+
+
+def sdpa_forward_host_workspace_bytes(B, h, T_q, T_k, d_k=64, d_v=64, dtype=None) -> int:
+    torch = _torch()
+    dt = MHA_F32 if dtype == torch.float32 else MHA_BF16
+    return int(lib.sdpa_forward_host_workspace_bytes(dt, B, h, T_q, T_k, d_k, d_v))
+
+
+def sdpa_forward_host(q, k, v, out=None, workspace=None, *, scale=None, mask="none", key_lens=None,
+                      status=None, stream=None):
+    """sdpa_forward with q, k, v, out (and key_lens) in host memory (CPU
+    tensors, page-locked for overlapped copies) and a device workspace; the
+    library copies, computes and copies back in chunks that overlap.  The
+    result is in `out` once `stream` has been synchronised.  Returns out."""
+    torch = _torch()
+    dtype = q.dtype
+    if dtype not in (torch.float32, torch.bfloat16):
+        raise ValueError("q must be float32 or bfloat16")
+    for n, t in (("q", q), ("k", k), ("v", v)):
+        _check_host(n, t, dtype)
+    B, h, T_q, d_k = q.shape
+    T_k, d_v = k.shape[2], v.shape[3]
+    if out is None:
+        out = torch.empty((B, h, T_q, d_v), dtype=dtype, pin_memory=torch.cuda.is_available())
+    _check_host("out", out, dtype)
+    if key_lens is not None:
+        _check_host("key_lens", key_lens, torch.int32)
+    if status is not None:
+        _check_dev("status", status, torch.int32)
+    dt = MHA_F32 if dtype == torch.float32 else MHA_BF16
+    need = int(lib.sdpa_forward_host_workspace_bytes(dt, B, h, T_q, T_k, d_k, d_v))
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device="cuda")
+    _check_dev("workspace", workspace)
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_k)
+    rc = lib.sdpa_forward_host(dt, _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), B, h, T_q, T_k, d_k,
+                               d_v, float(scale), _mask_code(mask), _ptr(key_lens), _ptr(status),
+                               _stream_handle(stream))
+    if rc != MHA_OK:
+        raise MhaError(rc, "sdpa_forward_host")
+    return out
 
 
 def sdpa_backward(q, k, v, o, dout, lse, dq=None, dk=None, dv=None, workspace=None, *,

@@ -1,6 +1,7 @@
 // api.cu -- the C ABI declared in include/mha.h: argument checks, TMA
 // tensor-map encoding and kernel launches on the caller's stream.  Nothing
-// here allocates, frees or synchronises.
+// here allocates device memory, frees or synchronises; sdpa_forward_host
+// keeps two copy streams and a few events per device for its pipeline.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -8,6 +9,7 @@
 
 #include <stdio.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "../../include/mha.h"
@@ -224,6 +226,155 @@ MHA_EXPORT mha_status sdpa_forward_lse(mha_dtype dt, const void *q, const void *
     if (!lse && B > 0 && h > 0 && T_q > 0) return MHA_ERR_INVALID_ARG;
     return sdpa_impl(dt, q, k, v, o, lse, B, h, T_q, T_k, d_k, d_v, scale, mask, key_lens,
                      status_dev, stream);
+}
+
+namespace {
+
+// Internal streams and events of sdpa_forward_host, one set per device,
+// created on first use and kept for the life of the process.  The enqueue
+// sequence of one call holds the device's mutex: an event is re-recorded only
+// after every wait on its previous record has been enqueued.
+constexpr int kHostChunks = 8;
+struct HostPipe {
+    std::mutex mu;
+    bool ready = false;
+    cudaStream_t s_in = nullptr, s_out = nullptr;
+    cudaEvent_t start = nullptr, done = nullptr, in[kHostChunks] = {}, comp[kHostChunks] = {};
+};
+constexpr int kMaxDevices = 64;
+HostPipe g_host_pipe[kMaxDevices];
+
+mha_status host_pipe_init(HostPipe &hp) {
+    if (hp.ready) return MHA_OK;
+    cudaError_t e = cudaStreamCreateWithFlags(&hp.s_in, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&hp.s_out, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.done, cudaEventDisableTiming);
+    for (int i = 0; e == cudaSuccess && i < kHostChunks; ++i) {
+        e = cudaEventCreateWithFlags(&hp.in[i], cudaEventDisableTiming);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&hp.comp[i], cudaEventDisableTiming);
+    }
+    if (e != cudaSuccess) return cuda_fail("sdpa_forward_host setup", cudaGetErrorString(e));
+    hp.ready = true;
+    return MHA_OK;
+}
+
+// Device bytes of one copy of q, k, v, o and key_lens (each 256-byte aligned).
+size_t host_ws_parts(mha_dtype dt, int B, int h, int T_q, int T_k, int d_k, int d_v, size_t *off) {
+    const size_t es = dt == MHA_F32 ? 4 : 2;
+    const size_t BH = static_cast<size_t>(B) * static_cast<size_t>(h);
+    const size_t sz[5] = {BH * T_q * d_k * es, BH * T_k * d_k * es, BH * T_k * d_v * es,
+                          BH * T_q * d_v * es, static_cast<size_t>(B) * 4};
+    size_t at = 0;
+    for (int i = 0; i < 5; ++i) {
+        off[i] = at;
+        at += round256(sz[i]);
+    }
+    return at;
+}
+
+}  // namespace
+
+MHA_EXPORT size_t sdpa_forward_host_workspace_bytes(mha_dtype dt, int B, int h, int T_q, int T_k,
+                                                    int d_k, int d_v) {
+    if (B < 0 || h < 0 || T_q < 0 || T_k < 0 || d_k <= 0 || d_v <= 0) return 0;
+    size_t off[5];
+    return host_ws_parts(dt, B, h, T_q, T_k, d_k, d_v, off);
+}
+
+MHA_EXPORT mha_status sdpa_forward_host(mha_dtype dt, const void *q_host, const void *k_host,
+                                        const void *v_host, void *o_host, void *workspace,
+                                        size_t workspace_bytes, int B, int h, int T_q, int T_k,
+                                        int d_k, int d_v, float scale, mha_mask mask,
+                                        const int32_t *key_lens_host, int *status_dev,
+                                        cudaStream_t stream) {
+    if (B < 0 || h < 0 || T_q < 0 || T_k < 0 || d_k <= 0 || d_v <= 0) return MHA_ERR_INVALID_ARG;
+    if (dt != MHA_F32 && dt != MHA_BF16) return MHA_ERR_INVALID_ARG;
+    if (!valid_mask(mask) || !isfinite(scale)) return MHA_ERR_INVALID_ARG;
+    if ((mask & MHA_MASK_KEY_PADDING) && !key_lens_host) return MHA_ERR_INVALID_ARG;
+    if (static_cast<long long>(B) * h >= (1ll << 31)) return MHA_ERR_UNSUPPORTED;
+    if (B == 0 || h == 0 || T_q == 0) return MHA_OK;
+    if (!q_host || !o_host || (T_k > 0 && (!k_host || !v_host))) return MHA_ERR_INVALID_ARG;
+    size_t off[5];
+    const size_t need = host_ws_parts(dt, B, h, T_q, T_k, d_k, d_v, off);
+    if (!workspace || workspace_bytes < need) return MHA_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MHA_ERR_MISALIGNED;
+    if (dt == MHA_BF16 && (d_k != 64 || d_v != 64)) return MHA_ERR_UNSUPPORTED;
+    if (dt == MHA_F32 && (d_k > 128 || d_v > 128)) return MHA_ERR_UNSUPPORTED;
+
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail("cudaGetDevice", cudaGetErrorString(e));
+    if (dev < 0 || dev >= kMaxDevices) return MHA_ERR_UNSUPPORTED;
+    HostPipe &hp = g_host_pipe[dev];
+    std::lock_guard<std::mutex> lock(hp.mu);
+    mha_status st = host_pipe_init(hp);
+    if (st != MHA_OK) return st;
+
+    uint8_t *ws = static_cast<uint8_t *>(workspace);
+    uint8_t *qd = ws + off[0], *kd = ws + off[1], *vd = ws + off[2], *od = ws + off[3];
+    int32_t *lens_d = reinterpret_cast<int32_t *>(ws + off[4]);
+    const size_t es = dt == MHA_F32 ? 4 : 2;
+    const size_t q_head = static_cast<size_t>(T_q) * d_k * es, k_head = static_cast<size_t>(T_k) * d_k * es;
+    const size_t v_head = static_cast<size_t>(T_k) * d_v * es, o_head = static_cast<size_t>(T_q) * d_v * es;
+    const bool padded = (mask & MHA_MASK_KEY_PADDING) != 0;
+
+    // Chunks: whole batch items when h is small, else groups of heads of one
+    // batch item (the kernels take key_lens per batch item).
+    const long long BH = static_cast<long long>(B) * h;
+    const long long per = (BH + kHostChunks - 1) / kHostChunks;
+    const int nb = per >= h ? static_cast<int>(per / h) : 0;  // batch items per chunk
+    const int nh = per >= h ? h : static_cast<int>(per);      // heads per chunk (of one item)
+
+    auto fail = [](cudaError_t err, const char *what) { return cuda_fail(what, cudaGetErrorString(err)); };
+    if ((e = cudaEventRecord(hp.start, stream)) != cudaSuccess) return fail(e, "cudaEventRecord");
+    if ((e = cudaStreamWaitEvent(hp.s_in, hp.start, 0)) != cudaSuccess) return fail(e, "cudaStreamWaitEvent");
+    if ((e = cudaStreamWaitEvent(hp.s_out, hp.start, 0)) != cudaSuccess) return fail(e, "cudaStreamWaitEvent");
+    if (padded && (e = cudaMemcpyAsync(lens_d, key_lens_host, static_cast<size_t>(B) * 4,
+                                       cudaMemcpyHostToDevice, hp.s_in)) != cudaSuccess)
+        return fail(e, "key_lens copy");
+
+    int chunk = 0;
+    for (int b = 0; b < B;) {
+        const int cb = nb > 0 ? std::min(nb, B - b) : 1;  // batch items [b, b + cb)
+        for (int h0 = 0; h0 < h; h0 += (nb > 0 ? h : nh), ++chunk) {
+            const int ch = nb > 0 ? h : std::min(nh, h - h0);  // heads [h0, h0 + ch) of each
+            const size_t f = static_cast<size_t>(b) * h + h0;  // first flattened head
+            const size_t nheads = static_cast<size_t>(cb) * ch;
+            const int slot = chunk % kHostChunks;
+            const char *qh = static_cast<const char *>(q_host), *kh = static_cast<const char *>(k_host);
+            const char *vh = static_cast<const char *>(v_host);
+            if ((e = cudaMemcpyAsync(qd + f * q_head, qh + f * q_head, nheads * q_head,
+                                     cudaMemcpyHostToDevice, hp.s_in)) != cudaSuccess)
+                return fail(e, "q copy");
+            if (T_k > 0) {
+                if ((e = cudaMemcpyAsync(kd + f * k_head, kh + f * k_head, nheads * k_head,
+                                         cudaMemcpyHostToDevice, hp.s_in)) != cudaSuccess)
+                    return fail(e, "k copy");
+                if ((e = cudaMemcpyAsync(vd + f * v_head, vh + f * v_head, nheads * v_head,
+                                         cudaMemcpyHostToDevice, hp.s_in)) != cudaSuccess)
+                    return fail(e, "v copy");
+            }
+            if ((e = cudaEventRecord(hp.in[slot], hp.s_in)) != cudaSuccess) return fail(e, "cudaEventRecord");
+            if ((e = cudaStreamWaitEvent(stream, hp.in[slot], 0)) != cudaSuccess)
+                return fail(e, "cudaStreamWaitEvent");
+            st = sdpa_impl(dt, qd + f * q_head, kd + f * k_head, vd + f * v_head, od + f * o_head, nullptr, cb,
+                           ch, T_q, T_k, d_k, d_v, scale, mask, padded ? lens_d + b : nullptr, status_dev,
+                           stream);
+            if (st != MHA_OK) return st;
+            if ((e = cudaEventRecord(hp.comp[slot], stream)) != cudaSuccess) return fail(e, "cudaEventRecord");
+            if ((e = cudaStreamWaitEvent(hp.s_out, hp.comp[slot], 0)) != cudaSuccess)
+                return fail(e, "cudaStreamWaitEvent");
+            if ((e = cudaMemcpyAsync(static_cast<char *>(o_host) + f * o_head, od + f * o_head,
+                                     nheads * o_head, cudaMemcpyDeviceToHost, hp.s_out)) != cudaSuccess)
+                return fail(e, "o copy");
+        }
+        b += cb;
+    }
+    // later work on `stream` (and its synchronisation) covers the copies
+    if ((e = cudaEventRecord(hp.done, hp.s_out)) != cudaSuccess) return fail(e, "cudaEventRecord");
+    if ((e = cudaStreamWaitEvent(stream, hp.done, 0)) != cudaSuccess) return fail(e, "cudaStreamWaitEvent");
+    return MHA_OK;
 }
 
 MHA_EXPORT size_t sdpa_backward_workspace_bytes(int B, int h, int T_q, int T_k, int d_k, int d_v) {
