@@ -142,3 +142,22 @@ def test_decode_matches_full_kernel_with_padding(lib):
     full = lib.sdpa_forward(q, k, v, scale=w.scale, mask="key_padding", key_lens=lens)
     torch.cuda.synchronize()
     check_bf16(host(dec), host(full), "decode vs full kernel")
+
+
+# Batch sizes from one entry to more than the 8-CTA clusters fill in one wave,
+# with tied and empty caches among the lengths.
+@pytest.mark.parametrize("B", [1, 2, 5, 16, 64, 65, 70])
+def test_decode_batch_sizes(lib, B):
+    w = si.WORKLOADS[5].replace(B=B, h=3, T_q=2, T_k=700, len_lo=0, len_hi=700, seed=60 + B)
+    x = si.make_inputs(w)
+    lens = x["key_lens"].copy()
+    lens[::4] = lens[0]    # ties
+    lens[1::7] = 0         # empty caches
+    x["key_lens"] = lens
+    check_bf16(host(run_decode(lib, w, x)), oracle_decode(w, x), "B%d" % B)
+
+
+def test_decode_all_lengths_equal(lib):
+    w = si.WORKLOADS[5].replace(B=9, h=2, T_q=1, T_k=513, mask=si.MASK_NONE, seed=71)
+    x = si.make_inputs(w)
+    check_bf16(host(run_decode(lib, w, x)), oracle_decode(w, x), "equal lengths")
