@@ -15,12 +15,16 @@
 // CTAs (BN = 256, or 128 when D is not a multiple of 256), CTA r owning output
 // columns [r*BN, (r+1)*BN).  Per CTA:
 //
-//   warp 0      TMA producer: A = 128 rows x 64 k of the merged heads, B = 64 k
-//               x BN columns of W^O, 4-stage (BN = 256) / 6-stage ring.
+//   warp 0      TMA producer: first this CTA's 128 x BN block of the residual
+//               x (128-byte swizzled, for the epilogue, landing while the
+//               products run), then A = 128 rows x 64 k of the merged heads,
+//               B = 64 k x BN columns of W^O, 3-stage (BN = 256) / 5-stage ring.
 //   warp 1      MMA issuer (tcgen05.mma kind::f16, M=128 N=BN, fp32
 //               accumulator in BN tensor-memory columns, elected lane).
 //   warps 2-5   epilogue, one thread per row, three passes over the
-//               accumulator: (1) v = acc + x, row sum; (2) sum of (v - mu)^2;
+//               accumulator (x read from shared memory: 16-byte chunk j of row
+//               r at j ^ (r % 8), no bank conflicts): (1) v = acc + x, row sum;
+//               (2) sum of (v - mu)^2;
 //               (3) normalise, scale, shift, store bf16.  After (1) and (2) the
 //               CTAs of the cluster exchange their per-row partial sums through
 //               distributed shared memory, so mean and variance are exact
@@ -43,19 +47,22 @@ constexpr uint32_t kBBlock = BK * 64 * 2;  // 8 KiB: one 64-column block of a B 
 
 template <int BN>
 struct LnCfg {
-    static constexpr int kStages = BN == 128 ? 6 : 4;
+    static constexpr int kStages = BN == 128 ? 5 : 3;
     static constexpr uint32_t kBBytes = BK * BN * 2;
 };
+constexpr uint32_t kXBox = BM * 128;  // 16 KiB: 128 rows x 64 features of the residual
 
 template <int BN>
 struct __align__(1024) SmemLn {
     static constexpr int STAGES = LnCfg<BN>::kStages;
     uint8_t a[STAGES][kABytes];
     uint8_t b[STAGES][LnCfg<BN>::kBBytes];
+    uint8_t xs[BN / 64][kXBox];  // residual block, 64 features per box
     float part[2][BM];  // this CTA's per-row partial: [0] sum of v, [1] sum of (v - mu)^2
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
     uint64_t acc_full;
+    uint64_t x_full;
     uint64_t drain;
     uint32_t tmem_base;
     int abort_flag;
@@ -89,6 +96,13 @@ __device__ __forceinline__ void bf16x8(const uint4 &u, float (&f)[8]) {
     }
 }
 
+// Eight residual features [8j', 8j'+8) of row r, j' = column / 8 within the
+// block: box j'/8, chunk j' % 8 swizzled with the row.
+template <int BN>
+__device__ __forceinline__ uint4 x_chunk(const SmemLn<BN> &sm, int r, int j) {
+    return *reinterpret_cast<const uint4 *>(sm.xs[j >> 3] + r * 128 + (((j & 7) ^ (r & 7)) << 4));
+}
+
 // x[0..7] += bias[n .. n+7] (bf16), if there is a bias: the residual and the
 // sublayer's output bias enter the row together.
 __device__ __forceinline__ void add_bias(float (&x)[8], const __nv_bfloat16 *bias, int n) {
@@ -102,7 +116,7 @@ __device__ __forceinline__ void add_bias(float (&x)[8], const __nv_bfloat16 *bia
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_ln_bf16_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
-                        const LnParams p) {
+                        const __grid_constant__ CUtensorMap tx, const LnParams p) {
     constexpr int STAGES = LnCfg<BN>::kStages;
     constexpr uint32_t kBBytes = LnCfg<BN>::kBBytes;
     extern __shared__ uint8_t smem_raw[];
@@ -122,6 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sm.empty[i], 1);
         }
         mbar_init(&sm.acc_full, 1);
+        mbar_init(&sm.x_full, 1);
         mbar_init(&sm.drain, 1);
         sm.abort_flag = 0;
         fence_barrier_init();
@@ -133,6 +148,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&ta);
         prefetch_tensormap(&tb);
+        prefetch_tensormap(&tx);
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -152,6 +168,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
+            mbar_arrive_expect_tx(&sm.x_full, (BN / 64) * kXBox);
+#pragma unroll
+            for (int bx = 0; bx < BN / 64; ++bx)
+                tma_load_2d(&tx, &sm.x_full, sm.xs[bx], n_base + 64 * bx, tm * BM);
             int issued = 0;
             for (int kb = 0; kb < num_k; ++kb) {
                 const int st = kb % STAGES;
@@ -163,6 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             for (int x = max(0, issued - STAGES); x < issued; ++x)
                 mbar_wait_drain(&sm.full[x % STAGES], (x / STAGES) & 1);
+            mbar_wait_drain(&sm.x_full, 0);
         }
     } else if (warp == 1) {
         // ----------------------------------------------------- MMA issuer
@@ -187,11 +208,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_drain(&sm.drain, 0);
     } else {
         // ----------------------------------------- epilogue pass 1: row sums
-        ok = __all_sync(0xffffffffu, mbar_wait(&sm.acc_full, 0, ab));
+        ok = __all_sync(0xffffffffu, mbar_wait(&sm.acc_full, 0, ab)) &&
+             __all_sync(0xffffffffu, mbar_wait(&sm.x_full, 0, ab));
         float s1 = 0.f;
         if (ok) {
             tc_fence_after_sync();
-            const __nv_bfloat16 *xr = p.resid + static_cast<long long>(m) * p.D + n_base;
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t acc[32];
@@ -202,7 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         float xf[8];
-                        bf16x8(*reinterpret_cast<const uint4 *>(xr + 32 * c + 8 * q), xf);
+                        bf16x8(x_chunk(sm, r, 4 * c + q), xf);
                         add_bias(xf, p.bias, n_base + 32 * c + 8 * q);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) s1 += __uint_as_float(acc[8 * q + e]) + xf[e];
@@ -224,7 +245,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // `ok` is warp-uniform; every lane issues the tensor-memory loads
         // (rows past M included) and only the arithmetic depends on the row.
         if (ok) {
-            const __nv_bfloat16 *xr = p.resid + static_cast<long long>(m) * p.D + n_base;
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t acc[32];
@@ -235,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         float xf[8];
-                        bf16x8(*reinterpret_cast<const uint4 *>(xr + 32 * c + 8 * q), xf);
+                        bf16x8(x_chunk(sm, r, 4 * c + q), xf);
                         add_bias(xf, p.bias, n_base + 32 * c + 8 * q);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
@@ -257,7 +277,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = 0; q < csize; ++q) tot += dsmem_ld_f32(&sm.part[1][r], static_cast<uint32_t>(q));
         const float rstd = rsqrtf(tot / static_cast<float>(p.D) + p.eps);
         if (ok) {
-            const __nv_bfloat16 *xr = p.resid + static_cast<long long>(m) * p.D + n_base;
             __nv_bfloat16 *yr = p.out + static_cast<long long>(m) * p.D + n_base;
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
@@ -269,7 +288,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     float xf[8], gf[8], bf[8];
-                    bf16x8(*reinterpret_cast<const uint4 *>(xr + 32 * c + 8 * q), xf);
+                    bf16x8(x_chunk(sm, r, 4 * c + q), xf);
                     add_bias(xf, p.bias, n_base + 32 * c + 8 * q);
                     bf16x8(*reinterpret_cast<const uint4 *>(p.gamma + n_base + 32 * c + 8 * q), gf);
                     bf16x8(*reinterpret_cast<const uint4 *>(p.beta + n_base + 32 * c + 8 * q), bf);
@@ -300,8 +319,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 template <int BN>
-cudaError_t launch_bn(const CUtensorMap &a, const CUtensorMap &b, const LnParams &p,
-                      cudaStream_t stream) {
+cudaError_t launch_bn(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &x,
+                      const LnParams &p, cudaStream_t stream) {
     const size_t smem = sizeof(SmemLn<BN>) + 1024;
     cudaError_t e = cudaFuncSetAttribute(gemm_ln_bf16_kernel<BN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -321,7 +340,7 @@ cudaError_t launch_bn(const CUtensorMap &a, const CUtensorMap &b, const LnParams
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_ln_bf16_kernel<BN>, a, b, p);
+    return cudaLaunchKernelEx(&cfg, gemm_ln_bf16_kernel<BN>, a, b, x, p);
 }
 
 }  // namespace
@@ -339,11 +358,11 @@ int ln_tile_width(int D, long long M, int sms) {
     return 0;
 }
 
-cudaError_t launch_gemm_ln_bf16(const CUtensorMap &a, const CUtensorMap &b, const LnParams &p,
-                                cudaStream_t stream) {
+cudaError_t launch_gemm_ln_bf16(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &x,
+                                const LnParams &p, cudaStream_t stream) {
     if (p.M <= 0) return cudaSuccess;
-    if (p.bn == 256) return launch_bn<256>(a, b, p, stream);
-    if (p.bn == 128) return launch_bn<128>(a, b, p, stream);
+    if (p.bn == 256) return launch_bn<256>(a, b, x, p, stream);
+    if (p.bn == 128) return launch_bn<128>(a, b, x, p, stream);
     return cudaErrorInvalidValue;
 }
 
