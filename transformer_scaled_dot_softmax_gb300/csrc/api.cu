@@ -585,11 +585,12 @@ mha_status mha_impl(mha_dtype dt, const void *x_q, const void *x_kv, const void 
         lp.eps = ln->eps;
         lp.out = static_cast<__nv_bfloat16 *>(out);
         lp.status = status_dev;
-        CUtensorMap la, lb, lx;
+        CUtensorMap la, lb, lx, ly;
         if ((s = encode_act(&la, om, Mq, hd)) != MHA_OK) return s;
         if ((s = encode_weight(&lb, w_o, hd, d_model, lp.bn)) != MHA_OK) return s;
         if ((s = encode_act(&lx, x_q, Mq, d_model)) != MHA_OK) return s;
-        return launch_status(mha::launch_gemm_ln_bf16(la, lb, lx, lp, stream),
+        if ((s = encode_act(&ly, lp.out, Mq, d_model)) != MHA_OK) return s;
+        return launch_status(mha::launch_gemm_ln_bf16(la, lb, lx, ly, lp, stream),
                              "output projection + layer norm launch");
     }
     mha::GemmParams go{};
@@ -725,11 +726,12 @@ MHA_EXPORT mha_status encoder_layer_forward(
     lp.eps = eps;
     lp.out = static_cast<__nv_bfloat16 *>(out);
     lp.status = status_dev;
-    CUtensorMap la, lb, lx;
+    CUtensorMap la, lb, lx, ly;
     if ((s = encode_act(&la, hid, M, d_ff)) != MHA_OK) return s;
     if ((s = encode_weight(&lb, w2, d_ff, d_model, lp.bn)) != MHA_OK) return s;
     if ((s = encode_act(&lx, y1, M, d_model)) != MHA_OK) return s;
-    return launch_status(mha::launch_gemm_ln_bf16(la, lb, lx, lp, stream),
+    if ((s = encode_act(&ly, lp.out, M, d_model)) != MHA_OK) return s;
+    return launch_status(mha::launch_gemm_ln_bf16(la, lb, lx, ly, lp, stream),
                          "feed-forward output + layer norm launch");
 }
 

@@ -25,10 +25,13 @@
 //               accumulator (x read from shared memory: 16-byte chunk j of row
 //               r at j ^ (r % 8), no bank conflicts): (1) v = acc + x, row sum;
 //               (2) sum of (v - mu)^2;
-//               (3) normalise, scale, shift, store bf16.  After (1) and (2) the
-//               CTAs of the cluster exchange their per-row partial sums through
-//               distributed shared memory, so mean and variance are exact
-//               two-pass statistics over the whole row.
+//               (3) normalise, scale, shift, bf16 over the residual block in
+//               shared memory, which one thread then stores with TMA (a
+//               thread's own row is 32 scattered 16-byte stores otherwise).
+//               After (1) and (2) the CTAs of the cluster exchange their
+//               per-row partial sums through distributed shared memory, so
+//               mean and variance are exact two-pass statistics over the whole
+//               row.
 //
 // Every thread of every CTA passes the same three cluster barriers, whatever
 // its role and whether a bounded wait ran out, so no CTA can be left waiting.
@@ -58,6 +61,9 @@ struct __align__(1024) SmemLn {
     uint8_t a[STAGES][kABytes];
     uint8_t b[STAGES][LnCfg<BN>::kBBytes];
     uint8_t xs[BN / 64][kXBox];  // residual block, 64 features per box
+    __nv_bfloat16 gamma[BN];     // this CTA's columns of gamma, beta and the bias
+    __nv_bfloat16 beta[BN];
+    __nv_bfloat16 bias[BN];
     float part[2][BM];  // this CTA's per-row partial: [0] sum of v, [1] sum of (v - mu)^2
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
@@ -99,14 +105,15 @@ __device__ __forceinline__ void bf16x8(const uint4 &u, float (&f)[8]) {
 // Eight residual features [8j', 8j'+8) of row r, j' = column / 8 within the
 // block: box j'/8, chunk j' % 8 swizzled with the row.
 template <int BN>
-__device__ __forceinline__ uint4 x_chunk(const SmemLn<BN> &sm, int r, int j) {
-    return *reinterpret_cast<const uint4 *>(sm.xs[j >> 3] + r * 128 + (((j & 7) ^ (r & 7)) << 4));
+__device__ __forceinline__ uint4 *x_chunk(SmemLn<BN> &sm, int r, int j) {
+    return reinterpret_cast<uint4 *>(sm.xs[j >> 3] + r * 128 + (((j & 7) ^ (r & 7)) << 4));
 }
 
-// x[0..7] += bias[n .. n+7] (bf16), if there is a bias: the residual and the
-// sublayer's output bias enter the row together.
-__device__ __forceinline__ void add_bias(float (&x)[8], const __nv_bfloat16 *bias, int n) {
-    if (!bias) return;
+// x[0..7] += bias[n .. n+7] (bf16, this CTA's columns in shared memory), if
+// there is a bias: the residual and the sublayer's output bias enter the row
+// together.
+__device__ __forceinline__ void add_bias(float (&x)[8], bool has_bias, const __nv_bfloat16 *bias, int n) {
+    if (!has_bias) return;
     float b[8];
     bf16x8(*reinterpret_cast<const uint4 *>(bias + n), b);
 #pragma unroll
@@ -116,7 +123,8 @@ __device__ __forceinline__ void add_bias(float (&x)[8], const __nv_bfloat16 *bia
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_ln_bf16_kernel(const __grid_constant__ CUtensorMap ta, const __grid_constant__ CUtensorMap tb,
-                        const __grid_constant__ CUtensorMap tx, const LnParams p) {
+                        const __grid_constant__ CUtensorMap tx, const __grid_constant__ CUtensorMap ty,
+                        const LnParams p) {
     constexpr int STAGES = LnCfg<BN>::kStages;
     constexpr uint32_t kBBytes = LnCfg<BN>::kBBytes;
     extern __shared__ uint8_t smem_raw[];
@@ -149,6 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         prefetch_tensormap(&ta);
         prefetch_tensormap(&tb);
         prefetch_tensormap(&tx);
+        prefetch_tensormap(&ty);
     }
     tc_fence_before_sync();
     __syncthreads();
@@ -162,6 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int m = tm * BM + r;
     const bool row_ok = m < p.M;
     const bool epi = warp >= 2;
+    const bool has_bias = p.bias != nullptr;
     bool ok = true;
     float mu = 0.f;
 
@@ -207,6 +217,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         warp_commit(&sm.drain);
         mbar_wait_drain(&sm.drain, 0);
     } else {
+        // The CTA's columns of gamma, beta (and the bias) into shared memory
+        // while the products run (every (c, q) step of the passes below reads
+        // a new 16-byte piece of each).
+        for (int i = threadIdx.x - 64; i < BN / 8; i += 128) {
+            reinterpret_cast<uint4 *>(sm.gamma)[i] = reinterpret_cast<const uint4 *>(p.gamma + n_base)[i];
+            reinterpret_cast<uint4 *>(sm.beta)[i] = reinterpret_cast<const uint4 *>(p.beta + n_base)[i];
+            if (has_bias) reinterpret_cast<uint4 *>(sm.bias)[i] = reinterpret_cast<const uint4 *>(p.bias + n_base)[i];
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
         // ----------------------------------------- epilogue pass 1: row sums
         ok = __all_sync(0xffffffffu, mbar_wait(&sm.acc_full, 0, ab)) &&
              __all_sync(0xffffffffu, mbar_wait(&sm.x_full, 0, ab));
@@ -223,8 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         float xf[8];
-                        bf16x8(x_chunk(sm, r, 4 * c + q), xf);
-                        add_bias(xf, p.bias, n_base + 32 * c + 8 * q);
+                        bf16x8(*x_chunk(sm, r, 4 * c + q), xf);
+                        add_bias(xf, has_bias, sm.bias, 32 * c + 8 * q);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) s1 += __uint_as_float(acc[8 * q + e]) + xf[e];
                     }
@@ -255,8 +274,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         float xf[8];
-                        bf16x8(x_chunk(sm, r, 4 * c + q), xf);
-                        add_bias(xf, p.bias, n_base + 32 * c + 8 * q);
+                        bf16x8(*x_chunk(sm, r, 4 * c + q), xf);
+                        add_bias(xf, has_bias, sm.bias, 32 * c + 8 * q);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
                             const float d = __uint_as_float(acc[8 * q + e]) + xf[e] - mu;
@@ -277,21 +296,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int q = 0; q < csize; ++q) tot += dsmem_ld_f32(&sm.part[1][r], static_cast<uint32_t>(q));
         const float rstd = rsqrtf(tot / static_cast<float>(p.D) + p.eps);
         if (ok) {
-            __nv_bfloat16 *yr = p.out + static_cast<long long>(m) * p.D + n_base;
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t acc[32];
                 __syncwarp();
                 tmem_ld32(tmem_addr(tmem, lane_base, 32u * c), acc);
                 tmem_ld_wait(acc);
-                if (!row_ok) continue;  // nothing below is warp-collective
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
+                    uint4 *xy = x_chunk(sm, r, 4 * c + q);  // x in, y out (same row, same chunk)
                     float xf[8], gf[8], bf[8];
-                    bf16x8(x_chunk(sm, r, 4 * c + q), xf);
-                    add_bias(xf, p.bias, n_base + 32 * c + 8 * q);
-                    bf16x8(*reinterpret_cast<const uint4 *>(p.gamma + n_base + 32 * c + 8 * q), gf);
-                    bf16x8(*reinterpret_cast<const uint4 *>(p.beta + n_base + 32 * c + 8 * q), bf);
+                    bf16x8(*xy, xf);
+                    add_bias(xf, has_bias, sm.bias, 32 * c + 8 * q);
+                    bf16x8(*reinterpret_cast<const uint4 *>(sm.gamma + 32 * c + 8 * q), gf);
+                    bf16x8(*reinterpret_cast<const uint4 *>(sm.beta + 32 * c + 8 * q), bf);
                     uint32_t packed[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -301,10 +319,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                                           mu) * rstd * gf[2 * e + 1] + bf[2 * e + 1];
                         packed[e] = pack_bf16x2(y0, y1);
                     }
-                    *reinterpret_cast<uint4 *>(yr + 32 * c + 8 * q) =
-                        make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                    *xy = make_uint4(packed[0], packed[1], packed[2], packed[3]);
                 }
             }
+        }
+        // The block in shared memory is complete: one thread stores it (rows
+        // past M are clipped by the tensor map), unless a wait ran out.
+        fence_proxy_async_smem();
+        __syncwarp();
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
+        if (warp == 2 && lane == 0) {
+            if (!*ab.cta_flag) {
+#pragma unroll
+                for (int bx = 0; bx < BN / 64; ++bx) tma_store_2d(&ty, sm.xs[bx], n_base + 64 * bx, tm * BM);
+                bulk_commit_group();
+            }
+            bulk_wait_all();
         }
     }
 
@@ -320,7 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int BN>
 cudaError_t launch_bn(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &x,
-                      const LnParams &p, cudaStream_t stream) {
+                      const CUtensorMap &y, const LnParams &p, cudaStream_t stream) {
     const size_t smem = sizeof(SmemLn<BN>) + 1024;
     cudaError_t e = cudaFuncSetAttribute(gemm_ln_bf16_kernel<BN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -340,7 +370,7 @@ cudaError_t launch_bn(const CUtensorMap &a, const CUtensorMap &b, const CUtensor
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_ln_bf16_kernel<BN>, a, b, x, p);
+    return cudaLaunchKernelEx(&cfg, gemm_ln_bf16_kernel<BN>, a, b, x, y, p);
 }
 
 }  // namespace
@@ -359,10 +389,10 @@ int ln_tile_width(int D, long long M, int sms) {
 }
 
 cudaError_t launch_gemm_ln_bf16(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &x,
-                                const LnParams &p, cudaStream_t stream) {
+                                const CUtensorMap &y, const LnParams &p, cudaStream_t stream) {
     if (p.M <= 0) return cudaSuccess;
-    if (p.bn == 256) return launch_bn<256>(a, b, x, p, stream);
-    if (p.bn == 128) return launch_bn<128>(a, b, x, p, stream);
+    if (p.bn == 256) return launch_bn<256>(a, b, x, y, p, stream);
+    if (p.bn == 128) return launch_bn<128>(a, b, x, y, p, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -126,9 +126,9 @@ struct LnParams {
 // M rows on `sms` SMs, or 0 if D is not supported.
 int ln_tile_width(int D, long long M, int sms);
 // a: 2-D TMA map over A (K inner, M rows), box (64, 128); b: 3-D map over W
-// viewed as (64, K, D/64), box (64, 64, bn/64); x: 2-D map over the residual
-// (D inner, M rows), box (64, 128).
+// viewed as (64, K, D/64), box (64, 64, bn/64); x, y: 2-D maps over the
+// residual and the output (D inner, M rows), box (64, 128).
 cudaError_t launch_gemm_ln_bf16(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &x,
-                                const LnParams &p, cudaStream_t stream);
+                                const CUtensorMap &y, const LnParams &p, cudaStream_t stream);
 
 }  // namespace mha

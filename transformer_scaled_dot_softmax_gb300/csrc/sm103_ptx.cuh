@@ -152,6 +152,27 @@ __device__ __forceinline__ void tma_load_3d(const CUtensorMap *map, uint64_t *ba
         : "memory");
 }
 
+// Tiled bulk store of a shared-memory box to global memory (coordinates
+// innermost first, never negative; rows outside the tensor are not written),
+// in the calling thread's bulk group.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void *src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(smem_u32(src)), "r"(x), "r"(y)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit_group() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// This thread's bulk groups have completed (their writes are performed).
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+// The shared-memory sources of this thread's bulk groups have been read.
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // Untiled bulk copy of `bytes` (a multiple of 16; both addresses 16-byte
 // aligned) from global to shared memory, completing on `bar`.
 __device__ __forceinline__ void bulk_load_1d(void *dst, const void *src, uint32_t bytes,
