@@ -38,7 +38,9 @@ def bf16_host(bits, pinned):
 # lengths that span several tiles, cross attention.
 CASES = [(2, 16, 200, 200, si.MASK_CAUSAL), (3, 5, 130, 257, si.MASK_KEY_PADDING),
          (8, 1, 64, 64, si.MASK_NONE), (1, 9, 300, 300, si.MASK_CAUSAL_KEY_PADDING),
-         (2, 3, 129, 1000, si.MASK_NONE)]
+         (2, 3, 129, 1000, si.MASK_NONE),
+         # longer causal sequences, with and without padding
+         (2, 3, 1000, 1000, si.MASK_CAUSAL), (1, 4, 1024, 1024, si.MASK_CAUSAL_KEY_PADDING)]
 
 
 @pytest.mark.parametrize("pinned", [True, False])
