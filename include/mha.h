@@ -118,7 +118,7 @@ mha_status sdpa_forward_lse(mha_dtype dt, const void *q, const void *k, const vo
  * caller (the device copies of q, k, v, o and key_lens).  key_lens: HOST
  * int32 array of B entries (key-padding masks only).
  *
- * The heads are taken in up to 8 chunks (groups of heads of one batch item,
+ * The heads are taken in up to 6 chunks (groups of heads of one batch item,
  * or whole batch items): chunk i's host-to-device copies, its attention launch
  * on `stream` and its device-to-host copy of o are chained by events, the
  * copies run on two internal copy streams (created on first use, one pair per
