@@ -24,9 +24,11 @@
  *
  * Conventions shared by every entry point:
  *   - All tensor pointers are DEVICE pointers to caller-owned memory,
- *     row-major and contiguous.  The library never allocates, frees or
- *     synchronises; every launch is enqueued on `stream` (0 = legacy default
- *     stream) and the call returns immediately.
+ *     row-major and contiguous (sdpa_forward_host alone takes host tensors).
+ *     The library never allocates device memory, frees or synchronises
+ *     (sdpa_forward_host keeps two copy streams and a few events per device);
+ *     every launch is enqueued on `stream` (0 = legacy default stream) and the
+ *     call returns immediately.
  *   - Argument errors are detected on the host before anything is enqueued
  *     and returned synchronously (nothing is launched).  A failed launch
  *     returns MHA_ERR_CUDA.
