@@ -120,6 +120,23 @@ bool valid_mask(int mask) { return mask >= MHA_MASK_NONE && mask <= MHA_MASK_CAU
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
+// Output map of a projection problem for the GEMM's TMA-store epilogue: 2-D
+// over a row-major output, 3-D (64, T, B*H) over a head-split one whose T is a
+// multiple of 128 (a 128-row tile then lies in one batch entry).  Sets
+// pr.tma_store; a head-split output with another T is stored row by row.
+mha_status encode_out(CUtensorMap *m, mha::GemmProblem &pr) {
+    pr.tma_store = 0;
+    mha_status s = MHA_OK;
+    if (pr.out_mode == mha::kOutHeadSplit) {
+        if (pr.T <= 0 || pr.T % mha::kGemmBM != 0) return MHA_OK;
+        s = encode_heads(m, pr.out, static_cast<long long>(pr.M / pr.T) * pr.H, pr.T);
+    } else {
+        s = encode_act(m, pr.out, pr.M, pr.N);
+    }
+    if (s == MHA_OK) pr.tma_store = 1;
+    return s;
+}
+
 mha_status launch_status(cudaError_t e, const char *what) {
     if (e == cudaSuccess) return MHA_OK;
     return cuda_fail(what, cudaGetErrorName(e));
@@ -521,7 +538,7 @@ mha_status mha_impl(mha_dtype dt, const void *x_q, const void *x_kv, const void 
         return cuda_fail("cudaDeviceGetAttribute", "SM count");
 
     // 1. Q, K, V projections with the head split folded into the epilogue.
-    CUtensorMap ta[mha::kGemmMaxProblems], tb[mha::kGemmMaxProblems];
+    CUtensorMap ta[mha::kGemmMaxProblems], tb[mha::kGemmMaxProblems], ty[mha::kGemmMaxProblems] = {};
     mha::GemmParams gp{};
     gp.status = status_dev;
     mha_status s;
@@ -552,16 +569,18 @@ mha_status mha_impl(mha_dtype dt, const void *x_q, const void *x_kv, const void 
         pr.out_mode = mha::kOutHeadSplit;
         pr.T = ins[i].T;
         pr.H = h;
+        if ((s = encode_out(&ty[np], pr)) != MHA_OK) return s;
         tiles += pr.tile_count;
         ++np;
     }
     for (int i = np; i < mha::kGemmMaxProblems; ++i) {
         ta[i] = ta[0];
         tb[i] = tb[0];
+        ty[i] = ty[0];
     }
     gp.num_problems = np;
     gp.total_tiles = tiles;
-    if ((s = launch_status(mha::launch_gemm_bf16(ta, tb, gp, stream), "projection GEMM launch")) !=
+    if ((s = launch_status(mha::launch_gemm_bf16(ta, tb, ty, gp, stream), "projection GEMM launch")) !=
         MHA_OK)
         return s;
 
@@ -598,10 +617,6 @@ mha_status mha_impl(mha_dtype dt, const void *x_q, const void *x_kv, const void 
     go.bn = choose_bn(&Mq, 1, d_model, sms);
     if ((s = encode_act(&ta[0], om, Mq, hd)) != MHA_OK) return s;
     if ((s = encode_weight(&tb[0], w_o, hd, d_model, go.bn)) != MHA_OK) return s;
-    for (int i = 1; i < mha::kGemmMaxProblems; ++i) {
-        ta[i] = ta[0];
-        tb[i] = tb[0];
-    }
     mha::GemmProblem &pr = go.prob[0];
     pr.M = static_cast<int>(Mq);
     pr.N = d_model;
@@ -613,9 +628,15 @@ mha_status mha_impl(mha_dtype dt, const void *x_q, const void *x_kv, const void 
     pr.out_mode = mha::kOutRowMajor;
     pr.T = T_q;
     pr.H = h;
+    if ((s = encode_out(&ty[0], pr)) != MHA_OK) return s;
+    for (int i = 1; i < mha::kGemmMaxProblems; ++i) {
+        ta[i] = ta[0];
+        tb[i] = tb[0];
+        ty[i] = ty[0];
+    }
     go.num_problems = 1;
     go.total_tiles = pr.tile_count;
-    return launch_status(mha::launch_gemm_bf16(ta, tb, go, stream), "output GEMM launch");
+    return launch_status(mha::launch_gemm_bf16(ta, tb, ty, go, stream), "output GEMM launch");
 }
 
 }  // namespace
@@ -687,16 +708,12 @@ MHA_EXPORT mha_status encoder_layer_forward(
         return cuda_fail("cudaDeviceGetAttribute", "SM count");
     const long long M = static_cast<long long>(rows);
     // 2. hid = max(0, y1 W1 + b1): projection GEMM with a bias + ReLU epilogue.
-    CUtensorMap ta[mha::kGemmMaxProblems], tb[mha::kGemmMaxProblems];
+    CUtensorMap ta[mha::kGemmMaxProblems], tb[mha::kGemmMaxProblems], ty[mha::kGemmMaxProblems] = {};
     mha::GemmParams gp{};
     gp.status = status_dev;
     gp.bn = choose_bn(&M, 1, d_ff, sms);
     if ((s = encode_act(&ta[0], y1, M, d_model)) != MHA_OK) return s;
     if ((s = encode_weight(&tb[0], w1, d_model, d_ff, gp.bn)) != MHA_OK) return s;
-    for (int i = 1; i < mha::kGemmMaxProblems; ++i) {
-        ta[i] = ta[0];
-        tb[i] = tb[0];
-    }
     mha::GemmProblem &pr = gp.prob[0];
     pr.M = static_cast<int>(M);
     pr.N = d_ff;
@@ -708,9 +725,15 @@ MHA_EXPORT mha_status encoder_layer_forward(
     pr.out_mode = mha::kOutRowMajor;
     pr.bias = static_cast<const __nv_bfloat16 *>(b1);
     pr.relu = 1;
+    if ((s = encode_out(&ty[0], pr)) != MHA_OK) return s;
+    for (int i = 1; i < mha::kGemmMaxProblems; ++i) {
+        ta[i] = ta[0];
+        tb[i] = tb[0];
+        ty[i] = ty[0];
+    }
     gp.num_problems = 1;
     gp.total_tiles = pr.tile_count;
-    if ((s = launch_status(mha::launch_gemm_bf16(ta, tb, gp, stream), "feed-forward GEMM launch")) !=
+    if ((s = launch_status(mha::launch_gemm_bf16(ta, tb, ty, gp, stream), "feed-forward GEMM launch")) !=
         MHA_OK)
         return s;
     // 3. out = LayerNorm2(y1 + hid W2 + b2): the normalising GEMM with a bias.

@@ -23,12 +23,17 @@
 //               output columns (96 instead of 128 bytes per cycle at the
 //               tensor rate).
 //   warps 2-5   epilogue: tensor memory -> registers (the buffer is handed
-//               back as soon as it is read) -> [+ bias, ReLU] -> bf16 ->
-//               global.  In head-split
-//               mode column n = head*64 + c of row m = b*T + t is stored at
-//               ((b*H + head)*T + t)*64 + c, i.e. straight into the
-//               (B, H, T, 64) layout attention reads -- the view/transpose of
-//               the head split costs no extra pass over memory.
+//               back as soon as it is read) -> [+ bias, ReLU] -> bf16 -> a
+//               128-byte swizzled 128 x 128 staging block in shared memory,
+//               which one thread stores with TMA (two 64-column boxes; rows
+//               and columns past the output are clipped), 128 columns at a
+//               time.  In head-split mode column n = head*64 + c of row
+//               m = b*T + t goes to ((b*H + head)*T + t)*64 + c, i.e. straight
+//               into the (B, H, T, 64) layout attention reads -- the
+//               view/transpose of the head split costs no extra pass over
+//               memory; the box is then (head, rows t0 .. t0+127 of batch b),
+//               so T must be a multiple of 128, else each thread stores its
+//               row directly.
 #include <cuda_bf16.h>
 
 #include "kernels.h"
@@ -41,6 +46,7 @@ constexpr int BM = kGemmBM, BK = kGemmBK;
 constexpr int kThreads = 192;
 constexpr uint32_t kABytes = BM * BK * 2;  // 16 KiB
 constexpr uint32_t kBBlock = BK * 64 * 2;  // 8 KiB: one 64-column block of a B tile
+constexpr uint32_t kYBox = BM * 128;       // 16 KiB: 128 rows x 64 output columns
 
 template <int BN>
 struct GemmCfg {
@@ -54,6 +60,7 @@ struct __align__(1024) SmemGemm {
     static constexpr int STAGES = GemmCfg<BN>::kStages;
     uint8_t a[STAGES][kABytes];
     uint8_t b[STAGES][GemmCfg<BN>::kBBytes];
+    uint8_t ys[2][kYBox];  // output staging: 128 columns, 128-byte swizzled
     uint64_t full[STAGES];
     uint64_t empty[STAGES];
     uint64_t acc_full[2];   // MMA -> epilogue (commit)
@@ -83,7 +90,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_bf16_kernel(const __grid_constant__ CUtensorMap a0, const __grid_constant__ CUtensorMap a1,
                      const __grid_constant__ CUtensorMap a2, const __grid_constant__ CUtensorMap b0,
                      const __grid_constant__ CUtensorMap b1, const __grid_constant__ CUtensorMap b2,
-                     const GemmParams p) {
+                     const __grid_constant__ CUtensorMap y0, const __grid_constant__ CUtensorMap y1,
+                     const __grid_constant__ CUtensorMap y2, const GemmParams p) {
     constexpr int STAGES = GemmCfg<BN>::kStages;
     constexpr uint32_t kBBytes = GemmCfg<BN>::kBBytes;
     constexpr uint32_t kTmemCols = GemmCfg<BN>::kTmemCols;
@@ -115,13 +123,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&a0);
         prefetch_tensormap(&b0);
+        if (p.prob[0].tma_store) prefetch_tensormap(&y0);
         if (p.num_problems > 1) {
             prefetch_tensormap(&a1);
             prefetch_tensormap(&b1);
+            if (p.prob[1].tma_store) prefetch_tensormap(&y1);
         }
         if (p.num_problems > 2) {
             prefetch_tensormap(&a2);
             prefetch_tensormap(&b2);
+            if (p.prob[2].tma_store) prefetch_tensormap(&y2);
         }
     }
     tc_fence_before_sync();
@@ -212,6 +223,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             } else {
                 row_off = static_cast<long long>(m) * pr.N;
             }
+            const CUtensorMap *ty = t.pi == 0 ? &y0 : (t.pi == 1 ? &y1 : &y2);
             // 128 columns at a time; after the last group the accumulator is
             // handed back (the MMA warp may start the tile after next in it).
 #pragma unroll 1
@@ -230,36 +242,49 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&sm.acc_empty[acc]);
                 }
-                if (m >= pr.M) continue;
+                if (pr.tma_store) {
+                    // the previous group's store has read the staging block
+                    if (warp == 2 && lane == 0) bulk_wait_read();
+                    asm volatile("bar.sync 1, 128;" ::: "memory");  // the four epilogue warps
+                }
+                const int rr = static_cast<int>(lane_base) + lane;  // row in the tile
 #pragma unroll
                 for (int c = 0; c < 4; ++c) {
                     const int n0 = t.tn * BN + grp * 128 + c * 32;
-                    if (n0 < pr.N) {
-                        uint32_t packed[16];
-                        if (pr.bias) {
-                            // bias (+ ReLU): the feed-forward network's first layer
+                    uint32_t packed[16];
+                    if (pr.bias && n0 < pr.N) {
+                        // bias (+ ReLU): the feed-forward network's first layer
 #pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                const uint4 bw = *reinterpret_cast<const uint4 *>(pr.bias + n0 + 8 * q);
-                                const uint32_t bb[4] = {bw.x, bw.y, bw.z, bw.w};
+                        for (int q = 0; q < 4; ++q) {
+                            const uint4 bw = *reinterpret_cast<const uint4 *>(pr.bias + n0 + 8 * q);
+                            const uint32_t bb[4] = {bw.x, bw.y, bw.z, bw.w};
 #pragma unroll
-                                for (int e = 0; e < 4; ++e) {
-                                    float y0 = __uint_as_float(r[c][8 * q + 2 * e]) + __uint_as_float(bb[e] << 16);
-                                    float y1 = __uint_as_float(r[c][8 * q + 2 * e + 1]) +
-                                               __uint_as_float(bb[e] & 0xffff0000u);
-                                    if (pr.relu) {
-                                        y0 = fmaxf(y0, 0.f);
-                                        y1 = fmaxf(y1, 0.f);
-                                    }
-                                    packed[4 * q + e] = pack_bf16x2(y0, y1);
+                            for (int e = 0; e < 4; ++e) {
+                                float v0 = __uint_as_float(r[c][8 * q + 2 * e]) + __uint_as_float(bb[e] << 16);
+                                float v1 = __uint_as_float(r[c][8 * q + 2 * e + 1]) +
+                                           __uint_as_float(bb[e] & 0xffff0000u);
+                                if (pr.relu) {
+                                    v0 = fmaxf(v0, 0.f);
+                                    v1 = fmaxf(v1, 0.f);
                                 }
+                                packed[4 * q + e] = pack_bf16x2(v0, v1);
                             }
-                        } else {
-#pragma unroll
-                            for (int q = 0; q < 16; ++q)
-                                packed[q] = pack_bf16x2(__uint_as_float(r[c][2 * q]),
-                                                        __uint_as_float(r[c][2 * q + 1]));
                         }
+                    } else {
+#pragma unroll
+                        for (int q = 0; q < 16; ++q)
+                            packed[q] = pack_bf16x2(__uint_as_float(r[c][2 * q]), __uint_as_float(r[c][2 * q + 1]));
+                    }
+                    if (pr.tma_store) {
+                        // 16-byte chunk j = 4c + q of the row: box j / 8, position
+                        // (j % 8) ^ (row % 8)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const int j = 4 * c + q;
+                            *reinterpret_cast<uint4 *>(sm.ys[j >> 3] + rr * 128 + (((j & 7) ^ (rr & 7)) << 4)) =
+                                make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+                        }
+                    } else if (m < pr.M && n0 < pr.N) {
                         __nv_bfloat16 *dst;
                         if (pr.out_mode == kOutHeadSplit) {
                             const int head = n0 >> 6, c0 = n0 & 63;
@@ -274,8 +299,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                packed[4 * q + 3]);
                     }
                 }
+                if (pr.tma_store) {
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    asm volatile("bar.sync 1, 128;" ::: "memory");
+                    if (warp == 2 && lane == 0) {
+#pragma unroll
+                        for (int bx = 0; bx < 2; ++bx) {
+                            const int nb = t.tn * BN + grp * 128 + 64 * bx;
+                            if (nb >= pr.N) break;
+                            if (pr.out_mode == kOutHeadSplit) {
+                                const int m0 = t.tm * BM, bb = m0 / pr.T;
+                                tma_store_3d(ty, sm.ys[bx], 0, m0 - bb * pr.T, bb * pr.H + (nb >> 6));
+                            } else {
+                                tma_store_2d(ty, sm.ys[bx], nb, t.tm * BM);
+                            }
+                        }
+                        bulk_commit_group();
+                    }
+                }
             }
         }
+        if (warp == 2 && lane == 0) bulk_wait_all();  // the last stores have landed
     }
 
     tc_fence_before_sync();
@@ -288,7 +333,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int BN>
 cudaError_t launch_bn(const CUtensorMap (&a)[kGemmMaxProblems],
-                      const CUtensorMap (&b)[kGemmMaxProblems], const GemmParams &p, int sms,
+                      const CUtensorMap (&b)[kGemmMaxProblems],
+                      const CUtensorMap (&y)[kGemmMaxProblems], const GemmParams &p, int sms,
                       cudaStream_t stream) {
     const size_t smem = sizeof(SmemGemm<BN>) + 1024;
     cudaError_t e = cudaFuncSetAttribute(gemm_bf16_kernel<BN>,
@@ -298,7 +344,8 @@ cudaError_t launch_bn(const CUtensorMap (&a)[kGemmMaxProblems],
     // One persistent CTA per SM (fewer if there are fewer tiles).
     const int grid = p.total_tiles < sms ? p.total_tiles : sms;
     if (grid <= 0) return cudaSuccess;
-    gemm_bf16_kernel<BN><<<grid, kThreads, smem, stream>>>(a[0], a[1], a[2], b[0], b[1], b[2], p);
+    gemm_bf16_kernel<BN><<<grid, kThreads, smem, stream>>>(a[0], a[1], a[2], b[0], b[1], b[2], y[0], y[1],
+                                                           y[2], p);
     return cudaGetLastError();
 }
 
@@ -312,13 +359,14 @@ cudaError_t sm_count(int *sms) {
 }
 
 cudaError_t launch_gemm_bf16(const CUtensorMap (&a)[kGemmMaxProblems],
-                             const CUtensorMap (&b)[kGemmMaxProblems], const GemmParams &p,
+                             const CUtensorMap (&b)[kGemmMaxProblems],
+                             const CUtensorMap (&y)[kGemmMaxProblems], const GemmParams &p,
                              cudaStream_t stream) {
     int sms = 0;
     cudaError_t e = sm_count(&sms);
     if (e != cudaSuccess) return e;
-    if (p.bn == 256) return launch_bn<256>(a, b, p, sms, stream);
-    if (p.bn == 128) return launch_bn<128>(a, b, p, sms, stream);
+    if (p.bn == 256) return launch_bn<256>(a, b, y, p, sms, stream);
+    if (p.bn == 128) return launch_bn<128>(a, b, y, p, sms, stream);
     return cudaErrorInvalidValue;
 }
 

@@ -90,6 +90,7 @@ struct GemmProblem {
     int T, H;
     const __nv_bfloat16 *bias;  // optional (N): added to every row
     int relu;                   // nonzero: max(0, .) after the bias
+    int tma_store;              // nonzero: the output goes out through its TMA map (y below)
 };
 struct GemmParams {
     int num_problems;
@@ -102,8 +103,12 @@ constexpr int kGemmBM = 128, kGemmBK = 64;
 
 // a[i]: 2-D TMA map over the activation (K inner, M rows), box (64, 128).
 // b[i]: 3-D TMA map over the weight viewed as (64, K, N/64), box (64, 64, bn/64).
+// y[i] (problems with tma_store): the output, 2-D (N inner, M rows) box (64, 128)
+// for row-major, 3-D (64, T, B*H) box (64, 128, 1) for head-split with T a
+// multiple of 128.
 cudaError_t launch_gemm_bf16(const CUtensorMap (&a)[kGemmMaxProblems],
-                             const CUtensorMap (&b)[kGemmMaxProblems], const GemmParams &p,
+                             const CUtensorMap (&b)[kGemmMaxProblems],
+                             const CUtensorMap (&y)[kGemmMaxProblems], const GemmParams &p,
                              cudaStream_t stream);
 
 // Number of SMs of the current device.
