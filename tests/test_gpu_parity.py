@@ -244,6 +244,11 @@ MHA_SMALL = [
     (2, 64, 64, 64, 1, si.MASK_CAUSAL_KEY_PADDING, False),
     # enough tiles for 128 x 256 projection tiles, with a ragged last row tile
     (3, 1000, 1000, 512, 8, si.MASK_CAUSAL, False),
+    # one projection launch whose Q output (T_q a multiple of 128) leaves by
+    # TMA tensor stores and whose K, V outputs (T_k not) by row stores; and
+    # both by tensor stores
+    (2, 128, 300, 256, 4, si.MASK_KEY_PADDING, True),
+    (1, 256, 128, 128, 2, si.MASK_NONE, True),
     (2, 700, 900, 512, 8, si.MASK_KEY_PADDING, True),
 ]
 
