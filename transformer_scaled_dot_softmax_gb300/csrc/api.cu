@@ -145,7 +145,8 @@ mha_status launch_status(cudaError_t e, const char *what) {
 mha_status run_attention_bf16(const void *q, const void *k, const void *v, void *o,
                               long long o_sb, long long o_sh, long long o_st, int B, int h,
                               int T_q, int T_k, float scale, int mask, const int32_t *key_lens,
-                              int *status_dev, cudaStream_t stream, float *lse = nullptr) {
+                              int *status_dev, cudaStream_t stream, float *lse = nullptr,
+                              bool pdl = false) {
     CUtensorMap tq, tk, tv;
     const long long BH = static_cast<long long>(B) * h;
     mha_status s;
@@ -174,7 +175,7 @@ mha_status run_attention_bf16(const void *q, const void *k, const void *v, void 
     if (items >= (1ll << 30)) return MHA_ERR_UNSUPPORTED;
     p.total_items = static_cast<int>(items);
     p.status = status_dev;
-    return launch_status(mha::launch_attn_bf16(tq, tk, tv, p, stream), "attention launch");
+    return launch_status(mha::launch_attn_bf16(tq, tk, tv, p, stream, pdl), "attention launch");
 }
 
 }  // namespace
@@ -587,7 +588,7 @@ mha_status mha_impl(mha_dtype dt, const void *x_q, const void *x_kv, const void 
     // 2. Fused attention, writing the merged (B, T_q, h*64) layout directly.
     if ((s = run_attention_bf16(qh, T_k > 0 ? kh : qh, T_k > 0 ? vh : qh, om,
                                 static_cast<long long>(T_q) * hd, 64, hd, B, h, T_q, T_k, scale,
-                                mask, key_lens, status_dev, stream)) != MHA_OK)
+                                mask, key_lens, status_dev, stream, nullptr, true)) != MHA_OK)
         return s;
 
     // 3. Output projection Concat(heads) W^O, alone or fused with the
@@ -609,7 +610,7 @@ mha_status mha_impl(mha_dtype dt, const void *x_q, const void *x_kv, const void 
         if ((s = encode_weight(&lb, w_o, hd, d_model, lp.bn)) != MHA_OK) return s;
         if ((s = encode_act(&lx, x_q, Mq, d_model)) != MHA_OK) return s;
         if ((s = encode_act(&ly, lp.out, Mq, d_model)) != MHA_OK) return s;
-        return launch_status(mha::launch_gemm_ln_bf16(la, lb, lx, ly, lp, stream),
+        return launch_status(mha::launch_gemm_ln_bf16(la, lb, lx, ly, lp, stream, true),
                              "output projection + layer norm launch");
     }
     mha::GemmParams go{};
@@ -636,7 +637,7 @@ mha_status mha_impl(mha_dtype dt, const void *x_q, const void *x_kv, const void 
     }
     go.num_problems = 1;
     go.total_tiles = pr.tile_count;
-    return launch_status(mha::launch_gemm_bf16(ta, tb, ty, go, stream), "output GEMM launch");
+    return launch_status(mha::launch_gemm_bf16(ta, tb, ty, go, stream, true), "output GEMM launch");
 }
 
 }  // namespace
@@ -733,7 +734,7 @@ MHA_EXPORT mha_status encoder_layer_forward(
     }
     gp.num_problems = 1;
     gp.total_tiles = pr.tile_count;
-    if ((s = launch_status(mha::launch_gemm_bf16(ta, tb, ty, gp, stream), "feed-forward GEMM launch")) !=
+    if ((s = launch_status(mha::launch_gemm_bf16(ta, tb, ty, gp, stream, true), "feed-forward GEMM launch")) !=
         MHA_OK)
         return s;
     // 3. out = LayerNorm2(y1 + hid W2 + b2): the normalising GEMM with a bias.
@@ -754,7 +755,7 @@ MHA_EXPORT mha_status encoder_layer_forward(
     if ((s = encode_weight(&lb, w2, d_ff, d_model, lp.bn)) != MHA_OK) return s;
     if ((s = encode_act(&lx, y1, M, d_model)) != MHA_OK) return s;
     if ((s = encode_act(&ly, lp.out, M, d_model)) != MHA_OK) return s;
-    return launch_status(mha::launch_gemm_ln_bf16(la, lb, lx, ly, lp, stream),
+    return launch_status(mha::launch_gemm_ln_bf16(la, lb, lx, ly, lp, stream, true),
                          "feed-forward output + layer norm launch");
 }
 

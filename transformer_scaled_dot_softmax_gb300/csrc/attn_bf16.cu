@@ -199,6 +199,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem = sm.tmem_base;
     const AbortState ab{&sm.abort_flag, p.status};
+    // Programmatic dependent launch: the next kernel may begin its prologue;
+    // nothing below touches global memory written by the kernel before this
+    // one until that kernel has completed.
+    pdl_launch_dependents();
+    pdl_wait();
 
     // Every role walks the same item list and counts, over the items that
     // have key tiles, the items (v: Q buffer v mod 2 and the per-item
@@ -586,7 +591,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t launch_attn_bf16(const CUtensorMap &tq, const CUtensorMap &tk,
-                             const CUtensorMap &tv, const AttnParams &p, cudaStream_t stream) {
+                             const CUtensorMap &tv, const AttnParams &p, cudaStream_t stream,
+                             bool pdl) {
     const size_t smem = sizeof(SmemAttn) + 1024;
     cudaError_t e = cudaFuncSetAttribute(attn_fwd_bf16_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -599,8 +605,7 @@ cudaError_t launch_attn_bf16(const CUtensorMap &tq, const CUtensorMap &tk,
         return e;
     const int grid = p.total_items < sms ? p.total_items : sms;
     if (grid <= 0) return cudaSuccess;
-    attn_fwd_bf16_kernel<<<grid, kThreads, smem, stream>>>(tq, tk, tv, p);
-    return cudaGetLastError();
+    return launch_kernel(attn_fwd_bf16_kernel, dim3(grid), dim3(kThreads), smem, stream, pdl, 1, tq, tk, tv, p);
 }
 
 }  // namespace mha

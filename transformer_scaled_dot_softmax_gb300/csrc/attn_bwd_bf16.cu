@@ -86,6 +86,7 @@ __device__ __forceinline__ long long dq_acc_index(long long bh, int Tq_pad, int 
 // feature group (coalesced accumulator reads).
 __global__ void attn_bwd_post(const float *__restrict__ dq_acc, __nv_bfloat16 *__restrict__ dq,
                               long long BH, int Tq, int Tq_pad, float scale) {
+    pdl_wait();  // the accumulator is complete once the main kernel is
     const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
     const long long grp = t >> 8;  // 32-row group over BH * Tq_pad / 32
     const int part = static_cast<int>((t >> 5) & 7);
@@ -261,6 +262,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem = sm.tmem_base;
     const AbortState ab{&sm.abort_flag, p.status};
+    // Programmatic dependent launch: the next kernel may begin its prologue;
+    // nothing below touches global memory written by the kernel before this
+    // one until that kernel has completed.
+    pdl_launch_dependents();
+    pdl_wait();
 
     if (warp == 0) {
         // -------------------------------------------------------------- TMA
@@ -526,14 +532,14 @@ cudaError_t launch_attn_bwd_bf16(const CUtensorMap &tq, const CUtensorMap &tk, c
                                  static_cast<int>(smem));
         if (e != cudaSuccess) return e;
         dim3 grid(static_cast<unsigned>(BH), static_cast<unsigned>((p.Tk + BKB - 1) / BKB));
-        attn_bwd_main<<<grid, kBwdThreads, smem, stream>>>(tq, tk, tv, tg, p);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if ((e = launch_kernel(attn_bwd_main, grid, dim3(kBwdThreads), smem, stream, true, 1, tq, tk, tv, tg, p)) !=
+            cudaSuccess)
+            return e;
     }
     const long long post_threads = p.Tq > 0 ? BH * p.Tq_pad * 8 : 0;
     if (post_threads == 0) return cudaSuccess;
-    attn_bwd_post<<<static_cast<unsigned>((post_threads + 255) / 256), 256, 0, stream>>>(
-        p.dq_acc, dq, BH, p.Tq, p.Tq_pad, p.scale);
-    return cudaGetLastError();
+    return launch_kernel(attn_bwd_post, dim3(static_cast<unsigned>((post_threads + 255) / 256)), dim3(256), 0,
+                         stream, true, 1, static_cast<const float *>(p.dq_acc), dq, BH, p.Tq, p.Tq_pad, p.scale);
 }
 
 }  // namespace mha

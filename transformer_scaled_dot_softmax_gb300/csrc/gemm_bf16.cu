@@ -140,6 +140,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem = sm.tmem_base;
     const AbortState ab{&sm.abort_flag, p.status};
+    // Programmatic dependent launch: the next kernel may begin its prologue;
+    // nothing below touches global memory written by the kernel before this
+    // one until that kernel has completed.
+    pdl_launch_dependents();
+    pdl_wait();
 
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
@@ -335,7 +340,7 @@ template <int BN>
 cudaError_t launch_bn(const CUtensorMap (&a)[kGemmMaxProblems],
                       const CUtensorMap (&b)[kGemmMaxProblems],
                       const CUtensorMap (&y)[kGemmMaxProblems], const GemmParams &p, int sms,
-                      cudaStream_t stream) {
+                      cudaStream_t stream, bool pdl) {
     const size_t smem = sizeof(SmemGemm<BN>) + 1024;
     cudaError_t e = cudaFuncSetAttribute(gemm_bf16_kernel<BN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -344,9 +349,8 @@ cudaError_t launch_bn(const CUtensorMap (&a)[kGemmMaxProblems],
     // One persistent CTA per SM (fewer if there are fewer tiles).
     const int grid = p.total_tiles < sms ? p.total_tiles : sms;
     if (grid <= 0) return cudaSuccess;
-    gemm_bf16_kernel<BN><<<grid, kThreads, smem, stream>>>(a[0], a[1], a[2], b[0], b[1], b[2], y[0], y[1],
-                                                           y[2], p);
-    return cudaGetLastError();
+    return launch_kernel(gemm_bf16_kernel<BN>, dim3(grid), dim3(kThreads), smem, stream, pdl, 1, a[0], a[1],
+                         a[2], b[0], b[1], b[2], y[0], y[1], y[2], p);
 }
 
 }  // namespace
@@ -361,12 +365,12 @@ cudaError_t sm_count(int *sms) {
 cudaError_t launch_gemm_bf16(const CUtensorMap (&a)[kGemmMaxProblems],
                              const CUtensorMap (&b)[kGemmMaxProblems],
                              const CUtensorMap (&y)[kGemmMaxProblems], const GemmParams &p,
-                             cudaStream_t stream) {
+                             cudaStream_t stream, bool pdl) {
     int sms = 0;
     cudaError_t e = sm_count(&sms);
     if (e != cudaSuccess) return e;
-    if (p.bn == 256) return launch_bn<256>(a, b, y, p, sms, stream);
-    if (p.bn == 128) return launch_bn<128>(a, b, y, p, sms, stream);
+    if (p.bn == 256) return launch_bn<256>(a, b, y, p, sms, stream, pdl);
+    if (p.bn == 128) return launch_bn<128>(a, b, y, p, sms, stream, pdl);
     return cudaErrorInvalidValue;
 }
 

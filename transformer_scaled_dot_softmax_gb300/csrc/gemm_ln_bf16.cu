@@ -164,6 +164,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem = sm.tmem_base;
     const AbortState ab{&sm.abort_flag, p.status};
+    // Programmatic dependent launch: the next kernel may begin its prologue;
+    // nothing below touches global memory written by the kernel before this
+    // one until that kernel has completed.
+    pdl_launch_dependents();
+    pdl_wait();
 
     // Epilogue state (warps 2-5): row of this thread and its statistics.
     const uint32_t lane_base = static_cast<uint32_t>(warp & 3) * 32;
@@ -350,7 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int BN>
 cudaError_t launch_bn(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &x,
-                      const CUtensorMap &y, const LnParams &p, cudaStream_t stream) {
+                      const CUtensorMap &y, const LnParams &p, cudaStream_t stream, bool pdl) {
     const size_t smem = sizeof(SmemLn<BN>) + 1024;
     cudaError_t e = cudaFuncSetAttribute(gemm_ln_bf16_kernel<BN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -358,19 +363,8 @@ cudaError_t launch_bn(const CUtensorMap &a, const CUtensorMap &b, const CUtensor
     if (e != cudaSuccess) return e;
     const int csize = p.D / BN;
     const int row_tiles = (p.M + BM - 1) / BM;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(row_tiles * csize));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = static_cast<unsigned>(csize);
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, gemm_ln_bf16_kernel<BN>, a, b, x, y, p);
+    return launch_kernel(gemm_ln_bf16_kernel<BN>, dim3(static_cast<unsigned>(row_tiles * csize)), dim3(kThreads),
+                         smem, stream, pdl, static_cast<unsigned>(csize), a, b, x, y, p);
 }
 
 }  // namespace
@@ -389,10 +383,10 @@ int ln_tile_width(int D, long long M, int sms) {
 }
 
 cudaError_t launch_gemm_ln_bf16(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &x,
-                                const CUtensorMap &y, const LnParams &p, cudaStream_t stream) {
+                                const CUtensorMap &y, const LnParams &p, cudaStream_t stream, bool pdl) {
     if (p.M <= 0) return cudaSuccess;
-    if (p.bn == 256) return launch_bn<256>(a, b, x, y, p, stream);
-    if (p.bn == 128) return launch_bn<128>(a, b, x, y, p, stream);
+    if (p.bn == 256) return launch_bn<256>(a, b, x, y, p, stream, pdl);
+    if (p.bn == 128) return launch_bn<128>(a, b, x, y, p, stream, pdl);
     return cudaErrorInvalidValue;
 }
 

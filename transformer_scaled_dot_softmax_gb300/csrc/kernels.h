@@ -11,6 +11,38 @@ namespace mha {
 constexpr int kMaskCausalBit = 1;
 constexpr int kMaskPaddingBit = 2;
 
+// ------------------------------------------------ launch helper
+// Launches `kernel` on `stream`.  With pdl the launch may begin while the
+// kernel before it on the stream finishes (programmatic dependent launch);
+// every kernel launched that way waits for its predecessor (pdl_wait) after
+// its prologue and before it touches global memory.  Optional cluster size.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t stream, bool pdl, unsigned cluster, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    if (cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = cluster;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // ------------------------------------------------ fused bf16 attention
 struct AttnParams {
     int B, H, Tq, Tk;
@@ -31,7 +63,8 @@ constexpr int kAttnHeadDim = 64;
 // q, k, v: head-split (B, H, T, 64) bf16 tensors described by 3-D TMA maps
 // over (64, T, B*H) with 128-byte swizzling and 128-row boxes.
 cudaError_t launch_attn_bf16(const CUtensorMap &tq, const CUtensorMap &tk,
-                             const CUtensorMap &tv, const AttnParams &p, cudaStream_t stream);
+                             const CUtensorMap &tv, const AttnParams &p, cudaStream_t stream,
+                             bool pdl = false);
 
 // ------------------------------------------------ bf16 decode attention
 constexpr int kDecodeMaxRows = 8;  // query rows per (b, h) in one decode call
@@ -109,7 +142,7 @@ constexpr int kGemmBM = 128, kGemmBK = 64;
 cudaError_t launch_gemm_bf16(const CUtensorMap (&a)[kGemmMaxProblems],
                              const CUtensorMap (&b)[kGemmMaxProblems],
                              const CUtensorMap (&y)[kGemmMaxProblems], const GemmParams &p,
-                             cudaStream_t stream);
+                             cudaStream_t stream, bool pdl = false);
 
 // Number of SMs of the current device.
 cudaError_t sm_count(int *sms);
@@ -134,6 +167,7 @@ int ln_tile_width(int D, long long M, int sms);
 // viewed as (64, K, D/64), box (64, 64, bn/64); x, y: 2-D maps over the
 // residual and the output (D inner, M rows), box (64, 128).
 cudaError_t launch_gemm_ln_bf16(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &x,
-                                const CUtensorMap &y, const LnParams &p, cudaStream_t stream);
+                                const CUtensorMap &y, const LnParams &p, cudaStream_t stream,
+                                bool pdl = false);
 
 }  // namespace mha

@@ -190,6 +190,18 @@ __device__ __forceinline__ void bulk_load_1d(void *dst, const void *src, uint32_
         : "memory");
 }
 
+// Programmatic dependent launch.  pdl_launch_dependents: the grid launched
+// after this one on the stream with programmatic serialisation may begin
+// (its prologue overlaps this grid's tail).  pdl_wait: waits until the grid
+// this one follows has completed and its memory operations are visible
+// (returns at once for a grid launched without programmatic serialisation).
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Makes this thread's generic-proxy writes to shared memory visible to the
 // async proxy (a tcgen05.mma that reads them as an operand).
 __device__ __forceinline__ void fence_proxy_async_smem() {
