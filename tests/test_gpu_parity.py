@@ -117,6 +117,40 @@ def test_bf16_sdpa_vs_oracle(lib, B, h, T_q, T_k, mask):
     check_bf16(host(out), ref, "B%d h%d Tq%d Tk%d mask%d" % (B, h, T_q, T_k, mask))
 
 
+def splits_by_tiles(T_q, T_k, causal):
+    """The launcher's choice of split between the attention kernel's two
+    softmax groups: alternate key tiles when a 128-row query tile has on
+    average 8 key tiles or more (key padding ignored), key halves of every
+    tile otherwise."""
+    nqb = -(-T_q // 128)
+    tiles = sum(-(-(min(T_k, (qb + 1) * 128, T_q) if causal else T_k) // 128) for qb in range(nqb))
+    return tiles >= 8 * nqb
+
+
+# Every mask under both splits, with ragged query and key tails.
+SPLIT_SHAPES = [
+    (1, 2, 2048, 2048, si.MASK_CAUSAL, True),
+    (2, 2, 640, 640, si.MASK_CAUSAL, False),
+    (1, 2, 1000, 900, si.MASK_NONE, True),
+    (2, 1, 300, 896, si.MASK_NONE, False),
+    (2, 2, 700, 1100, si.MASK_KEY_PADDING, True),
+    (2, 2, 513, 700, si.MASK_KEY_PADDING, False),
+    (2, 1, 2100, 2100, si.MASK_CAUSAL_KEY_PADDING, True),
+    (2, 2, 384, 384, si.MASK_CAUSAL_KEY_PADDING, False),
+]
+
+
+@pytest.mark.parametrize("B,h,T_q,T_k,mask,tiles", SPLIT_SHAPES)
+def test_bf16_both_key_splits(lib, B, h, T_q, T_k, mask, tiles):
+    assert splits_by_tiles(T_q, T_k, bool(mask & si.MASK_CAUSAL)) == tiles
+    w = si.WORKLOADS[4].replace(B=B, h=h, T_q=T_q, T_k=T_k, mask=mask, len_lo=1, len_hi=T_k,
+                                seed=23)
+    x = si.make_inputs(w)
+    out = run_sdpa_bf16(lib, w, x)
+    ref = oracle.sdpa(x["q"], x["k"], x["v"], scale=w.scale, mask=mask, key_lens=x["key_lens"])
+    check_bf16(host(out), ref, "B%d h%d Tq%d Tk%d mask%d tiles%d" % (B, h, T_q, T_k, mask, tiles))
+
+
 def test_config5_full_size_sampled_rows(lib):
     w = si.WORKLOADS[4]
     x = si.make_inputs(w)
@@ -173,22 +207,34 @@ def test_bf16_constant_values(lib):
     np.testing.assert_allclose(host(out), 1.5, rtol=0, atol=1.5 * 2 ** -7)
 
 
+@pytest.mark.parametrize("T", [1024, 2048])
 @pytest.mark.parametrize("mask", [si.MASK_NONE, si.MASK_CAUSAL])
 @pytest.mark.parametrize("profile", ["growing", "jump", "shrinking"])
-def test_bf16_reference_maximum_updates(lib, profile, mask):
+def test_bf16_reference_maximum_updates(lib, profile, mask, T):
     """Key tiles (128 keys) scaled so that a row's maximum score keeps growing
     (every tile by ~20 log2 units: the exact step runs tile after tile),
     jumps far enough that exponentials against the old maximum overflow
-    fp32, or only shrinks (the first maximum stays the reference)."""
-    w = si.WORKLOADS[4].replace(B=1, h=2, T_q=1024, T_k=1024, mask=mask, seed=36)
+    fp32, or only shrinks (the first maximum stays the reference).  Causal
+    T = 1024 runs the kernel's key-halves split, the other three its
+    alternate-tiles split (see splits_by_tiles).
+
+    Such scores make almost every row select one value row, so the output is
+    that row of V.  Values are halved (exact in bf16) to keep |v| <= 3: at
+    |out| in [4, 8) the bf16 output's half-ulp alone is 2^-6 = 0.0156, and
+    the bf16 rounding of the dominant weight (unit roundoff 2^-8) adds up to
+    2^-8 |v|, which together can pass the 2e-2 bound whatever the kernel's
+    arithmetic; with |v| <= 3 the two stay under 2^-7 + 3 * 2^-8 = 0.0195."""
+    w = si.WORKLOADS[4].replace(B=1, h=2, T_q=T, T_k=T, mask=mask, seed=36)
     x = si.make_inputs(w)
     nt = w.T_k // 128
     f = {"growing": [6 * j + 1 for j in range(nt)],
          "jump": [80 if j in (2, 5) else 1 for j in range(nt)],
          "shrinking": [6 * (nt - j) + 1 for j in range(nt)]}[profile]
     k = si.round_bf16(x["k"] * np.repeat(np.array(f, dtype=np.float64), 128)[None, None, :, None])
-    out = run_sdpa_bf16(lib, w, x, k=bf16_dev(si.f64_to_bf16_bits(k)))
-    ref = oracle.sdpa(x["q"], k, x["v"], scale=w.scale, mask=mask)
+    v = x["v"] * 0.5
+    assert np.abs(v).max() <= 3.0
+    out = run_sdpa_bf16(lib, w, x, k=bf16_dev(si.f64_to_bf16_bits(k)), v=bf16_dev(si.f64_to_bf16_bits(v)))
+    ref = oracle.sdpa(x["q"], k, v, scale=w.scale, mask=mask)
     check_bf16(host(out), ref, "%s mask%d" % (profile, mask))
 
 

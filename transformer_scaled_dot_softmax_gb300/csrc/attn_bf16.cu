@@ -19,29 +19,33 @@
 //               V_j together into a 5-stage ring (one barrier per stage).
 //   warp 9      issues S_j = Q K_j^T (tcgen05.mma kind::f16, M=128 N=128,
 //               fp32 accumulator in tensor memory).
-//   warps 10,11 issue O_A += P_A,j V_j and O_B += P_B,j V_j for key halves
-//               A = [0, 64) and B = [64, 128) of every tile (N = 64, A
-//               operand P read straight from tensor memory).
-//   warps 0-3   softmax over key half A, warps 4-7 over key half B: one
-//               thread per (query row = tensor-memory lane, half).  Each
-//               thread loads its 64 scores, applies the causal / key-padding
-//               mask in-tile (masked score = -inf, i.e. exactly zero weight:
-//               aiany.app Step 10; notebook chapter "Masked Attention in the
-//               Decoder"), keeps its own reference maximum m_h and sum l_h,
-//               and writes P_h = bf16(2^(s*c - m_h*c)) back over its scores.
+//   warps 10,11 issue O_A += P_g V_g for the even tiles g of the CTA and
+//               O_B += P_g V_g for the odd ones (M = 128, N = 64, K = 128 keys;
+//               A operand P read straight from tensor memory).
+//   warps 0-3   softmax of the even tiles (group A), warps 4-7 of the odd
+//               tiles (group B): one thread per query row (= tensor-memory
+//               lane) and tile, taking the 128 scores in two rounds of 64.
+//               Each thread applies the causal / key-padding mask in-tile
+//               (masked score = -inf, i.e. exactly zero weight: aiany.app
+//               Step 10; notebook chapter "Masked Attention in the Decoder"),
+//               keeps its group's reference maximum m_h and sum l_h, and
+//               writes P = bf16(2^(s*c - m_h*c)) back over the scores.
 //   warps 12-15 output: once an item's products are complete, combine the
-//               halves, normalise, store, and hand the accumulators back.
+//               two groups, normalise, store, and hand the accumulators back.
 //
-// Splitting the row over two halves with their own maxima, sums and
+// Splitting a row's keys between two groups with their own maxima, sums and
 // accumulators is exact: the output is
 //   out = (O_A 2^((m_A-M)c) + O_B 2^((m_B-M)c)) / (l_A 2^((m_A-M)c) + l_B 2^((m_B-M)c)),
-// M = max(m_A, m_B).  The halves never wait for each other inside the loop.
+// M = max(m_A, m_B).  The groups never wait for each other inside the loop.
+// Because they take alternate tiles, the two softmax warps that share a
+// sub-partition work one score tile apart instead of in lockstep, so one's
+// tensor-memory round trips overlap the other's exponentials.
 //
 // MMA issue: one thread can issue a tcgen05.mma only every ~50-80 cycles
 // when it runs alone inside `if (lane == 0)`, while an N = 64 product needs
 // ~32 cycles of tensor-core time; issued by an elected lane of a converged
 // warp with descriptors formed as base + constant, the rate matches the
-// tensor core.  Three issuing warps keep S and the two P.V halves
+// tensor core.  Three issuing warps keep S and the two groups' P.V products
 // independent of each other.
 //
 // Score tiles rotate through three tensor-memory buffers (global tile g of
@@ -49,11 +53,17 @@
 // ready and S_{g+2} is being computed.  Issuers are ordered only through
 // barriers:
 //   S ready (per buffer)           S issuer -> softmax,
-//   P_h ready (per buffer, half)   softmax half h -> PV issuer h,
-//   stage released (count 2)      both PV issuers -> TMA producer, S issuer
-//                                  (S_g overwrites tile g-3's buffer, so it
-//                                  waits for tile g-3's release) and a
-//                                  softmax that must rescale O_h,
+//   P ready (per group, two deep)  softmax group h -> PV issuer h.  Each
+//                                  group counts its own tiles: a barrier
+//                                  shared by both groups would let one
+//                                  group's issuer mistake the other group's
+//                                  unfinished phase (parity one behind) for
+//                                  its own finished one,
+//   stage released                 the tile's PV issuer -> TMA producer, S
+//                                  issuer (S_g overwrites tile g-3's buffer,
+//                                  so it waits for tile g-3's release) and a
+//                                  softmax that must rescale O_h (its group's
+//                                  previous tile, g-2),
 //   Q released (per Q buffer)      S issuer -> TMA producer,
 //   output final (count 2)         both PV issuers -> output warps,
 //   row statistics (count 8)      softmax -> output warps, and back,
@@ -61,17 +71,21 @@
 // A buffer's next use needs its current use to be consumed, so no barrier
 // can run two phases ahead of its waiter.
 //
-// No maximum pass per tile: a tile is exponentiated against the half's
-// current reference maximum (softmax is shift-invariant, so any reference
-// that keeps the exponentials finite gives the same result), and only a row
-// whose tile sum exceeds 2^16 -- its maximum grew by 10 to 16 log2 units or
-// more -- or that has no reference yet takes the exact step (tile maximum,
-// O_h and l_h rescaled, P recomputed).  Decided per row.
+// No maximum pass per tile: each round of 64 scores is exponentiated against
+// the group's current reference maximum (softmax is shift-invariant, so any
+// reference that keeps the exponentials finite gives the same result), and
+// only a row whose round sum exceeds 2^16 -- its maximum grew by 10 to 16
+// log2 units or more -- or that has no reference yet takes the exact step
+// (round maximum, O_h, l_h and the tile's first-round P rescaled, P
+// recomputed).  Decided per row.
 //
 // Tensor memory (512 columns): S buffers [0,128), [128,256), [256,384);
-// O_A [384,448), O_B [448,512).  P_A sits in buffer columns [0,32) and P_B
-// in [64,96): each half writes over scores it has already read.
+// O_A [384,448), O_B [448,512).  P (128 keys, two per column) sits in buffer
+// columns [0,64): round 0 writes [0,32) over scores it has read, round 1
+// writes [32,64), also already read.
 #include <cuda_bf16.h>
+
+#include <algorithm>
 
 #include "kernels.h"
 #include "sm103_ptx.cuh"
@@ -88,7 +102,7 @@ constexpr int kThreads = 512;        // 8 softmax + load + 3 MMA + 4 output warp
 constexpr int kSoftmaxWarps = 8;
 constexpr int kLoadWarp = 8;
 constexpr int kMmaSWarp = 9;         // issues S = Q K^T
-constexpr int kMmaPvWarp = 10;       // warps 10, 11 issue PV for key halves A, B
+constexpr int kMmaPvWarp = 10;       // warps 10, 11 issue PV for the even / odd tiles
 constexpr int kOutWarp = 12;         // warps 12-15: output
 constexpr uint32_t kTileBytes = BM * HD * 2;  // 16 KiB, one 128 x 64 bf16 tile
 constexpr uint32_t kTmemCols = 512;
@@ -99,17 +113,17 @@ struct __align__(1024) SmemAttn {
     uint8_t q[2][kTileBytes];
     uint8_t k[STAGES][kTileBytes];
     uint8_t v[STAGES][kTileBytes];
-    float red_m[2][BM];  // [column half][row]: reference maximum at the end of an item
-    float red_l[2][BM];  // [column half][row]: row sum at the end of an item
+    float red_m[2][BM];  // [group][row]: reference maximum at the end of an item
+    float red_l[2][BM];  // [group][row]: row sum at the end of an item
     uint64_t q_full[2];
     uint64_t q_empty[2];
     uint64_t kv_full[STAGES];
     uint64_t kv_empty[STAGES];
     uint64_t s_full[kSBufs];
-    uint64_t p_full[kSBufs][2];  // [buffer][column half]
+    uint64_t p_full[kSBufs][2];  // P written (4 warps): [buffer][half] / [group tile mod 2][group]
     uint64_t ml_full;            // row statistics written (8 softmax warps)
     uint64_t ml_free;            // row statistics read (4 output warps)
-    uint64_t o_final;            // both P.V halves of an item complete
+    uint64_t o_final;            // both groups' P.V products of an item complete
     uint64_t o_free;             // accumulators read (4 output warps)
     uint64_t drain[3];           // one per MMA-issuing warp
     uint32_t tmem_base;
@@ -148,6 +162,7 @@ __device__ __forceinline__ Item make_item(const AttnParams &p, int k) {
     return it;
 }
 
+template <bool kTiles>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q,
                          const __grid_constant__ CUtensorMap tmap_k,
@@ -170,11 +185,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < STAGES; ++i) {
             mbar_init(&sm.kv_full[i], 1);
-            mbar_init(&sm.kv_empty[i], 2);  // one commit per PV issuer
+            mbar_init(&sm.kv_empty[i], kTiles ? 1 : 2);  // the tile's PV issuer(s)
         }
         for (int i = 0; i < kSBufs; ++i) {
             mbar_init(&sm.s_full[i], 1);
-            mbar_init(&sm.p_full[i][0], kSoftmaxWarps / 2);  // one arrival per warp of a half
+            mbar_init(&sm.p_full[i][0], kSoftmaxWarps / 2);
             mbar_init(&sm.p_full[i][1], kSoftmaxWarps / 2);
         }
         mbar_init(&sm.ml_full, kSoftmaxWarps);
@@ -293,17 +308,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_wait_drain(&sm.drain[0], 0);
     } else if (warp == kMmaPvWarp || warp == kMmaPvWarp + 1) {
         // ---------------------------------------------------- PV issuers
-        // Warp 10 + h: O_h (+)= P_h,g V_g[keys 64h .. 64h+63], A = P_h in
-        // tensor memory (8 columns per 16 keys, at buffer columns 64h..),
-        // B = V tile (MN-major, 16 keys = 2 KiB = 128 per K step).  The
-        // first product of an item overwrites O_h, so it waits until the
-        // output warps have read the previous item's accumulators.
+        // Warp 10 + h: O_h (+)= P_g V_g for the tiles g with g mod 2 = h,
+        // eight MMAs of 16 keys: A = P in tensor memory (8 columns per 16
+        // keys, buffer columns [0,64)), B = V tile (MN-major, 16 keys = 2 KiB
+        // = 128 per K step).  The group's first product of an item (j < 2)
+        // overwrites O_h, so every item starts by waiting until the output
+        // warps have read the previous item's accumulators; the item's
+        // "output final" commit follows the group's last product (or none).
         const int hf = warp - kMmaPvWarp;
         constexpr uint32_t idesc_o = idesc_bf16_f32(BM, HD, false, true);
         constexpr uint64_t kTileDesc = kTileBytes >> 4;
-        const uint64_t v_desc = smem_desc_sw128(smem_u32(sm.v[0]), 1024, 1024) + 128 * 4 * hf;
+        constexpr int kKSteps = kTiles ? 8 : 4;  // 16-key MMAs per product
+        const uint64_t v_desc =
+            smem_desc_sw128(smem_u32(sm.v[0]), 1024, 1024) + (kTiles ? 0 : 128 * 4 * hf);
         const uint32_t d_o = tmem + kOCol + 64u * static_cast<uint32_t>(hf);
-        const uint32_t p_col = tmem + 64u * static_cast<uint32_t>(hf);
+        const uint32_t p_col = tmem + (kTiles ? 0u : 64u * static_cast<uint32_t>(hf));
         int g = 0, v = 0;
         bool ok = true;
         for (int t = 0; ok; ++t) {
@@ -313,49 +332,56 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (it.n_kv == 0) continue;
             if (v >= 1 && !(ok = warp_wait(&sm.o_free, (v - 1) & 1, ab))) break;
             for (int j = 0; j < it.n_kv; ++j, ++g) {
+                if (kTiles && (g & 1) != hf) continue;
                 const int st = g % STAGES, sb = g % kSBufs;
-                if (!(ok = warp_wait(&sm.p_full[sb][hf], (g / kSBufs) & 1, ab))) break;
+                if (!(ok = warp_wait(kTiles ? &sm.p_full[(g >> 1) & 1][hf] : &sm.p_full[sb][hf],
+                                     kTiles ? (g >> 2) & 1 : (g / kSBufs) & 1, ab)))
+                    break;
                 if (!(ok = warp_wait(&sm.kv_full[st], (g / STAGES) & 1, ab))) break;
                 tc_fence_after_sync();
                 const uint32_t a = p_col + 128u * static_cast<uint32_t>(sb);
                 const uint64_t vd = v_desc + static_cast<uint64_t>(st) * kTileDesc;
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
+                for (int kk = 0; kk < kKSteps; ++kk)
                     warp_mma_bf16_ts(d_o, a + 8 * kk, vd + 128 * kk, idesc_o,
-                                     (j > 0 || kk > 0) ? 1u : 0u);
-                if (j == it.n_kv - 1) warp_commit(&sm.o_final);
+                                     (j >= (kTiles ? 2 : 1) || kk > 0) ? 1u : 0u);
                 warp_commit(&sm.kv_empty[st]);
             }
             if (!ok) break;
+            warp_commit(&sm.o_final);
             ++v;
         }
         warp_commit(&sm.drain[1 + hf]);
         mbar_wait_drain(&sm.drain[1 + hf], 0);
     } else if (warp < kSoftmaxWarps) {
         // --------------------------------------------------------- softmax
-        // Half h owns keys [64h, 64h+64) of every tile with its own reference
-        // maximum m_h, running sum l_h and accumulator O_h; the two halves
-        // are combined by the output warps.
+        // Group h owns the tiles g with g mod 2 = h, with its own reference
+        // maximum m_h, running sum l_h and accumulator O_h; the two groups
+        // are combined by the output warps.  A tile's 128 scores are taken
+        // in two rounds of 64 (registers), each written back as 32 columns
+        // of P over scores already read.
         //
         // Softmax is unchanged by a common shift of a row's scores, so P may
         // be taken against any reference m_h that keeps 2^(s c - m_h c)
-        // finite; the running maximum is only one such choice.  A tile is
+        // finite; the running maximum is only one such choice.  A round is
         // therefore exponentiated straight against the current m_h (no
-        // maximum pass), and the row checks its own tile sum: only a row
+        // maximum pass), and the row checks its own round sum: only a row
         // whose sum exceeds 2^16 (its maximum grew by 10 to 16 log2 units or
         // more, or overflowed) or that has not yet seen a visible key takes
-        // the exact step -- tile maximum, new m_h, O_h and l_h scaled by
-        // 2^((m_old - m_new) c), P recomputed.  Each decision uses only the
-        // row's own visible scores, so a row's result never depends on
-        // another row or on masked keys.
-        const int half = warp >> 2;
+        // the exact step -- round maximum, new m_h, O_h and l_h scaled by
+        // 2^((m_old - m_new) c), P recomputed; in the second round the first
+        // round's P (already written) is scaled the same way.  Each decision
+        // uses only the row's own visible scores, so a row's result never
+        // depends on another row or on masked keys.
+        const int half = warp >> 2;  // the group (by tiles) or key half (by halves)
+        constexpr int kRounds = kTiles ? 2 : 1;  // 64-score rounds per tile
         const uint32_t lane_base = static_cast<uint32_t>(warp & 3) * 32;
         const int r = static_cast<int>(lane_base) + lane;    // row in tile = TMEM lane
         const uint32_t tl = tmem_addr(tmem, lane_base, 0);
         const uint32_t to = tl + kOCol + 64u * half;         // O_h: 64 columns
         const float C = p.scale_log2;
 
-        // Keys at or past `lim` (relative to the half's first key) get -inf:
+        // Keys at or past `lim` (relative to the round's first key) get -inf:
         // weight exactly zero.
         auto mask_scores = [](uint32_t(&a)[32], uint32_t(&b)[32], int lim) {
 #pragma unroll
@@ -365,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         };
         // P = 2^(s c - mc) in bf16 (column c of the packed tile holds keys
-        // 2c, 2c+1 of the half) and the fp32 row sum of P.  Packed fp32x2
+        // 2c, 2c+1 of the round) and the fp32 row sum of P.  Packed fp32x2
         // FMA / add (one instruction per two scores) keep the instruction
         // count -- and the issue slots taken from the MMA warps -- down.
         auto exp_tile = [C](const uint32_t(&a)[32], const uint32_t(&b)[32], float mc,
@@ -388,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             f32x2_unpack(add_f32x2(add_f32x2(acc2[0], acc2[1]), add_f32x2(acc2[2], acc2[3])), u0, u1);
             return u0 + u1;
         };
-        // Row maximum of the half's 64 scores: four chains of three-input max.
+        // Row maximum of the round's 64 scores: four chains of three-input max.
         auto row_max = [](const uint32_t(&a)[32], const uint32_t(&b)[32]) -> float {
             float t0 = fmaxf(u2f(a[0]), u2f(a[1])), t1 = fmaxf(u2f(a[2]), u2f(a[3]));
             float t2 = fmaxf(u2f(b[0]), u2f(b[1])), t3 = fmaxf(u2f(b[2]), u2f(b[3]));
@@ -411,83 +437,106 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (it.n_kv == 0) continue;
             const int row = it.q0 + r;  // query index
             const int row_lim = causal ? min(it.kv_len, row + 1) : it.kv_len;  // keys < row_lim visible
-            float m_run = -INFINITY;  // -inf until this half has seen a visible key
+            float m_run = -INFINITY;  // -inf until this group has seen a visible key
             float l_run = 0.f;
 
             for (int j = 0; j < it.n_kv; ++j, ++g) {
+                if (kTiles && (g & 1) != half) continue;
                 const int sb = g % kSBufs;
                 ok = __all_sync(0xffffffffu, mbar_wait(&sm.s_full[sb], (g / kSBufs) & 1, ab));
                 if (!ok) break;
                 tc_fence_after_sync();
-                const uint32_t ts = tl + 128u * static_cast<uint32_t>(sb) + 64u * half;
-                // In-tile mask only on tiles that reach past the padding
-                // length or the diagonal (tile-uniform branch).
+                const uint32_t ts = tl + 128u * static_cast<uint32_t>(sb);
                 const bool edge =
                     (j * BN + BN > it.kv_len) || (causal && j * BN + BN - 1 > it.q0);
-                const int lim = row_lim - (j * BN + 64 * half);
-
-                uint32_t pk[32];
-                float lt = 0.f;
-                bool need = true;  // first tile of the item: no row has a reference yet
-                if (j > 0) {
-                    uint32_t s0[32], s1[32];
-                    tmem_ld32(ts, s0);
-                    tmem_ld32(ts + 32, s1);
-                    tmem_ld_wait(s0);
-                    reg_fence32(s1);
-                    if (edge) mask_scores(s0, s1, lim);
-                    lt = exp_tile(s0, s1, m_run == -INFINITY ? 0.f : m_run * C, pk);
-                    need = m_run == -INFINITY || !(lt <= kTileSumLimit);
-                }
-                if (__any_sync(0xffffffffu, need)) {
-                    // Exact step for the rows that need it (scores reloaded
-                    // from tensor memory: P has not been written over them).
-                    uint32_t s0[32], s1[32];
-                    tmem_ld32(ts, s0);
-                    tmem_ld32(ts + 32, s1);
-                    tmem_ld_wait(s0);
-                    reg_fence32(s1);
-                    if (edge) mask_scores(s0, s1, lim);
-                    float alpha = 1.f;
-                    if (need) {
-                        const float m_new = fmaxf(m_run, row_max(s0, s1));
-                        if (m_run != -INFINITY) alpha = ex2_approx((m_run - m_new) * C);
-                        m_run = m_new;  // stays -inf while every key so far is masked
-                        l_run *= alpha;
+                float p0_alpha = 1.f;  // rescale of the first round's P by the second round
+#pragma unroll 1
+                for (int rd = 0; rd < kRounds; ++rd) {
+                    const int c0 = kTiles ? 64 * rd : 64 * half;  // the round's first key in the tile
+                    const uint32_t tr = ts + static_cast<uint32_t>(c0);
+                    const int lim = row_lim - (j * BN + c0);
+                    uint32_t pk[32];
+                    float lt = 0.f;
+                    bool need = true;  // the first round of the item: no reference yet
+                    if (kTiles ? (j >= 2 || rd == 1) : j > 0) {
+                        uint32_t s0[32], s1[32];
+                        tmem_ld32(tr, s0);
+                        tmem_ld32(tr + 32, s1);
+                        tmem_ld_wait(s0);
+                        reg_fence32(s1);
+                        if (edge) mask_scores(s0, s1, lim);
                         lt = exp_tile(s0, s1, m_run == -INFINITY ? 0.f : m_run * C, pk);
+                        need = m_run == -INFINITY || !(lt <= kTileSumLimit);
                     }
-                    if (__any_sync(0xffffffffu, alpha != 1.f)) {
-                        // O_h must hold exactly sum_{j' < j} P V: wait for
-                        // the release of tile g-1's stage (committed after
-                        // both products of tile g-1; j >= 1 here since no row
-                        // has a finite reference on an item's first tile).
-                        // Its next release needs P_g, which this thread has
-                        // not yet published, so the parity cannot alias.
-                        // Rows with alpha == 1 are rewritten unchanged.
-                        ok = __all_sync(0xffffffffu, mbar_wait(&sm.kv_empty[(g - 1) % STAGES],
-                                                               ((g - 1) / STAGES) & 1, ab));
-                        if (!ok) break;
-                        tc_fence_after_sync();
-                        uint32_t o0[32], o1[32];
-                        tmem_ld32(to, o0);
-                        tmem_ld32(to + 32, o1);
-                        tmem_ld_wait(o0);
-                        reg_fence32(o1);
-#pragma unroll
-                        for (int c = 0; c < 32; ++c) {
-                            o0[c] = f2u(u2f(o0[c]) * alpha);
-                            o1[c] = f2u(u2f(o1[c]) * alpha);
+                    if (__any_sync(0xffffffffu, need)) {
+                        uint32_t s0[32], s1[32];
+                        tmem_ld32(tr, s0);
+                        tmem_ld32(tr + 32, s1);
+                        tmem_ld_wait(s0);
+                        reg_fence32(s1);
+                        if (edge) mask_scores(s0, s1, lim);
+                        float alpha = 1.f;
+                        if (need) {
+                            const float m_new = fmaxf(m_run, row_max(s0, s1));
+                            if (m_run != -INFINITY) alpha = ex2_approx((m_run - m_new) * C);
+                            m_run = m_new;
+                            l_run *= alpha;
+                            lt = exp_tile(s0, s1, m_run == -INFINITY ? 0.f : m_run * C, pk);
                         }
-                        tmem_st32(to, o0);
-                        tmem_st32(to + 32, o1);
+                        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+                            if (!kTiles || j >= 2) {
+                                // O_h holds the earlier tiles of the item:
+                                // wait for the product of the previous tile
+                                // it took (g-2 by tiles; g-1, both halves, by
+                                // halves, where a finite old reference means
+                                // j >= 1).  That release's next phase needs
+                                // P_g, not yet published, so it cannot alias.
+                                const int gp = g - (kTiles ? 2 : 1);
+                                ok = __all_sync(0xffffffffu,
+                                                mbar_wait(&sm.kv_empty[gp % STAGES],
+                                                          (gp / STAGES) & 1, ab));
+                                if (!ok) break;
+                                tc_fence_after_sync();
+#pragma unroll 1
+                                for (int part = 0; part < 2; ++part) {
+                                    uint32_t o0[32];
+                                    tmem_ld32(to + 32u * static_cast<uint32_t>(part), o0);
+                                    tmem_ld_wait(o0);
+#pragma unroll
+                                    for (int c = 0; c < 32; ++c) o0[c] = f2u(u2f(o0[c]) * alpha);
+                                    tmem_st32(to + 32u * static_cast<uint32_t>(part), o0);
+                                    tmem_st_wait();
+                                }
+                            }
+                            if (kTiles && rd == 1) p0_alpha = alpha;
+                        }
+                    }
+                    // P columns: [32 rd, 32 rd + 32) by tiles, [64 h, 64 h + 32)
+                    // by halves; both lie over scores already read.
+                    tmem_st32(ts + static_cast<uint32_t>(kTiles ? 32 * rd : 64 * half), pk);
+                    l_run += lt;
+                }
+                if (!ok) break;
+                if (kTiles && __any_sync(0xffffffffu, p0_alpha != 1.f)) {
+                    // The first round's P was taken against the old
+                    // reference: scale it like O_h and l_h.
+                    tmem_st_wait();
+#pragma unroll 1
+                    for (int part = 0; part < 4; ++part) {
+                        uint32_t p0[8];
+                        tmem_ld8_waited(ts + 8u * static_cast<uint32_t>(part), p0);
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            p0[c] = pack_bf16x2(u2f(p0[c] << 16) * p0_alpha,
+                                                u2f(p0[c] & 0xffff0000u) * p0_alpha);
+                        tmem_st8(ts + 8u * static_cast<uint32_t>(part), p0);
+                        tmem_st_wait();
                     }
                 }
-                tmem_st32(ts, pk);
-                l_run += lt;
                 tmem_st_wait();
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&sm.p_full[sb][half]);
+                if (lane == 0) mbar_arrive(kTiles ? &sm.p_full[(g >> 1) & 1][half] : &sm.p_full[sb][half]);
             }
             if (!ok) break;
             // Row statistics of this item for the output warps, once they have
@@ -507,8 +556,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // q):
         //   out = (O_A w_A + O_B w_B) / (l_A w_A + l_B w_B),
         //   w_h = 2^((m_h - M) c), M = max(m_A, m_B);
-        // a half that saw no visible key has weight 0, a row with no visible
-        // key at all outputs 0.
+        // a group that saw no visible key (or no tile) has weight 0 and its
+        // accumulator, possibly never written for this item, is left out of
+        // the result; a row with no visible key at all outputs 0.
         const uint32_t lane_base = static_cast<uint32_t>(warp & 3) * 32;
         const int r = static_cast<int>(lane_base) + lane;
         const uint32_t tl = tmem_addr(tmem, lane_base, 0);
@@ -568,8 +618,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint32_t packed[16];
 #pragma unroll
                     for (int c = 0; c < 16; ++c)
-                        packed[c] = pack_bf16x2(u2f(oa[2 * c]) * fa + u2f(ob[2 * c]) * fb,
-                                                u2f(oa[2 * c + 1]) * fa + u2f(ob[2 * c + 1]) * fb);
+                        packed[c] = pack_bf16x2((la > 0.f ? u2f(oa[2 * c]) * fa : 0.f) +
+                                                    (lb > 0.f ? u2f(ob[2 * c]) * fb : 0.f),
+                                                (la > 0.f ? u2f(oa[2 * c + 1]) * fa : 0.f) +
+                                                    (lb > 0.f ? u2f(ob[2 * c + 1]) * fb : 0.f));
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
                         d4[4 * part + c] = make_uint4(packed[4 * c], packed[4 * c + 1],
@@ -590,12 +642,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
+bool attn_bf16_splits_by_tiles(int Tq, int Tk, int mask) {
+    // Average key tiles per 128-row query tile (key padding ignored).
+    const int nqb = (Tq + kAttnRowsPerCta - 1) / kAttnRowsPerCta;
+    if (nqb <= 0 || Tk <= 0) return false;
+    long long tiles = 0;
+    for (int qb = 0; qb < nqb; ++qb) {
+        const int kv_end = (mask & kMaskCausalBit) ? std::min(Tk, std::min((qb + 1) * kAttnRowsPerCta, Tq)) : Tk;
+        tiles += (kv_end + BN - 1) / BN;
+    }
+    return tiles >= static_cast<long long>(kAttnTilesSplitMin) * nqb;
+}
+
 cudaError_t launch_attn_bf16(const CUtensorMap &tq, const CUtensorMap &tk,
                              const CUtensorMap &tv, const AttnParams &p, cudaStream_t stream,
                              bool pdl) {
+    const bool by_tiles = attn_bf16_splits_by_tiles(p.Tq, p.Tk, p.mask);
+    auto kernel = by_tiles ? attn_fwd_bf16_kernel<true> : attn_fwd_bf16_kernel<false>;
     const size_t smem = sizeof(SmemAttn) + 1024;
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_bf16_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     // One persistent CTA per SM (fewer if there are fewer items).
@@ -605,7 +670,7 @@ cudaError_t launch_attn_bf16(const CUtensorMap &tq, const CUtensorMap &tk,
         return e;
     const int grid = p.total_items < sms ? p.total_items : sms;
     if (grid <= 0) return cudaSuccess;
-    return launch_kernel(attn_fwd_bf16_kernel, dim3(grid), dim3(kThreads), smem, stream, pdl, 1, tq, tk, tv, p);
+    return launch_kernel(kernel, dim3(grid), dim3(kThreads), smem, stream, pdl, 1, tq, tk, tv, p);
 }
 
 }  // namespace mha

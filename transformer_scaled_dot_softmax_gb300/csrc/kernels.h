@@ -60,6 +60,14 @@ struct AttnParams {
 constexpr int kAttnRowsPerCta = 128;  // one work item = one 128-row query tile
 constexpr int kAttnHeadDim = 64;
 
+// The kernel's two softmax groups split a row's keys either into the two
+// 64-key halves of every tile or into alternate tiles; alternate tiles keep
+// the groups out of lockstep and pay once a query tile has, on average,
+// kAttnTilesSplitMin key tiles or more (measured on GB300: +3 % at causal
+// T = 8192), while short items finish sooner by halves.
+constexpr int kAttnTilesSplitMin = 8;
+bool attn_bf16_splits_by_tiles(int Tq, int Tk, int mask);
+
 // q, k, v: head-split (B, H, T, 64) bf16 tensors described by 3-D TMA maps
 // over (64, T, B*H) with 128-byte swizzling and 128-row boxes.
 cudaError_t launch_attn_bf16(const CUtensorMap &tq, const CUtensorMap &tk,
