@@ -53,12 +53,20 @@
 // ready and S_{g+2} is being computed.  Issuers are ordered only through
 // barriers:
 //   S ready (per buffer)           S issuer -> softmax,
-//   P ready (per group, two deep)  softmax group h -> PV issuer h.  Each
-//                                  group counts its own tiles: a barrier
-//                                  shared by both groups would let one
-//                                  group's issuer mistake the other group's
-//                                  unfinished phase (parity one behind) for
-//                                  its own finished one,
+//   P ready                        softmax -> PV issuer: by halves per
+//                                  (buffer, half); by tiles per (group,
+//                                  round), two deep over the group's own
+//                                  tiles.  The issuer starts a tile's first
+//                                  four products on round 0's P, while the
+//                                  softmax works on round 1, and the last
+//                                  four on round 1's.  A barrier shared by
+//                                  both groups would let one group's issuer
+//                                  mistake the other group's unfinished
+//                                  phase (parity one behind) for its own
+//                                  finished one,
+//   round 0 product done (by tiles, per group, two deep)  PV issuer h ->
+//                                  softmax group h when round 1 must rescale
+//                                  O_h,
 //   stage released                 the tile's PV issuer -> TMA producer, S
 //                                  issuer (S_g overwrites tile g-3's buffer,
 //                                  so it waits for tile g-3's release) and a
@@ -76,7 +84,8 @@
 // reference that keeps the exponentials finite gives the same result), and
 // only a row whose round sum exceeds 2^16 -- its maximum grew by 10 to 16
 // log2 units or more -- or that has no reference yet takes the exact step
-// (round maximum, O_h, l_h and the tile's first-round P rescaled, P
+// (round maximum, O_h and l_h rescaled -- in round 1 after the round-0
+// product, taken against the old reference, has landed in O_h -- P
 // recomputed).  Decided per row.
 //
 // Tensor memory (512 columns): S buffers [0,128), [128,256), [256,384);
@@ -120,7 +129,9 @@ struct __align__(1024) SmemAttn {
     uint64_t kv_full[STAGES];
     uint64_t kv_empty[STAGES];
     uint64_t s_full[kSBufs];
-    uint64_t p_full[kSBufs][2];  // P written (4 warps): [buffer][half] / [group tile mod 2][group]
+    uint64_t p_full[kSBufs][2];  // P written (4 warps), by halves: [buffer][half]
+    uint64_t p_rd[2][2][2];      // by tiles: [group][round][group tile mod 2], P round written
+    uint64_t pv0[2][2];          // by tiles: [group][group tile mod 2], round-0 product complete
     uint64_t ml_full;            // row statistics written (8 softmax warps)
     uint64_t ml_free;            // row statistics read (4 output warps)
     uint64_t o_final;            // both groups' P.V products of an item complete
@@ -192,6 +203,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sm.p_full[i][0], kSoftmaxWarps / 2);
             mbar_init(&sm.p_full[i][1], kSoftmaxWarps / 2);
         }
+        for (int i = 0; i < 8; ++i) mbar_init(&sm.p_rd[i >> 2][(i >> 1) & 1][i & 1], kSoftmaxWarps / 2);
+        for (int i = 0; i < 4; ++i) mbar_init(&sm.pv0[i >> 1][i & 1], 1);
         mbar_init(&sm.ml_full, kSoftmaxWarps);
         mbar_init(&sm.ml_free, 4);
         mbar_init(&sm.o_final, 2);  // one commit per PV issuer
@@ -334,17 +347,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < it.n_kv; ++j, ++g) {
                 if (kTiles && (g & 1) != hf) continue;
                 const int st = g % STAGES, sb = g % kSBufs;
-                if (!(ok = warp_wait(kTiles ? &sm.p_full[(g >> 1) & 1][hf] : &sm.p_full[sb][hf],
-                                     kTiles ? (g >> 2) & 1 : (g / kSBufs) & 1, ab)))
+                const int slot = (g >> 1) & 1, par = (g >> 2) & 1;
+                if (!(ok = warp_wait(kTiles ? &sm.p_rd[hf][0][slot] : &sm.p_full[sb][hf],
+                                     kTiles ? par : (g / kSBufs) & 1, ab)))
                     break;
                 if (!(ok = warp_wait(&sm.kv_full[st], (g / STAGES) & 1, ab))) break;
                 tc_fence_after_sync();
                 const uint32_t a = p_col + 128u * static_cast<uint32_t>(sb);
                 const uint64_t vd = v_desc + static_cast<uint64_t>(st) * kTileDesc;
 #pragma unroll
-                for (int kk = 0; kk < kKSteps; ++kk)
+                for (int kk = 0; kk < 4; ++kk)
                     warp_mma_bf16_ts(d_o, a + 8 * kk, vd + 128 * kk, idesc_o,
                                      (j >= (kTiles ? 2 : 1) || kk > 0) ? 1u : 0u);
+                if (kTiles) {
+                    // The round-0 half is issued while the softmax works on
+                    // round 1; the second half follows round 1's P.
+                    warp_commit(&sm.pv0[hf][slot]);
+                    if (!(ok = warp_wait(&sm.p_rd[hf][1][slot], par, ab))) break;
+                    tc_fence_after_sync();
+#pragma unroll
+                    for (int kk = 4; kk < 8; ++kk)
+                        warp_mma_bf16_ts(d_o, a + 8 * kk, vd + 128 * kk, idesc_o, 1u);
+                }
                 warp_commit(&sm.kv_empty[st]);
             }
             if (!ok) break;
@@ -369,8 +393,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // whose sum exceeds 2^16 (its maximum grew by 10 to 16 log2 units or
         // more, or overflowed) or that has not yet seen a visible key takes
         // the exact step -- round maximum, new m_h, O_h and l_h scaled by
-        // 2^((m_old - m_new) c), P recomputed; in the second round the first
-        // round's P (already written) is scaled the same way.  Each decision
+        // 2^((m_old - m_new) c), P recomputed; in the second round O_h is
+        // scaled once the first round's product is in it.  Each decision
         // uses only the row's own visible scores, so a row's result never
         // depends on another row or on masked keys.
         const int half = warp >> 2;  // the group (by tiles) or key half (by halves)
@@ -449,8 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t ts = tl + 128u * static_cast<uint32_t>(sb);
                 const bool edge =
                     (j * BN + BN > it.kv_len) || (causal && j * BN + BN - 1 > it.q0);
-                float p0_alpha = 1.f;  // rescale of the first round's P by the second round
-#pragma unroll 1
+#pragma unroll
                 for (int rd = 0; rd < kRounds; ++rd) {
                     const int c0 = kTiles ? 64 * rd : 64 * half;  // the round's first key in the tile
                     const uint32_t tr = ts + static_cast<uint32_t>(c0);
@@ -484,7 +507,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                             lt = exp_tile(s0, s1, m_run == -INFINITY ? 0.f : m_run * C, pk);
                         }
                         if (__any_sync(0xffffffffu, alpha != 1.f)) {
-                            if (!kTiles || j >= 2) {
+                            if (kTiles && rd == 1) {
+                                // O_h holds the item's earlier tiles and this
+                                // tile's round 0 (taken against the old
+                                // reference): wait for that product.
+                                ok = __all_sync(0xffffffffu, mbar_wait(&sm.pv0[half][(g >> 1) & 1],
+                                                                       (g >> 2) & 1, ab));
+                                if (!ok) break;
+                                tc_fence_after_sync();
+#pragma unroll 1
+                                for (int part = 0; part < 2; ++part) {
+                                    uint32_t o0[32];
+                                    tmem_ld32(to + 32u * static_cast<uint32_t>(part), o0);
+                                    tmem_ld_wait(o0);
+#pragma unroll
+                                    for (int c = 0; c < 32; ++c) o0[c] = f2u(u2f(o0[c]) * alpha);
+                                    tmem_st32(to + 32u * static_cast<uint32_t>(part), o0);
+                                    tmem_st_wait();
+                                }
+                            } else if (!kTiles || j >= 2) {
                                 // O_h holds the earlier tiles of the item:
                                 // wait for the product of the previous tile
                                 // it took (g-2 by tiles; g-1, both halves, by
@@ -508,35 +549,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     tmem_st_wait();
                                 }
                             }
-                            if (kTiles && rd == 1) p0_alpha = alpha;
+
                         }
                     }
                     // P columns: [32 rd, 32 rd + 32) by tiles, [64 h, 64 h + 32)
                     // by halves; both lie over scores already read.
                     tmem_st32(ts + static_cast<uint32_t>(kTiles ? 32 * rd : 64 * half), pk);
                     l_run += lt;
-                }
-                if (!ok) break;
-                if (kTiles && __any_sync(0xffffffffu, p0_alpha != 1.f)) {
-                    // The first round's P was taken against the old
-                    // reference: scale it like O_h and l_h.
-                    tmem_st_wait();
-#pragma unroll 1
-                    for (int part = 0; part < 4; ++part) {
-                        uint32_t p0[8];
-                        tmem_ld8_waited(ts + 8u * static_cast<uint32_t>(part), p0);
-#pragma unroll
-                        for (int c = 0; c < 8; ++c)
-                            p0[c] = pack_bf16x2(u2f(p0[c] << 16) * p0_alpha,
-                                                u2f(p0[c] & 0xffff0000u) * p0_alpha);
-                        tmem_st8(ts + 8u * static_cast<uint32_t>(part), p0);
+                    if (kTiles) {
                         tmem_st_wait();
+                        tc_fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&sm.p_rd[half][rd][(g >> 1) & 1]);
                     }
                 }
-                tmem_st_wait();
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(kTiles ? &sm.p_full[(g >> 1) & 1][half] : &sm.p_full[sb][half]);
+                if (!ok) break;
+                if (!kTiles) {
+                    tmem_st_wait();
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sm.p_full[sb][half]);
+                }
             }
             if (!ok) break;
             // Row statistics of this item for the output warps, once they have
