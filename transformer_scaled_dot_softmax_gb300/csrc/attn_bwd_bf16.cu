@@ -149,24 +149,28 @@ __device__ __forceinline__ void softmax_terms(const uint32_t (&sv)[N], const uin
 //                 (2) dP^T = V dO_j^T    same shape
 //                 (3) dV  += P^T dO_j    M=128 keys, N=64, K=128 queries, A = P^T in
 //                                        tensor memory
-//                 (4) dK  += dS^T Q_j    same, A = dS^T in tensor memory
+//                 (4) dK  += dS^T Q_j    same, A = dS^T from shared memory (key
+//                                        rows, queries contiguous: K-major)
 //                 (5) dQ_j = dS K        M=128 queries, N=64, K=128 keys, A = dS from
-//                                        shared memory (queries contiguous)
+//                                        the same shared memory (MN-major)
 //               Computing S and dP transposed puts the keys on the
-//               tensor-memory lanes, so P^T and dS^T feed (3) and (4) straight
-//               from tensor memory.  Issue order: (4) of block j, (1) of
-//               block j+1, (2) of block j+1 once (4) has read dS^T, then (3)
-//               and (5) of block j -- the tensor pipe runs in issue order, so
-//               only (4) stands between block j's softmax terms and block
-//               j+1's scores.
+//               tensor-memory lanes, so P^T feeds (3) straight from tensor
+//               memory.  Issue order: (1) and (2) of block j+1 as soon as
+//               block j's softmax terms are written, then (4), (3) and (5) of
+//               block j -- the tensor pipe runs in issue order, so no product
+//               of block j stands between its softmax terms and block j+1's
+//               scores.  (4) reads dS^T from shared memory rather than tensor
+//               memory for that reason: in tensor memory it would have to sit
+//               over dP^T's columns, and (2) of block j+1 would wait for it.
 //   warps 2-17  one thread per (key, chunk of 32 queries) -- warp w takes the
 //               keys of lane quadrant w%4 and chunk (w-2)/4:
 //               P^T = 2^(S^T c - lse_j) (masked: 0), dS^T = P^T (dP^T - D_j),
 //               elementwise (lse and D are per-query inputs, no row
-//               reduction); P^T and dS^T written as bf16, dS^T also into
-//               shared memory for (5) (two buffers: block j+2 reuses block
-//               j's, whose (5) the commit of block j+1's scores already
-//               covers).  After block j's terms, the same warps add the
+//               reduction); P^T written as bf16 into tensor memory, dS into
+//               shared memory for (4) and (5) (two buffers: block j+2 reuses
+//               block j's, whose (4) and (5) the commit of block j+2's
+//               scores, which the warps wait for, already covers).  After
+//               block j's terms, the same warps add the
 //               dQ_{j-1} partial (warp w: the rows of quadrant w%4, features
 //               [16c, 16c+16)) to the fp32 accumulator in global memory with
 //               vector reductions, each warp instruction covering 512
@@ -175,9 +179,8 @@ __device__ __forceinline__ void softmax_terms(const uint32_t (&sv)[N], const uin
 //               chunks 2, 3 dV, 32 features each.
 //
 // Tensor memory: S^T [0,128), dP^T [128,256), P^T [256,320), dV [320,384),
-// dK [384,448), dQ_j [448,512).  dS^T of chunk c goes over dP^T columns
-// [128+32c, 128+32c+16), which only chunk c's warp reads; P^T has columns of
-// its own so that the next block's scores need not wait for (3).
+// dK [384,448), dQ_j [448,512).  P^T has columns of its own and dS^T stays
+// in shared memory, so the next block's scores wait for neither (3) nor (4).
 constexpr uint32_t kTile = BQ * HD * 2;  // 16 KiB
 constexpr uint32_t kColS = 0, kColDP = 128, kColP = 256, kColDV = 320, kColDK = 384, kColDQ = 448;
 constexpr int kBwdThreads = 576;
@@ -188,7 +191,7 @@ struct __align__(1024) SmemBwd {
     uint8_t v[kTile];
     uint8_t q[2][kTile];
     uint8_t g[2][kTile];      // dO
-    uint8_t ds[2][2 * kTile]; // dS as the A operand of (5): 2 blocks of 64 queries x 128 key rows
+    uint8_t ds[2][2 * kTile]; // dS, the A operand of (4) and (5): 2 blocks of 64 queries x 128 key rows
     float nlse2[2][BQ];
     float dvec[2][BQ];
     uint64_t kv_full;
@@ -196,8 +199,8 @@ struct __align__(1024) SmemBwd {
     uint64_t q_empty[2];  // (1), (4) have read Q_j (and the softmax lse_j, D_j)
     uint64_t g_empty[2];  // (2), (3) have read dO_j
     uint64_t sdp_full;   // (1), (2) complete
-    uint64_t pds_full;   // P^T, dS^T written (16 warps)
-    uint64_t tmem_free;  // (4) complete: the dP^T columns reusable
+    uint64_t pds_full;   // P^T (tensor memory), dS (shared memory) written (16 warps)
+    uint64_t tmem_free;  // (4) of the block complete
     uint64_t p_free;     // (3) complete: the P^T columns reusable
     uint64_t dq_full;    // (5) complete
     uint64_t dq_free;    // dQ_j read (16 warps)
@@ -302,15 +305,22 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             constexpr uint64_t kT = kTile >> 4;
             // K-major operands (a K step of 16 = 32 bytes = 2), MN-major
             // operands (16 rows of 128 bytes = 2 KiB = 128 per K step).
+            // One base descriptor (K-major, at sm.k): every operand lies a
+            // whole number of 16 KiB tiles further (the address field counts
+            // 16-byte units and stays below 2^14), and the MN-major form
+            // differs only in the leading byte offset field (1024 bytes
+            // instead of 16; 16 KiB between dS's two 64-query blocks).
             const uint64_t k_km = smem_desc_sw128(smem_u32(sm.k), 16, 1024);
-            const uint64_t v_km = smem_desc_sw128(smem_u32(sm.v), 16, 1024);
-            const uint64_t q_km = smem_desc_sw128(smem_u32(sm.q[0]), 16, 1024);
-            const uint64_t g_km = smem_desc_sw128(smem_u32(sm.g[0]), 16, 1024);
-            const uint64_t q_mn = smem_desc_sw128(smem_u32(sm.q[0]), 1024, 1024);
-            const uint64_t g_mn = smem_desc_sw128(smem_u32(sm.g[0]), 1024, 1024);
-            const uint64_t k_mn = smem_desc_sw128(smem_u32(sm.k), 1024, 1024);
-            // dS: two 64-query blocks 16 KiB apart (leading byte offset)
-            const uint64_t ds_mn = smem_desc_sw128(smem_u32(sm.ds[0]), kTile, 1024);
+            constexpr uint64_t kMn = static_cast<uint64_t>((1024 >> 4) - 1) << 16;
+            constexpr uint64_t kDsMn = static_cast<uint64_t>((kTile >> 4) - 1) << 16;
+            const uint64_t v_km = k_km + kT;
+            const uint64_t q_km = k_km + 2 * kT;
+            const uint64_t g_km = k_km + 4 * kT;
+            const uint64_t ds_km0 = k_km + 6 * kT;
+            const uint64_t q_mn = q_km + kMn;
+            const uint64_t g_mn = g_km + kMn;
+            const uint64_t k_mn = k_km + kMn;
+            const uint64_t ds_mn = ds_km0 + kDsMn;
             // (1) and (2) of the block in stage s
             auto score_s = [&](int s) {
                 const uint64_t so = static_cast<uint64_t>(s) * kT;
@@ -336,24 +346,23 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const uint64_t so = static_cast<uint64_t>(st) * kT;  // q[st], g[st] stage offset
                 if (!(ok = warp_wait(&sm.pds_full, t & 1, ab))) break;
                 tc_fence_after_sync();
-                // (4): the 16 queries of K step kk are chunk kk/2, half kk%2
-#pragma unroll
-                for (int kk = 0; kk < BQ / 16; ++kk)
-                    warp_mma_bf16_ts(tmem + kColDK, tmem + kColDP + 32 * (kk >> 1) + 8 * (kk & 1),
-                                     q_mn + so + 128 * kk, id_kv, (t > 0 || kk > 0) ? 1u : 0u);
-                warp_commit(&sm.tmem_free);
-                warp_commit(&sm.q_empty[st]);
                 if (t + 1 < n_j) {
-                    // the next block's scores; (1) runs while (4)'s completion
-                    // comes back, (2) overwrites the dS^T that (4) reads
+                    // the next block's scores first: the softmax terms of
+                    // block t have read S^T and dP^T
                     if (!(ok = warp_wait(&sm.stage_full[st ^ 1], ((t + 1) >> 1) & 1, ab))) break;
                     tc_fence_after_sync();
                     score_s(st ^ 1);
-                    if (!(ok = warp_wait(&sm.tmem_free, t & 1, ab))) break;
-                    tc_fence_after_sync();
                     score_dp(st ^ 1);
                     warp_commit(&sm.sdp_full);
                 }
+                // (4) from dS^T in shared memory
+                const uint64_t dso = static_cast<uint64_t>(st) * (2 * kT);
+#pragma unroll
+                for (int kk = 0; kk < BQ / 16; ++kk)
+                    warp_mma_bf16_ss(tmem + kColDK, ds_km0 + dso + (kk >> 2) * kT + 2 * (kk & 3),
+                                     q_mn + so + 128 * kk, id_kv, (t > 0 || kk > 0) ? 1u : 0u);
+                warp_commit(&sm.q_empty[st]);
+                warp_commit(&sm.tmem_free);
                 // (3) after the next block's scores: P^T has columns of its
                 // own, which the softmax warps rewrite only after p_free
 #pragma unroll
@@ -364,12 +373,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 warp_commit(&sm.g_empty[st]);
                 if (t >= 1 && !(ok = warp_wait(&sm.dq_free, (t - 1) & 1, ab))) break;
                 tc_fence_after_sync();
-                const uint64_t dso = static_cast<uint64_t>(st) * (2 * kT);
 #pragma unroll
                 for (int kk = 0; kk < BKB / 16; ++kk)
                     warp_mma_bf16_ss(tmem + kColDQ, ds_mn + dso + 128 * kk, k_mn + 128 * kk, id_q,
                                      kk > 0 ? 1u : 0u);
                 warp_commit(&sm.dq_full);
+                // (4) of this block complete before the next: it has long
+                // finished when the next block's softmax terms arrive, and
+                // the wait keeps the kernel within its 96 registers without
+                // spills (without it ptxas spills 12 bytes).
+                if (!(ok = warp_wait(&sm.tmem_free, t & 1, ab))) break;
             }
             if (ok) warp_commit(&sm.acc_done);
         }
@@ -432,12 +445,11 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 else
                     softmax_terms<16, true>(sv, dp, l2, dv, C, lim, pk, dsk);
                 // P^T into its own columns once (3) of the previous block has
-                // read them, dS^T over dP^T columns this warp has read
+                // read them
                 if (h == 0 && t >= 1 && !(ok = __all_sync(0xffffffffu, mbar_wait(&sm.p_free, (t - 1) & 1, ab))))
                     break;
                 tmem_st8(tl + kColP + 16u * c + 8u * h, pk);
-                tmem_st8(tl + kColDP + 32u * c + 8u * h, dsk);
-                // dS into shared memory as the A operand of (5): queries
+                // dS into shared memory as the A operand of (4) and (5): queries
                 // contiguous, 128-byte swizzled rows (16-byte chunk x of key
                 // row r at x ^ (r % 8)), 64 queries per 16 KiB block.
 #pragma unroll
