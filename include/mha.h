@@ -97,6 +97,17 @@ mha_status sdpa_forward(mha_dtype dt, const void *q, const void *k, const void *
                         cudaStream_t stream);
 
 /*
+ * Which of its two key splits the MHA_BF16 attention kernel takes for a
+ * problem of this shape (host-only; no device call): 1 when the two softmax
+ * warp groups take alternate 128-key tiles (a 128-row query tile sees, on
+ * average, 8 or more key tiles, key padding not counted), 0 when they take
+ * the two 64-key halves of every tile; -1 for negative extents or an invalid
+ * mask.  Both splits compute the same function (they round differently); the
+ * choice is a speed heuristic, exposed so that tests can cover both.
+ */
+int sdpa_bf16_key_split(int T_q, int T_k, mha_mask mask);
+
+/*
  * sdpa_forward (bf16 only) that also writes, per query row, the log-sum-exp of
  * its visible scores,
  *   lse[b, h, i] = log sum_{j visible} exp(scale * q_i . k_j)   (natural log),

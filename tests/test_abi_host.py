@@ -237,3 +237,17 @@ def test_host_workspace_bytes(lib):
     f32 = lib.lib.sdpa_forward_host_workspace_bytes(0, B, h, Tq, Tk, 32, 48)
     assert f32 == r(B * h * Tq * 128) + r(B * h * Tk * 128) + r(B * h * Tk * 192) + r(B * h * Tq * 192) + r(B * 4)
     assert lib.lib.sdpa_forward_host_workspace_bytes(1, -1, h, Tq, Tk, 64, 64) == 0
+
+
+def test_bf16_key_split_rule(lib):
+    """The kernel's choice between its two key splits, a host-side rule: by
+    alternate tiles once a 128-row query tile sees 8 key tiles on average."""
+    split = lib.lib.sdpa_bf16_key_split
+    assert split(8192, 8192, 1) == 1 and split(8192, 8192, 0) == 1   # the causal T=8192 workload
+    assert split(128, 128, 0) == 0 and split(512, 512, 1) == 0       # short items: key halves
+    assert split(2048, 2048, 1) == 1 and split(1920, 1920, 1) == 1   # causal: 136/16, 120/15 tiles
+    assert split(1792, 1792, 1) == 0                                 # 105 tiles over 14 query tiles
+    assert split(1000, 1024, 0) == 1 and split(1000, 896, 0) == 0    # non-causal: ceil(T_k/128) >= 8
+    assert split(256, 1024, 2) == 1                                  # padding is not counted
+    assert split(0, 1024, 0) == 0 and split(64, 0, 0) == 0           # empty problems
+    assert split(-1, 8, 0) == -1 and split(8, 8, 7) == -1

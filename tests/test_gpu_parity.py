@@ -143,6 +143,7 @@ SPLIT_SHAPES = [
 @pytest.mark.parametrize("B,h,T_q,T_k,mask,tiles", SPLIT_SHAPES)
 def test_bf16_both_key_splits(lib, B, h, T_q, T_k, mask, tiles):
     assert splits_by_tiles(T_q, T_k, bool(mask & si.MASK_CAUSAL)) == tiles
+    assert lib.sdpa_bf16_key_split(T_q, T_k, MASK_NAMES[mask]) == int(tiles)
     w = si.WORKLOADS[4].replace(B=B, h=h, T_q=T_q, T_k=T_k, mask=mask, len_lo=1, len_hi=T_k,
                                 seed=23)
     x = si.make_inputs(w)

@@ -16,7 +16,8 @@ from . import _native
 from ._native import (MHA_BF16, MHA_F32, MHA_MASK_CAUSAL, MHA_MASK_CAUSAL_KEY_PADDING,
                       MHA_MASK_KEY_PADDING, MHA_MASK_NONE, MHA_OK, lib)
 
-__all__ = ["sdpa_forward", "sdpa_forward_lse", "sdpa_forward_host", "sdpa_forward_host_workspace_bytes", "sdpa_backward", "positional_encoding_add",
+__all__ = ["sdpa_forward", "sdpa_forward_lse", "sdpa_forward_host", "sdpa_forward_host_workspace_bytes",
+           "sdpa_bf16_key_split", "sdpa_backward", "positional_encoding_add",
            "encoder_layer_forward", "ENCODER_PARAMS", "sdpa_decode_forward", "mha_forward", "mha_forward_add_layernorm", "mha_workspace_bytes", "status_string", "MhaError",
            "MASKS", "lib"]
 
@@ -134,6 +135,15 @@ def _check_host(name, t, dtype=None):
         raise ValueError("%s must be contiguous" % name)
     if dtype is not None and t.dtype != dtype:
         raise ValueError("%s must be %s" % (name, dtype))
+
+
+def sdpa_bf16_key_split(T_q, T_k, mask="none") -> int:
+    """1 if the bf16 attention kernel splits a row's keys between its two
+    softmax groups by alternate tiles for this shape, 0 if by key halves."""
+    r = int(lib.sdpa_bf16_key_split(T_q, T_k, _mask_code(mask)))
+    if r < 0:
+        raise ValueError("invalid shape or mask")
+    return r
 
 
 def sdpa_forward_host_workspace_bytes(B, h, T_q, T_k, d_k=64, d_v=64, dtype=None) -> int:

@@ -293,6 +293,11 @@ size_t host_ws_parts(mha_dtype dt, int B, int h, int T_q, int T_k, int d_k, int 
 
 }  // namespace
 
+MHA_EXPORT int sdpa_bf16_key_split(int T_q, int T_k, mha_mask mask) {
+    if (T_q < 0 || T_k < 0 || !valid_mask(mask)) return -1;
+    return mha::attn_bf16_splits_by_tiles(T_q, T_k, static_cast<int>(mask)) ? 1 : 0;
+}
+
 MHA_EXPORT size_t sdpa_forward_host_workspace_bytes(mha_dtype dt, int B, int h, int T_q, int T_k,
                                                     int d_k, int d_v) {
     if (B < 0 || h < 0 || T_q < 0 || T_k < 0 || d_k <= 0 || d_v <= 0) return 0;
