@@ -331,7 +331,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int hf = warp - kMmaPvWarp;
         constexpr uint32_t idesc_o = idesc_bf16_f32(BM, HD, false, true);
         constexpr uint64_t kTileDesc = kTileBytes >> 4;
-        constexpr int kKSteps = kTiles ? 8 : 4;  // 16-key MMAs per product
         const uint64_t v_desc =
             smem_desc_sw128(smem_u32(sm.v[0]), 1024, 1024) + (kTiles ? 0 : 128 * 4 * hf);
         const uint32_t d_o = tmem + kOCol + 64u * static_cast<uint32_t>(hf);
