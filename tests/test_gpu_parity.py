@@ -296,6 +296,7 @@ MHA_SMALL = [
     # both by tensor stores
     (2, 128, 300, 256, 4, si.MASK_KEY_PADDING, True),
     (1, 256, 128, 128, 2, si.MASK_NONE, True),
+    # 8 key tiles per query tile: the attention takes alternate key tiles
     (2, 700, 900, 512, 8, si.MASK_KEY_PADDING, True),
 ]
 
