@@ -137,6 +137,10 @@ SPLIT_SHAPES = [
     (2, 2, 513, 700, si.MASK_KEY_PADDING, False),
     (2, 1, 2100, 2100, si.MASK_CAUSAL_KEY_PADDING, True),
     (2, 2, 384, 384, si.MASK_CAUSAL_KEY_PADDING, False),
+    # one partial query tile against long key sequences
+    (1, 2, 1, 4096, si.MASK_NONE, True),
+    (2, 1, 5, 3000, si.MASK_KEY_PADDING, True),
+    (1, 1, 77, 895, si.MASK_NONE, False),
 ]
 
 
