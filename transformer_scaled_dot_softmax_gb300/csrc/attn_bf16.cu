@@ -19,12 +19,16 @@
 //               V_j together into a 5-stage ring (one barrier per stage).
 //   warp 9      issues S_j = Q K_j^T (tcgen05.mma kind::f16, M=128 N=128,
 //               fp32 accumulator in tensor memory).
-//   warps 10,11 issue O_A += P_g V_g for the even tiles g of the CTA and
-//               O_B += P_g V_g for the odd ones (M = 128, N = 64, K = 128 keys;
-//               A operand P read straight from tensor memory).
-//   warps 0-3   softmax of the even tiles (group A), warps 4-7 of the odd
-//               tiles (group B): one thread per query row (= tensor-memory
-//               lane) and tile, taking the 128 scores in two rounds of 64.
+//   warps 10,11 issue the P.V products of softmax groups A and B into
+//               their accumulators O_A and O_B (M = 128, N = 64; A operand P
+//               read straight from tensor memory).
+//   warps 0-3   softmax group A, warps 4-7 group B: one thread per query row
+//               (= tensor-memory lane).  The kernel is a template over how
+//               the groups split a row's keys: by key halves (group h takes
+//               keys [64h, 64h+64) of every tile; chosen for short items) or
+//               by alternate tiles (group A the CTA's even tiles g, group B
+//               the odd ones, each tile's 128 scores in two rounds of 64;
+//               chosen for long items).
 //               Each thread applies the causal / key-padding mask in-tile
 //               (masked score = -inf, i.e. exactly zero weight: aiany.app
 //               Step 10; notebook chapter "Masked Attention in the Decoder"),
@@ -37,9 +41,10 @@
 // accumulators is exact: the output is
 //   out = (O_A 2^((m_A-M)c) + O_B 2^((m_B-M)c)) / (l_A 2^((m_A-M)c) + l_B 2^((m_B-M)c)),
 // M = max(m_A, m_B).  The groups never wait for each other inside the loop.
-// Because they take alternate tiles, the two softmax warps that share a
-// sub-partition work one score tile apart instead of in lockstep, so one's
-// tensor-memory round trips overlap the other's exponentials.
+// By alternate tiles, the two softmax warps that share a sub-partition work
+// one score tile apart instead of in lockstep, so one's tensor-memory round
+// trips overlap the other's exponentials; by halves, a one-tile item is
+// finished by both groups at once.
 //
 // MMA issue: one thread can issue a tcgen05.mma only every ~50-80 cycles
 // when it runs alone inside `if (lane == 0)`, while an N = 64 product needs
@@ -79,7 +84,8 @@
 // A buffer's next use needs its current use to be consumed, so no barrier
 // can run two phases ahead of its waiter.
 //
-// No maximum pass per tile: each round of 64 scores is exponentiated against
+// No maximum pass per tile: each round of 64 scores (by halves: a group's
+// 64 scores of a tile) is exponentiated against
 // the group's current reference maximum (softmax is shift-invariant, so any
 // reference that keeps the exponentials finite gives the same result), and
 // only a row whose round sum exceeds 2^16 -- its maximum grew by 10 to 16
@@ -89,9 +95,9 @@
 // recomputed).  Decided per row.
 //
 // Tensor memory (512 columns): S buffers [0,128), [128,256), [256,384);
-// O_A [384,448), O_B [448,512).  P (128 keys, two per column) sits in buffer
-// columns [0,64): round 0 writes [0,32) over scores it has read, round 1
-// writes [32,64), also already read.
+// O_A [384,448), O_B [448,512).  P (bf16, two keys per column) goes over
+// scores already read: by tiles into buffer columns [0,64) (round 0 writes
+// [0,32), round 1 [32,64)); by halves, half h's 32 columns at [64h, 64h+32).
 #include <cuda_bf16.h>
 
 #include <algorithm>
