@@ -108,6 +108,27 @@ mha_status sdpa_forward(mha_dtype dt, const void *q, const void *k, const void *
 int sdpa_bf16_key_split(int T_q, int T_k, mha_mask mask);
 
 /*
+ * Failure-detection drill (testing only; no product path uses it).  Runs the
+ * MHA_BF16 attention of sdpa_forward on (B, h, T, 64) tensors, but every CTA's
+ * loader issues no copy for its skip_tile-th key tile (counted over the
+ * CTA's work in order, from 0), so the waits on that tile never complete,
+ * and every wait of the kernel gives up after wait_limit_ns (1e5 .. 1e9 ns)
+ * instead of the usual 1 s.  The kernel then records MHA_ERR_TIMEOUT in
+ * *status_dev (required, a DEVICE int the caller zeroes first), drains the
+ * copies and tensor-core products it has in flight, frees its tensor memory
+ * and returns; the output is unspecified.  The context stays usable: a
+ * following call on the same stream computes normally.  A CTA with fewer
+ * than skip_tile + 1 key tiles completes normally.  Returns MHA_OK when the
+ * launch succeeded (the timeout is reported on the device), argument errors
+ * as sdpa_forward (here every extent must be positive).
+ */
+mha_status sdpa_forward_timeout_drill(const void *q, const void *k, const void *v, void *o,
+                                      int B, int h, int T_q, int T_k, float scale,
+                                      mha_mask mask, const int32_t *key_lens,
+                                      unsigned long long wait_limit_ns, int skip_tile,
+                                      int *status_dev, cudaStream_t stream);
+
+/*
  * sdpa_forward (bf16 only) that also writes, per query row, the log-sum-exp of
  * its visible scores,
  *   lse[b, h, i] = log sum_{j visible} exp(scale * q_i . k_j)   (natural log),
@@ -115,6 +136,11 @@ int sdpa_bf16_key_split(int T_q, int T_k, mha_mask mask);
  * backward pass needs to recompute the weights.  lse: DEVICE fp32 array of
  * B*h*T_q entries (required when the problem is not empty); -inf for a row
  * with no visible key.  MHA_F32 returns MHA_ERR_UNSUPPORTED.
+ * The value is the log of the normaliser the output was divided by: the sum
+ * of the bf16-rounded weights the P.V product used, so it lies within the
+ * relative bf16 rounding (2^-8) of the exact sum, |lse - exact| <= 2^-8 plus
+ * fp32 rounding, and is consistent with o (exp(lse) o is the weighted value
+ * sum the kernel formed, as a merge of partial results over key ranges needs).
  */
 mha_status sdpa_forward_lse(mha_dtype dt, const void *q, const void *k, const void *v, void *o,
                             float *lse, int B, int h, int T_q, int T_k, int d_k, int d_v,
@@ -314,14 +340,19 @@ mha_status mha_forward_add_layernorm(mha_dtype dt, const void *x_q, const void *
  * MHA_ERR_WORKSPACE and launch nothing.  Every GPU that loads the library
  * holds those 32 MiB until the process exits.
  *
- * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current) and caches it; make that
- * first call before any stream capture.  A failure there returns
- * MHA_ERR_CUDA.  All calls on a device share the one array and it keeps the
- * previous call's contents (every byte read is written earlier in the same
- * call, so nothing needs clearing): calls that overlap on the GPU -- on
- * different streams, or from different host threads -- race on it and must
- * be serialised by the caller.  Other arguments and errors as mha_forward.
+ * Arguments are checked first, exactly as mha_forward checks them (errors
+ * and the empty-problem MHA_OK come back before any device work).  Then every
+ * call looks up the array's device address (cudaGetSymbolAddress, on the
+ * caller's current device and context); nothing is cached, so the call stays
+ * valid after cudaDeviceReset or under another context.  The first call in a
+ * context is the one that loads the library's device code there (the
+ * runtime's set-up), so make that first call before any stream capture.  A
+ * failed lookup returns MHA_ERR_CUDA with the detail in mha_last_error().
+ * All calls on a device share the one array and it keeps the previous call's
+ * contents (every byte read is written earlier in the same call, so nothing
+ * needs clearing): calls that overlap on the GPU -- on different streams, or
+ * from different host threads -- race on it and must be serialised by the
+ * caller.  Other arguments and errors as mha_forward.
  */
 #define MHA_STATIC_WORKSPACE_BYTES (32u << 20)
 mha_status mha_forward_static_workspace(mha_dtype dt, const void *x_q, const void *x_kv,

@@ -251,3 +251,25 @@ def test_bf16_key_split_rule(lib):
     assert split(256, 1024, 2) == 1                                  # padding is not counted
     assert split(0, 1024, 0) == 0 and split(64, 0, 0) == 0           # empty problems
     assert split(-1, 8, 0) == -1 and split(8, 8, 7) == -1
+
+
+def drill(lib, q=FAKE, B=1, h=1, Tq=512, Tk=512, mask=0, lens=None, limit=2_000_000, skip=0,
+          status=FAKE):
+    return lib.lib.sdpa_forward_timeout_drill(q, FAKE, FAKE, FAKE, B, h, Tq, Tk, 0.125, mask, lens,
+                                              limit, skip, status, None)
+
+
+def test_timeout_drill_rejects_bad_arguments(lib):
+    """The failure-detection drill checks its arguments on the host: it needs
+    a status word, a wait limit between 0.1 ms and 1 s, a tile index >= 0 and
+    a non-empty problem."""
+    assert drill(lib, status=None) == lib.MHA_ERR_INVALID_ARG
+    assert drill(lib, limit=0) == lib.MHA_ERR_INVALID_ARG
+    assert drill(lib, limit=99_999) == lib.MHA_ERR_INVALID_ARG
+    assert drill(lib, limit=2_000_000_000) == lib.MHA_ERR_INVALID_ARG
+    assert drill(lib, skip=-1) == lib.MHA_ERR_INVALID_ARG
+    assert drill(lib, B=0) == lib.MHA_ERR_INVALID_ARG
+    assert drill(lib, Tk=0) == lib.MHA_ERR_INVALID_ARG
+    assert drill(lib, mask=2, lens=None) == lib.MHA_ERR_INVALID_ARG
+    assert drill(lib, q=None) == lib.MHA_ERR_INVALID_ARG
+    assert drill(lib, q=FAKE + 8) == lib.MHA_ERR_MISALIGNED

@@ -24,6 +24,8 @@ SIGNATURES = {
     "sdpa_forward_lse": (_ci, [_ci, _vp, _vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _ci, _ci, _cf,
                                _ci, _vp, _vp, _vp]),
     "sdpa_bf16_key_split": (_ci, [_ci, _ci, _ci]),
+    "sdpa_forward_timeout_drill": (_ci, [_vp, _vp, _vp, _vp, _ci, _ci, _ci, _ci, _cf, _ci, _vp,
+                                         ctypes.c_ulonglong, _ci, _vp, _vp]),
     "sdpa_forward_host_workspace_bytes": (_sz, [_ci, _ci, _ci, _ci, _ci, _ci, _ci]),
     "sdpa_forward_host": (_ci, [_ci, _vp, _vp, _vp, _vp, _vp, _sz, _ci, _ci, _ci, _ci, _ci, _ci,
                                 _cf, _ci, _vp, _vp, _vp]),

@@ -146,7 +146,8 @@ mha_status run_attention_bf16(const void *q, const void *k, const void *v, void 
                               long long o_sb, long long o_sh, long long o_st, int B, int h,
                               int T_q, int T_k, float scale, int mask, const int32_t *key_lens,
                               int *status_dev, cudaStream_t stream, float *lse = nullptr,
-                              bool pdl = false) {
+                              bool pdl = false, unsigned long long drill_wait_limit_ns = 0,
+                              int drill_skip_tile = 0) {
     CUtensorMap tq, tk, tv;
     const long long BH = static_cast<long long>(B) * h;
     mha_status s;
@@ -175,6 +176,8 @@ mha_status run_attention_bf16(const void *q, const void *k, const void *v, void 
     if (items >= (1ll << 30)) return MHA_ERR_UNSUPPORTED;
     p.total_items = static_cast<int>(items);
     p.status = status_dev;
+    p.wait_limit_ns = drill_wait_limit_ns;
+    p.drill_skip_tile = drill_skip_tile;
     return launch_status(mha::launch_attn_bf16(tq, tk, tv, p, stream, pdl), "attention launch");
 }
 
@@ -195,6 +198,10 @@ MHA_EXPORT const char *mha_status_string(mha_status status) {
 
 MHA_EXPORT const char *mha_last_error(void) { return g_last_error; }
 
+namespace mha {
+mha_status record_cuda_failure(const char *what, const char *detail) { return cuda_fail(what, detail); }
+}  // namespace mha
+
 namespace {
 
 mha_status sdpa_impl(mha_dtype dt, const void *q, const void *k, const void *v, void *o,
@@ -210,7 +217,7 @@ mha_status sdpa_impl(mha_dtype dt, const void *q, const void *k, const void *v, 
     if (lse && dt != MHA_BF16) return dt == MHA_F32 ? MHA_ERR_UNSUPPORTED : MHA_ERR_INVALID_ARG;
     if (dt == MHA_F32) {
         if (d_k > 128 || d_v > 128) return MHA_ERR_UNSUPPORTED;
-        if ((T_q + 3) / 4 > 65535) return MHA_ERR_UNSUPPORTED;
+        if ((T_q + mha::kF32RowsPerCta - 1) / mha::kF32RowsPerCta > 65535) return MHA_ERR_UNSUPPORTED;
         return launch_status(mha::launch_sdpa_f32(
             static_cast<const float *>(q), static_cast<const float *>(k),
             static_cast<const float *>(v), static_cast<float *>(o), B, h, T_q, T_k, d_k, d_v,
@@ -234,6 +241,25 @@ MHA_EXPORT mha_status sdpa_forward(mha_dtype dt, const void *q, const void *k, c
                                    int *status_dev, cudaStream_t stream) {
     return sdpa_impl(dt, q, k, v, o, nullptr, B, h, T_q, T_k, d_k, d_v, scale, mask, key_lens,
                      status_dev, stream);
+}
+
+MHA_EXPORT mha_status sdpa_forward_timeout_drill(const void *q, const void *k, const void *v,
+                                                void *o, int B, int h, int T_q, int T_k,
+                                                float scale, mha_mask mask,
+                                                const int32_t *key_lens,
+                                                unsigned long long wait_limit_ns, int skip_tile,
+                                                int *status_dev, cudaStream_t stream) {
+    if (B <= 0 || h <= 0 || T_q <= 0 || T_k <= 0 || skip_tile < 0) return MHA_ERR_INVALID_ARG;
+    if (!valid_mask(mask) || !isfinite(scale)) return MHA_ERR_INVALID_ARG;
+    if ((mask & MHA_MASK_KEY_PADDING) && !key_lens) return MHA_ERR_INVALID_ARG;
+    if (wait_limit_ns < 100000ull || wait_limit_ns > 1000000000ull) return MHA_ERR_INVALID_ARG;
+    if (!q || !k || !v || !o || !status_dev) return MHA_ERR_INVALID_ARG;
+    if (static_cast<long long>(B) * h >= (1ll << 31)) return MHA_ERR_UNSUPPORTED;
+    if ((T_q + mha::kAttnRowsPerCta - 1) / mha::kAttnRowsPerCta > 65535) return MHA_ERR_UNSUPPORTED;
+    if (!aligned16(q) || !aligned16(o) || !aligned16(k) || !aligned16(v)) return MHA_ERR_MISALIGNED;
+    const long long so_t = 64, so_h = static_cast<long long>(T_q) * 64, so_b = so_h * h;
+    return run_attention_bf16(q, k, v, o, so_b, so_h, so_t, B, h, T_q, T_k, scale, mask, key_lens,
+                              status_dev, stream, nullptr, false, wait_limit_ns, skip_tile + 1);
 }
 
 MHA_EXPORT mha_status sdpa_forward_lse(mha_dtype dt, const void *q, const void *k, const void *v,

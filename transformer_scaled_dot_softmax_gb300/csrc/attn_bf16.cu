@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = sm.tmem_base;
-    const AbortState ab{&sm.abort_flag, p.status};
+    const AbortState ab{&sm.abort_flag, p.status, p.wait_limit_ns};
     // Programmatic dependent launch: the next kernel may begin its prologue;
     // nothing below touches global memory written by the kernel before this
     // one until that kernel has completed.
@@ -264,6 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int st = g % STAGES;
                     if (g >= STAGES && !(ok = mbar_wait(&sm.kv_empty[st], ((g / STAGES) - 1) & 1, ab)))
                         break;
+                    if (g + 1 == p.drill_skip_tile) continue;  // drill: this stage never fills
                     mbar_arrive_expect_tx(&sm.kv_full[st], 2 * kTileBytes);
                     tma_load_3d(&tmap_k, &sm.kv_full[st], sm.k[st], 0, j * BN, it.bh);
                     tma_load_3d(&tmap_v, &sm.kv_full[st], sm.v[st], 0, j * BN, it.bh);
@@ -272,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Let every copy still in flight land before the CTA exits (on the
             // normal path these phases completed long ago).
             for (int x = max(0, g - STAGES); x < g; ++x)
-                mbar_wait_drain(&sm.kv_full[x % STAGES], (x / STAGES) & 1);
+                if (x + 1 != p.drill_skip_tile) mbar_wait_drain(&sm.kv_full[x % STAGES], (x / STAGES) & 1);
             for (int x = max(0, v - 2); x < v; ++x) mbar_wait_drain(&sm.q_full[x & 1], (x >> 1) & 1);
         }
     } else if (warp == kMmaSWarp) {
@@ -420,28 +421,33 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         };
         // P = 2^(s c - mc) in bf16 (column c of the packed tile holds keys
-        // 2c, 2c+1 of the round) and the fp32 row sum of P.  Packed fp32x2
-        // FMA / add (one instruction per two scores) keep the instruction
-        // count -- and the issue slots taken from the MMA warps -- down.
+        // 2c, 2c+1 of the round) and the fp32 row sum of P.  The sum adds
+        // the bf16-rounded weights -- the values the P.V product multiplies
+        // -- so numerator and denominator of the output carry the same
+        // rounding and the normalised weights sum to 1: a key that dominates
+        // its row returns its value row up to the output rounding, whatever
+        // the reference maximum (with l summed from the unrounded weights
+        // the output would be off by the relative rounding of the dominant
+        // weight, up to 2^-8 |v|); the rounded weights are added by
+        // mixed-precision adds (bf16 operand, fp32 sum), one instruction per
+        // weight.  Packed fp32x2 FMA (one instruction per two scores) keeps
+        // the instruction count -- and the issue slots taken from the MMA
+        // warps -- down.
         auto exp_tile = [C](const uint32_t(&a)[32], const uint32_t(&b)[32], float mc,
                             uint32_t(&pk)[32]) -> float {
             const uint64_t c2 = f32x2_pack(C, C), nmc2 = f32x2_pack(-mc, -mc);
-            uint64_t acc2[4] = {0ull, 0ull, 0ull, 0ull};
+            float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
                 float x0, x1, x2, x3;
                 f32x2_unpack(fma_f32x2(f32x2_pack(u2f(a[2 * c]), u2f(a[2 * c + 1])), c2, nmc2), x0, x1);
                 f32x2_unpack(fma_f32x2(f32x2_pack(u2f(b[2 * c]), u2f(b[2 * c + 1])), c2, nmc2), x2, x3);
-                const float e0 = ex2_approx(x0), e1 = ex2_approx(x1);
-                const float e2 = ex2_approx(x2), e3 = ex2_approx(x3);
-                acc2[c & 1] = add_f32x2(acc2[c & 1], f32x2_pack(e0, e1));
-                acc2[2 + (c & 1)] = add_f32x2(acc2[2 + (c & 1)], f32x2_pack(e2, e3));
-                pk[c] = pack_bf16x2(e0, e1);
-                pk[16 + c] = pack_bf16x2(e2, e3);
+                pk[c] = pack_bf16x2(ex2_approx(x0), ex2_approx(x1));
+                pk[16 + c] = pack_bf16x2(ex2_approx(x2), ex2_approx(x3));
+                add_bf16x2_to_f32(acc[2 * (c & 1)], acc[2 * (c & 1) + 1], pk[c]);
+                add_bf16x2_to_f32(acc[4 + 2 * (c & 1)], acc[5 + 2 * (c & 1)], pk[16 + c]);
             }
-            float u0, u1;
-            f32x2_unpack(add_f32x2(add_f32x2(acc2[0], acc2[1]), add_f32x2(acc2[2], acc2[3])), u0, u1);
-            return u0 + u1;
+            return ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
         };
         // Row maximum of the round's 64 scores: four chains of three-input max.
         auto row_max = [](const uint32_t(&a)[32], const uint32_t(&b)[32]) -> float {
@@ -637,6 +643,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float fa = wa * inv, fb = wb * inv;
             // Log-sum-exp of the row's visible scores: sum_j 2^(s_j c) =
             // 2^(M c) L with c = scale log2(e), so lse = M scale + ln L.
+            // L sums the bf16-rounded weights (the normaliser of the output),
+            // within a relative 2^-8 of the exact sum.
             if (lse_row) *lse_row = L > 0.f ? M * p.scale + logf(L) : -INFINITY;
 #pragma unroll
             for (int part = 0; part < 2; ++part) {

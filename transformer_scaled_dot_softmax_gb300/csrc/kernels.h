@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "../../include/mha.h"
+
 namespace mha {
 
 constexpr int kMaskCausalBit = 1;
@@ -56,6 +58,11 @@ struct AttnParams {
     int num_qblocks;   // ceil(Tq / rows per item)
     int total_items;   // B * H * num_qblocks work items (query tiles)
     int *status;
+    // Failure-detection drill only (both 0 on every product path): the wait
+    // limit in ns (0: the default 1 s), and n > 0 makes every CTA's loader
+    // issue no copy for its (n-1)-th key tile, so the waits on it run out.
+    unsigned long long wait_limit_ns;
+    int drill_skip_tile;
 };
 constexpr int kAttnRowsPerCta = 128;  // one work item = one 128-row query tile
 constexpr int kAttnHeadDim = 64;
@@ -115,6 +122,7 @@ cudaError_t launch_posenc_add_bf16(const __nv_bfloat16 *x, __nv_bfloat16 *out, l
                                    int D, int pos0, cudaStream_t stream);
 
 // ------------------------------------------------ fp32 SIMT attention
+constexpr int kF32RowsPerCta = 8;  // query rows per CTA (one warp each)
 cudaError_t launch_sdpa_f32(const float *q, const float *k, const float *v, float *o, int B,
                             int H, int Tq, int Tk, int dk, int dv, float scale, int mask,
                             const int32_t *key_lens, cudaStream_t stream);
@@ -154,6 +162,10 @@ cudaError_t launch_gemm_bf16(const CUtensorMap (&a)[kGemmMaxProblems],
 
 // Number of SMs of the current device.
 cudaError_t sm_count(int *sms);
+
+// Records "what: detail" as the calling thread's mha_last_error() text and
+// returns MHA_ERR_CUDA.
+mha_status record_cuda_failure(const char *what, const char *detail);
 
 // ------------------------------------ output projection + residual + LayerNorm
 constexpr int kLnMaxCluster = 8;  // CTAs per 128-row block (portable cluster size)

@@ -2,72 +2,124 @@
 //
 // The full-precision path: o = softmax(scale * q k^T + mask) v with fp32
 // FFMA dot products and expf (no tensor cores: TF32 would round q and k to
-// 10 mantissa bits).  One warp per query row; lane l owns feature columns
-// l, l+32, l+64, l+96.  Keys are visited in order with a running maximum
-// and sum (online softmax: the partial output is rescaled by
-// exp(m_old - m_new) whenever the maximum grows), which equals the textbook
+// 10 mantissa bits).  The softmax is taken online over chunks of 32 keys:
+// per chunk the row's maximum, the partial output and sum rescaled by
+// exp(m_old - m_new) when the maximum grows, which equals the textbook
 // softmax up to rounding ("Attention Is All You Need" (azimuth.plus), "The
 // same idea in code": subtract the row maximum, exponentiate, normalise).
-// Masked keys are never visited, i.e. they get exactly zero weight
-// (notebook chapter, "Masked Attention in the Decoder").
+// Masked keys get weight exactly zero (notebook chapter, "Masked Attention in
+// the Decoder"): causal keys past the row and padded keys are never scored.
+//
+// One CTA per (b, h) and block of kF32RowsPerCta query rows, one warp per
+// row.  Each chunk of 32 key and value rows is first copied into shared
+// memory by the whole CTA -- every load of the chunk in flight at once, so a
+// chunk costs one memory round trip instead of one per key -- and then
+// serves all the CTA's rows: lane j scores key j of the chunk (K rows padded
+// by one float so the 32 lanes read 32 different banks), the warp reduces
+// the chunk's maximum and sum with shuffles, and lane l accumulates output
+// columns l, l+32, l+64, l+96 from the value rows.
 #include "kernels.h"
 
 namespace mha {
 namespace {
 
-constexpr int kRowsPerCta = 4;  // one warp per row
-constexpr int kMaxPerLane = 4;  // d_k, d_v <= 128
+constexpr int kRows = kF32RowsPerCta;  // one warp per query row
+constexpr int kChunk = 32;             // keys per shared-memory chunk (one per lane)
+constexpr int kMaxD = 128;             // d_k, d_v <= 128
+constexpr int kMaxPerLane = kMaxD / 32;
 
-__global__ void __launch_bounds__(kRowsPerCta * 32)
+__global__ void __launch_bounds__(kRows * 32)
     sdpa_f32_kernel(const float *__restrict__ q, const float *__restrict__ k,
                     const float *__restrict__ v, float *__restrict__ o, int H, int Tq, int Tk,
                     int dk, int dv, float scale, int mask, const int32_t *__restrict__ key_lens) {
+    __shared__ float ks[kChunk][kMaxD + 1];
+    __shared__ float vs[kChunk][kMaxD];
+    __shared__ float qs[kRows][kMaxD];
+
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const long long bh = blockIdx.x;
     const int b = static_cast<int>(bh / H);
-    const int row = blockIdx.y * kRowsPerCta + warp;
-    if (row >= Tq) return;
+    const int row0 = blockIdx.y * kRows;
+    const int row = row0 + warp;
+    const bool live = row < Tq;
 
-    int end = Tk;
-    if ((mask & kMaskPaddingBit) && key_lens) end = min(max(key_lens[b], 0), Tk);
-    if (mask & kMaskCausalBit) end = min(end, row + 1);
+    int kv_len = Tk;
+    if ((mask & kMaskPaddingBit) && key_lens) kv_len = min(max(key_lens[b], 0), Tk);
+    const bool causal = (mask & kMaskCausalBit) != 0;
+    // Keys this row sees, and keys any row of the CTA sees.
+    const int end = live ? (causal ? min(kv_len, row + 1) : kv_len) : 0;
+    const int last_row = min(row0 + kRows, Tq) - 1;
+    const int cta_end = causal ? min(kv_len, last_row + 1) : kv_len;
 
-    const float *qr = q + (bh * Tq + row) * dk;
-    float qv[kMaxPerLane], acc[kMaxPerLane];
-#pragma unroll
-    for (int i = 0; i < kMaxPerLane; ++i) {
-        const int c = lane + 32 * i;
-        qv[i] = c < dk ? qr[c] : 0.f;
-        acc[i] = 0.f;
+    if (live) {
+        const float *qr = q + (bh * Tq + row) * dk;
+        for (int c = lane; c < dk; c += 32) qs[warp][c] = qr[c];
     }
+    float acc[kMaxPerLane];
+#pragma unroll
+    for (int i = 0; i < kMaxPerLane; ++i) acc[i] = 0.f;
     float m = -INFINITY, l = 0.f;
+
     const float *kb = k + bh * Tk * dk;
     const float *vb = v + bh * Tk * dv;
-    for (int j = 0; j < end; ++j) {
-        const float *kr = kb + static_cast<long long>(j) * dk;
-        float part = 0.f;
-#pragma unroll
-        for (int i = 0; i < kMaxPerLane; ++i) {
-            const int c = lane + 32 * i;
-            if (c < dk) part = fmaf(qv[i], kr[c], part);
+    for (int c0 = 0; c0 < cta_end; c0 += kChunk) {
+        const int n = min(kChunk, cta_end - c0);
+        __syncthreads();  // the previous chunk (and, first time, q) is consumed / written
+        {
+            const float *ksrc = kb + static_cast<long long>(c0) * dk;
+            const float *vsrc = vb + static_cast<long long>(c0) * dv;
+            const int nk = n * dk, nv = n * dv;
+#pragma unroll 4
+            for (int x = threadIdx.x; x < nk; x += kRows * 32) {
+                const int j = x / dk;
+                ks[j][x - j * dk] = ksrc[x];
+            }
+#pragma unroll 4
+            for (int x = threadIdx.x; x < nv; x += kRows * 32) {
+                const int j = x / dv;
+                vs[j][x - j * dv] = vsrc[x];
+            }
         }
+        __syncthreads();
+        if (c0 >= end) continue;  // this row sees none of the chunk's keys
+        // Lane j: score of key c0 + j (-inf past the row's visible keys).
+        float s = -INFINITY;
+        if (c0 + lane < end) {
+            float part[4] = {0.f, 0.f, 0.f, 0.f};  // four chains for ILP
+            int c = 0;
+            for (; c + 4 <= dk; c += 4) {
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) part += __shfl_xor_sync(0xffffffffu, part, off);
-        const float s = part * scale;
-        const float m_new = fmaxf(m, s);
-        const float alpha = expf(m - m_new);  // 0 on the first key
-        const float pj = expf(s - m_new);
-        l = l * alpha + pj;
-        const float *vr = vb + static_cast<long long>(j) * dv;
+                for (int u = 0; u < 4; ++u) part[u] = fmaf(qs[warp][c + u], ks[lane][c + u], part[u]);
+            }
+            for (; c < dk; ++c) part[0] = fmaf(qs[warp][c], ks[lane][c], part[0]);
+            s = ((part[0] + part[1]) + (part[2] + part[3])) * scale;
+        }
+        float mc = s;
 #pragma unroll
-        for (int i = 0; i < kMaxPerLane; ++i) {
-            const int c = lane + 32 * i;
-            if (c < dv) acc[i] = fmaf(pj, vr[c], acc[i] * alpha);
+        for (int off = 16; off > 0; off >>= 1) mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, off));
+        const float m_new = fmaxf(m, mc);  // finite: key c0 is visible
+        const float alpha = expf(m - m_new);  // 0 for the row's first chunk
+        const float pj = expf(s - m_new);     // 0 for masked keys
+        float ps = pj;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, off);
+        l = l * alpha + ps;
+#pragma unroll
+        for (int i = 0; i < kMaxPerLane; ++i) acc[i] *= alpha;
+        const int nj = min(n, end - c0);
+        for (int j = 0; j < nj; ++j) {
+            const float pb = __shfl_sync(0xffffffffu, pj, j);
+#pragma unroll
+            for (int i = 0; i < kMaxPerLane; ++i) {
+                const int c = lane + 32 * i;
+                if (c < dv) acc[i] = fmaf(pb, vs[j][c], acc[i]);
+            }
         }
         m = m_new;
     }
-    const float inv = l > 0.f ? 1.0f / l : 0.f;
+    if (!live) return;
+    const float inv = l > 0.f ? 1.0f / l : 0.f;  // no visible key: zeros
     float *orow = o + (bh * Tq + row) * dv;
 #pragma unroll
     for (int i = 0; i < kMaxPerLane; ++i) {
@@ -81,10 +133,9 @@ __global__ void __launch_bounds__(kRowsPerCta * 32)
 cudaError_t launch_sdpa_f32(const float *q, const float *k, const float *v, float *o, int B,
                             int H, int Tq, int Tk, int dk, int dv, float scale, int mask,
                             const int32_t *key_lens, cudaStream_t stream) {
-    dim3 grid(static_cast<unsigned>(B * H),
-              static_cast<unsigned>((Tq + kRowsPerCta - 1) / kRowsPerCta));
-    sdpa_f32_kernel<<<grid, kRowsPerCta * 32, 0, stream>>>(q, k, v, o, H, Tq, Tk, dk, dv, scale,
-                                                          mask, key_lens);
+    dim3 grid(static_cast<unsigned>(B * H), static_cast<unsigned>((Tq + kRows - 1) / kRows));
+    sdpa_f32_kernel<<<grid, kRows * 32, 0, stream>>>(q, k, v, o, H, Tq, Tk, dk, dv, scale, mask,
+                                                    key_lens);
     return cudaGetLastError();
 }
 

@@ -82,8 +82,9 @@ __device__ __forceinline__ bool mbar_try_wait_suspend(uint64_t *bar, uint32_t pa
 
 // Per-CTA abort state shared by all waits of one kernel instance.
 struct AbortState {
-    volatile int *cta_flag;  // shared memory
-    int *status;             // caller's device status word (may be null)
+    volatile int *cta_flag;      // shared memory
+    int *status;                 // caller's device status word (may be null)
+    unsigned long long limit_ns; // wait limit; 0: kWaitLimitNs
 };
 
 __device__ __forceinline__ void raise_abort(const AbortState &ab) {
@@ -103,11 +104,12 @@ __device__ __forceinline__ bool should_abort(const AbortState &ab) {
 // Slow path of mbar_wait: polls with a time limit.
 static __device__ __noinline__ bool mbar_wait_slow(uint64_t *bar, uint32_t parity, AbortState ab) {
     const unsigned long long t0 = global_timer_ns();
+    const unsigned long long limit = ab.limit_ns ? ab.limit_ns : kWaitLimitNs;
     for (uint32_t it = 1;; ++it) {
         if (mbar_try_wait_suspend(bar, parity, kSuspendNs)) return true;
         if ((it & 3u) == 0) {
             if (should_abort(ab)) return false;
-            if (global_timer_ns() - t0 > kWaitLimitNs) {
+            if (global_timer_ns() - t0 > limit) {
                 raise_abort(ab);
                 return false;
             }
@@ -501,6 +503,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     uint32_t r;
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
     return r;
+}
+
+// lo += low bf16 half of `r`, hi += high half, each in fp32 (the bf16 value
+// enters exactly; one mixed-precision add per half, sm_100 and later).
+__device__ __forceinline__ void add_bf16x2_to_f32(float &lo, float &hi, uint32_t r) {
+    asm("{\n\t.reg .b16 l, h;\n\t"
+        "mov.b32 {l, h}, %2;\n\t"
+        "add.rn.f32.bf16 %0, l, %0;\n\t"
+        "add.rn.f32.bf16 %1, h, %1;\n\t}"
+        : "+f"(lo), "+f"(hi)
+        : "r"(r));
 }
 
 }  // namespace mha
