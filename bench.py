@@ -163,6 +163,49 @@ def time_oracle(x, w: si.Workload, stride: int, offset: int = 0):
     return flops / dt / 1e12, dt, len(rows), oracle.num_threads()
 
 
+def visible_keys(w: si.Workload, key_lens, b: np.ndarray, t: np.ndarray) -> np.ndarray:
+    """Visible keys of query row t of batch entry b."""
+    L = np.full(len(b), w.T_k) if key_lens is None else np.clip(np.asarray(key_lens)[b], 0, w.T_k)
+    return np.minimum(t + 1, L) if w.mask & si.MASK_CAUSAL else L
+
+
+def oracle_attention_by_workload(target_flops: float = 1.5e9):
+    """The oracle's scaled dot-product attention on the attention shapes of
+    workloads 1-4 (seeded N(0,1) Q/K/V of the projected (B, h, T, 64) shape,
+    the workload's mask and key lengths), timed on one thread and on all
+    cores over the same row sample: every n-th row, n chosen so the sample
+    holds about `target_flops` (about a second on one core)."""
+    import oracle
+    cores = oracle.num_threads()
+    res = {}
+    try:
+        for idx in range(4):
+            wl = si.WORKLOADS[idx]
+            w = si.WORKLOADS[4].replace(B=wl.B, h=wl.h, T_q=wl.T_q, T_k=wl.T_k, d_k=wl.d_k,
+                                        d_v=wl.d_v, mask=wl.mask, len_lo=wl.len_lo,
+                                        len_hi=wl.len_hi, seed=wl.seed, name=wl.name)
+            x = si.make_inputs(w)
+            nrows = w.B * w.h * w.T_q
+            b_of = np.arange(nrows) // (w.h * w.T_q)
+            t_of = np.arange(nrows) % w.T_q
+            per_row = 2.0 * (w.d_k + w.d_v) * visible_keys(w, x["key_lens"], b_of, t_of)
+            stride = max(1, int(per_row.sum() / target_flops))
+            rows = np.arange(0, nrows, stride, dtype=np.int64)
+            fl = float(per_row[rows].sum())
+            entry = {"rows": int(len(rows)), "of_rows": nrows}
+            for threads in (1, cores):
+                oracle.set_num_threads(threads)
+                t0 = time.perf_counter()
+                oracle.sdpa_rows(x["q"], x["k"], x["v"], rows, scale=w.scale, mask=w.mask,
+                                 key_lens=x["key_lens"])
+                dt = time.perf_counter() - t0
+                entry["threads_%d" % threads] = {"tflops": fl / dt / 1e12, "seconds": dt}
+            res[wl.name] = entry
+    finally:
+        oracle.set_num_threads(cores)
+    return res
+
+
 def run_reference(args, rank: int, world: int) -> int:
     if rank != 0:
         return 0
@@ -272,6 +315,19 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> int:
     ms_mean = max_over_ranks(float(ms.mean()), dist, dev)
     value = whole_job_value(flops, world, ms_mean)
 
+    # Beside the cold-L2 figure: the same launches back to back without the
+    # flush (Q, K, V, O = 128 MiB, about the size of L2, stay partly resident).
+    n_warm = min(args.steps, 100)
+    ws_, we_ = ([torch.cuda.Event(enable_timing=True) for _ in range(n_warm)] for _ in range(2))
+    for i in range(n_warm):
+        ws_[i].record(stream)
+        step()
+        we_[i].record(stream)
+    torch.cuda.synchronize(dev)
+    warm_ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in zip(ws_, we_)])), dist, dev)
+    warm = {"ms_mean": warm_ms, "value": whole_job_value(flops, world, warm_ms), "unit": UNIT,
+            "steps": n_warm, "l2": "not flushed between steps"}
+
     # End to end through the public API with host buffers: pinned host Q/K/V
     # -> device, attention, output -> pinned host, every step.
     e2e = None
@@ -282,7 +338,7 @@ def run_gpu(args, rank: int, world: int, local_rank: int) -> int:
     if rank == 0 and not args.no_other_workloads:
         others = time_other_workloads(dev, stream, flush)
     if rank == 0:
-        emit(args, w, x, ms, ms_mean, value, flops, world, clocks, e2e, others)
+        emit(args, w, x, ms, ms_mean, value, flops, world, clocks, e2e, others, warm)
     if dist is not None:
         dist.destroy_process_group()
     return 0
@@ -466,7 +522,7 @@ def run_e2e(args, q, k, v, out, w, stream, dev, dist, flops, world):
             "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
 
 
-def emit(args, w, x, ms, ms_mean, value, flops, world, clocks, e2e, others=None):
+def emit(args, w, x, ms, ms_mean, value, flops, world, clocks, e2e, others=None, warm=None):
     peaks, peak_src = load_peaks()
     peak = float(peaks["bf16_tflops"])
     achieved = flops / (float(ms.mean()) * 1e-3) / 1e12
@@ -476,7 +532,8 @@ def emit(args, w, x, ms, ms_mean, value, flops, world, clocks, e2e, others=None)
         cpu = {"value": cv, "unit": UNIT, "cores": cores, "kind": "oracle",
                "sample": "all %d (batch, head) pairs x every %d-th query row of the causal "
                          "T=8192 triangle (%d rows, %.1f s), fp64"
-                         % (w.B * w.h, args.oracle_stride, cn, cdt)}
+                         % (w.B * w.h, args.oracle_stride, cn, cdt),
+               "attention_by_workload": oracle_attention_by_workload()}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_mean,
@@ -495,6 +552,7 @@ def emit(args, w, x, ms, ms_mean, value, flops, world, clocks, e2e, others=None)
         "gpu_launches": args.steps,
         "clocks": clocks.summary(),
         "ms_min": float(ms.min()), "ms_median": float(np.median(ms)),
+        "warm_l2": warm,
         "other_workloads": others,
     }
     print(json.dumps(line), flush=True)

@@ -64,7 +64,9 @@ typedef enum {
     MHA_ERR_WORKSPACE = 3,   /* workspace NULL or smaller than mha_workspace_bytes() */
     MHA_ERR_MISALIGNED = 4,  /* a bf16 pointer is not 16-byte aligned (TMA rule) */
     MHA_ERR_CUDA = 5,        /* a CUDA runtime/driver call or a launch failed */
-    MHA_ERR_TIMEOUT = 6      /* written to *status_dev by a kernel whose wait ran out */
+    MHA_ERR_TIMEOUT = 6,     /* written to *status_dev by a kernel whose wait ran out */
+    MHA_ERR_BOUNDS = 7       /* written to *status_dev by a device-side bounds check; only a
+                                library built with MHA_BOUNDS_CHECK has the checks */
 } mha_status;
 
 typedef enum {

@@ -55,6 +55,8 @@ def _load():
         lib.oracle_add_layernorm.restype = ci
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = ci
+        lib.oracle_set_num_threads.argtypes = [ci]
+        lib.oracle_set_num_threads.restype = None
         _lib = lib
     return _lib
 
@@ -78,6 +80,12 @@ def _lens(key_lens, B):
 
 def num_threads() -> int:
     return int(_load().oracle_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads for the following calls (timing only; results do not depend
+    on it)."""
+    _load().oracle_set_num_threads(int(n))
 
 
 def sdpa(q, k, v, scale=None, mask=MASK_NONE, key_lens=None, return_weights=False):

@@ -527,3 +527,14 @@ int oracle_num_threads(void)
     return 1;
 #endif
 }
+
+/* Threads the next calls use (the benchmark times the oracle on one thread
+ * as well as on all cores); n < 1 is ignored.  No arithmetic depends on it. */
+void oracle_set_num_threads(int n)
+{
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}

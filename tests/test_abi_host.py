@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for code in range(7):
+    for code in range(8):
         s = lib.lib.mha_status_string(code)
         assert s and s != b"unknown status"
     assert lib.lib.mha_status_string(99) == b"unknown status"

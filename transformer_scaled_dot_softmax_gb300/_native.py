@@ -8,10 +8,12 @@ import ctypes
 import os
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "_build", "libmha.so")
+# MHA_LIBRARY may name another build of this same library (the tests load the
+# build with device-side bounds checks that way); by default the in-tree build.
+LIB_PATH = os.environ.get("MHA_LIBRARY") or os.path.join(_HERE, "_build", "libmha.so")
 
 MHA_OK, MHA_ERR_INVALID_ARG, MHA_ERR_UNSUPPORTED, MHA_ERR_WORKSPACE = 0, 1, 2, 3
-MHA_ERR_MISALIGNED, MHA_ERR_CUDA, MHA_ERR_TIMEOUT = 4, 5, 6
+MHA_ERR_MISALIGNED, MHA_ERR_CUDA, MHA_ERR_TIMEOUT, MHA_ERR_BOUNDS = 4, 5, 6, 7
 MHA_F32, MHA_BF16 = 0, 1
 MHA_STATIC_WORKSPACE_BYTES = 32 << 20
 MHA_MASK_NONE, MHA_MASK_CAUSAL, MHA_MASK_KEY_PADDING, MHA_MASK_CAUSAL_KEY_PADDING = 0, 1, 2, 3

@@ -16,6 +16,12 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libmha.so")
+# The same library with device-side bounds checks compiled in (MHA_BOUNDS_CHECK):
+# every TMA coordinate and direct global store of the kernels that report
+# through a status word is checked, a failed check records MHA_ERR_BOUNDS and
+# skips the access.  For testing; never loaded unless asked for.
+CHECKED_OUT_DIR = os.path.join(HERE, "_build_checked")
+CHECKED_LIB = os.path.join(CHECKED_OUT_DIR, "libmha.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC",
@@ -39,22 +45,25 @@ def _deps():
         os.path.join(CSRC, "*.h")) + glob.glob(os.path.join(INCLUDE, "*.h"))
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(OUT_DIR, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), checked: bool = False) -> str:
+    out_dir, lib = (CHECKED_OUT_DIR, CHECKED_LIB) if checked else (OUT_DIR, LIB)
+    if checked:
+        extra_flags = tuple(extra_flags) + ("-DMHA_BOUNDS_CHECK",)
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(out_dir, exist_ok=True)
     nvcc = _nvcc()
     objs = []
 
     def compile_one(src):
-        obj = os.path.join(OUT_DIR, os.path.basename(src).replace(".cu", ".o"))
+        obj = os.path.join(out_dir, os.path.basename(src).replace(".cu", ".o"))
         cmd = [nvcc, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -65,15 +74,16 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
         objs = list(ex.map(compile_one, _sources()))
-    tmp = LIB + ".tmp.%d" % os.getpid()
+    tmp = lib + ".tmp.%d" % os.getpid()
     cmd = [nvcc, "-shared", *ARCH, "-o", tmp, *objs, "-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n%s\n%s" % (r.stdout, r.stderr))
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     print(build(force="--force" in sys.argv, verbose="-v" in sys.argv,
-                extra_flags=["-Xptxas", "-v"] if "--ptxas-v" in sys.argv else []))
+                extra_flags=["-Xptxas", "-v"] if "--ptxas-v" in sys.argv else [],
+                checked="--checked" in sys.argv))

@@ -192,6 +192,7 @@ MHA_EXPORT const char *mha_status_string(mha_status status) {
         case MHA_ERR_MISALIGNED: return "pointer not 16-byte aligned";
         case MHA_ERR_CUDA: return "CUDA error";
         case MHA_ERR_TIMEOUT: return "kernel wait timed out";
+        case MHA_ERR_BOUNDS: return "device-side bounds check failed";
     }
     return "unknown status";
 }

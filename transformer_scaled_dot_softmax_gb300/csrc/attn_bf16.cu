@@ -123,6 +123,9 @@ constexpr uint32_t kTileBytes = BM * HD * 2;  // 16 KiB, one 128 x 64 bf16 tile
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 384;  // O_A [384,448), O_B [448,512)
 constexpr float kTileSumLimit = 65536.0f;  // 2^16: a tile sum above it takes the exact step
+// Per-batch key lengths are read from the CTA's shared-memory copy when it
+// holds them all (B <= kLensCache), else from global memory.
+constexpr int kLensCache = 1024;
 
 struct __align__(1024) SmemAttn {
     uint8_t q[2][kTileBytes];
@@ -143,6 +146,7 @@ struct __align__(1024) SmemAttn {
     uint64_t o_final;            // both groups' P.V products of an item complete
     uint64_t o_free;             // accumulators read (4 output warps)
     uint64_t drain[3];           // one per MMA-issuing warp
+    int lens[kLensCache];        // key_lens[0 .. B) when B <= kLensCache
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -163,7 +167,7 @@ __device__ __forceinline__ int item_index(int t, int c, int G) {
     return t * G + ((t & 1) ? (G - 1 - c) : c);
 }
 
-__device__ __forceinline__ Item make_item(const AttnParams &p, int k) {
+__device__ __forceinline__ Item make_item(const AttnParams &p, int k, const int *lens_smem) {
     Item it;
     const int BH = p.B * p.H;
     const int qb = p.num_qblocks - 1 - k / BH;
@@ -172,7 +176,8 @@ __device__ __forceinline__ Item make_item(const AttnParams &p, int k) {
     it.hh = it.bh - it.b * p.H;
     it.q0 = qb * BM;
     int kv_len = p.Tk;
-    if ((p.mask & kMaskPaddingBit) && p.key_lens) kv_len = min(max(p.key_lens[it.b], 0), p.Tk);
+    if ((p.mask & kMaskPaddingBit) && p.key_lens)
+        kv_len = min(max(p.B <= kLensCache ? lens_smem[it.b] : p.key_lens[it.b], 0), p.Tk);
     it.kv_len = kv_len;
     const int kv_end = (p.mask & kMaskCausalBit) ? min(kv_len, min(it.q0 + BM, p.Tq)) : kv_len;
     it.n_kv = (kv_end + BN - 1) / BN;
@@ -223,6 +228,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(&sm.tmem_base, kTmemCols);
         tmem_relinquish();
     }
+    // The key lengths are an input of the call that no kernel of the call
+    // writes, so they may be read before waiting for the previous kernel;
+    // every role looks them up per item, and a global load there would sit on
+    // each item's critical path.
+    if ((p.mask & kMaskPaddingBit) && p.key_lens && p.B <= kLensCache)
+        for (int i = threadIdx.x; i < p.B; i += kThreads) sm.lens[i] = p.key_lens[i];
     if (warp == kLoadWarp && lane == 0) {
         prefetch_tensormap(&tmap_q);
         prefetch_tensormap(&tmap_k);
@@ -237,6 +248,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // nothing below touches global memory written by the kernel before this
     // one until that kernel has completed.
     pdl_launch_dependents();
+    // Read the parameters every role needs for its first item now, while the
+    // previous kernel drains: the first reads of the parameter block miss the
+    // constant cache (~1,500 cycles measured at the start of each role).
+    asm volatile("" ::"r"(p.B), "r"(p.H), "r"(p.Tq), "r"(p.Tk), "r"(p.num_qblocks), "r"(p.mask),
+                 "r"(p.total_items), "f"(p.scale_log2), "l"(p.key_lens), "l"(p.o), "l"(p.status));
     pdl_wait();
 
     // Every role walks the same item list and counts, over the items that
@@ -251,14 +267,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int t = 0; ok; ++t) {
                 const int k = item_index(t, cta, G);
                 if (k >= total) break;
-                const Item it = make_item(p, k);
+                const Item it = make_item(p, k, sm.lens);
                 if (it.n_kv == 0) continue;
                 const int qbuf = v & 1;
                 // Q buffer qbuf last served item v-2: wait until all of its
                 // score products have completed.
                 if (v >= 2 && !(ok = mbar_wait(&sm.q_empty[qbuf], ((v - 2) >> 1) & 1, ab))) break;
                 mbar_arrive_expect_tx(&sm.q_full[qbuf], kTileBytes);
-                tma_load_3d(&tmap_q, &sm.q_full[qbuf], sm.q[qbuf], 0, it.q0, it.bh);
+                if (in_bounds(it.q0 >= 0 && it.q0 < p.Tq && it.bh >= 0 && it.bh < p.B * p.H, p.status))
+                    tma_load_3d(&tmap_q, &sm.q_full[qbuf], sm.q[qbuf], 0, it.q0, it.bh);
                 ++v;
                 for (int j = 0; j < it.n_kv; ++j, ++g) {
                     const int st = g % STAGES;
@@ -266,8 +283,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         break;
                     if (g + 1 == p.drill_skip_tile) continue;  // drill: this stage never fills
                     mbar_arrive_expect_tx(&sm.kv_full[st], 2 * kTileBytes);
-                    tma_load_3d(&tmap_k, &sm.kv_full[st], sm.k[st], 0, j * BN, it.bh);
-                    tma_load_3d(&tmap_v, &sm.kv_full[st], sm.v[st], 0, j * BN, it.bh);
+                    if (in_bounds(j * BN < p.Tk && it.bh < p.B * p.H, p.status)) {
+                        tma_load_3d(&tmap_k, &sm.kv_full[st], sm.k[st], 0, j * BN, it.bh);
+                        tma_load_3d(&tmap_v, &sm.kv_full[st], sm.v[st], 0, j * BN, it.bh);
+                    }
                 }
             }
             // Let every copy still in flight land before the CTA exits (on the
@@ -295,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; ok; ++t) {
             const int k = item_index(t, cta, G);
             if (k >= total) break;
-            const Item it = make_item(p, k);
+            const Item it = make_item(p, k, sm.lens);
             if (it.n_kv == 0) continue;
             const int qbuf = v & 1;
             if (!(ok = warp_wait(&sm.q_full[qbuf], (v >> 1) & 1, ab))) break;
@@ -347,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; ok; ++t) {
             const int k = item_index(t, cta, G);
             if (k >= total) break;
-            const Item it = make_item(p, k);
+            const Item it = make_item(p, k, sm.lens);
             if (it.n_kv == 0) continue;
             if (v >= 1 && !(ok = warp_wait(&sm.o_free, (v - 1) & 1, ab))) break;
             for (int j = 0; j < it.n_kv; ++j, ++g) {
@@ -468,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; ok; ++t) {
             const int k = item_index(t, cta, G);
             if (k >= total) break;
-            const Item it = make_item(p, k);
+            const Item it = make_item(p, k, sm.lens);
             if (it.n_kv == 0) continue;
             const int row = it.q0 + r;  // query index
             const int row_lim = causal ? min(it.kv_len, row + 1) : it.kv_len;  // keys < row_lim visible
@@ -612,7 +631,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int t = 0; ok; ++t) {
             const int k = item_index(t, cta, G);
             if (k >= total) break;
-            const Item it = make_item(p, k);
+            const Item it = make_item(p, k, sm.lens);
             const int row = it.q0 + r;
             __nv_bfloat16 *dst = p.o + it.b * p.o_stride_b + it.hh * p.o_stride_h +
                                  static_cast<long long>(row) * p.o_stride_t;
@@ -620,8 +639,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             float *lse_row = p.lse && row < p.Tq
                                  ? p.lse + (static_cast<long long>(it.bh) * p.Tq + row)
                                  : nullptr;
+            // The row's output lies inside the (B, H, T_q) index space.
+            const bool row_ok = in_bounds(it.b < p.B && it.hh < p.H && row >= 0, p.status);
+            if (!row_ok) lse_row = nullptr;
             if (it.n_kv == 0) {
-                if (row < p.Tq) {
+                if (row < p.Tq && row_ok) {
 #pragma unroll
                     for (int c = 0; c < 8; ++c) d4[c] = make_uint4(0u, 0u, 0u, 0u);
                     if (lse_row) *lse_row = -INFINITY;
@@ -660,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&sm.o_free);
                 }
-                if (row < p.Tq) {
+                if (row < p.Tq && row_ok) {
                     uint32_t packed[16];
 #pragma unroll
                     for (int c = 0; c < 16; ++c)

@@ -275,8 +275,10 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         // -------------------------------------------------------------- TMA
         if (lane == 0 && n_j > 0) {
             mbar_arrive_expect_tx(&sm.kv_full, 2 * kTile);
-            tma_load_3d(&tmap_k, &sm.kv_full, sm.k, 0, k0, bh);
-            tma_load_3d(&tmap_v, &sm.kv_full, sm.v, 0, k0, bh);
+            if (in_bounds(k0 < p.Tk && bh < p.B * p.H, p.status)) {
+                tma_load_3d(&tmap_k, &sm.kv_full, sm.k, 0, k0, bh);
+                tma_load_3d(&tmap_v, &sm.kv_full, sm.v, 0, k0, bh);
+            }
             int issued = 0;
             for (int t = 0; t < n_j; ++t) {
                 const int st = t & 1;
@@ -284,13 +286,18 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const int j = j_begin + t;
                 const long long vrow = static_cast<long long>(bh) * p.Tq_pad + j * BQ;
                 mbar_arrive_expect_tx(&sm.stage_full[st], 2 * kTile + 2 * BQ * 4);
-                tma_load_3d(&tmap_q, &sm.stage_full[st], sm.q[st], 0, j * BQ, bh);
-                bulk_load_1d(sm.nlse2[st], p.nlse2 + vrow, BQ * 4, &sm.stage_full[st]);
-                bulk_load_1d(sm.dvec[st], p.dvec + vrow, BQ * 4, &sm.stage_full[st]);
+                // query block j of (B*H, T_q_pad) rows: the row terms are padded
+                // to whole blocks, the Q / dO maps clip at T_q
+                const bool j_ok = in_bounds(j * BQ < p.Tq && j * BQ + BQ <= p.Tq_pad, p.status);
+                if (j_ok) {
+                    tma_load_3d(&tmap_q, &sm.stage_full[st], sm.q[st], 0, j * BQ, bh);
+                    bulk_load_1d(sm.nlse2[st], p.nlse2 + vrow, BQ * 4, &sm.stage_full[st]);
+                    bulk_load_1d(sm.dvec[st], p.dvec + vrow, BQ * 4, &sm.stage_full[st]);
+                }
                 issued = t + 1;
                 // dO_j last: its slot frees later (after (3))
                 if (t >= 2 && !mbar_wait(&sm.g_empty[st], ((t >> 1) - 1) & 1, ab)) break;
-                tma_load_3d(&tmap_g, &sm.stage_full[st], sm.g[st], 0, j * BQ, bh);
+                if (j_ok) tma_load_3d(&tmap_g, &sm.stage_full[st], sm.g[st], 0, j * BQ, bh);
             }
             mbar_wait_drain(&sm.kv_full, 0);
             for (int x = max(0, issued - 2); x < issued; ++x)
@@ -412,6 +419,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             // lanes' vectors are 512 contiguous bytes
             float *dst = p.dq_acc + (static_cast<long long>(bh) * p.Tq_pad + (j_begin + u) * BQ + lane_base) * HD +
                          512 * c + 4 * lane;
+            if (!in_bounds((j_begin + u) * BQ + BQ <= p.Tq_pad && bh < p.B * p.H, p.status)) return true;
 #pragma unroll
             for (int x = 0; x < 4; ++x)
                 red_add_v4(dst + 128 * x, __uint_as_float(a[4 * x]), __uint_as_float(a[4 * x + 1]),
@@ -486,7 +494,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 #pragma unroll
                 for (int e = 0; e < 32; ++e) a[e] = 0u;
             }
-            if (key < p.Tk) {
+            if (key < p.Tk && in_bounds(key >= 0 && bh < p.B * p.H, p.status)) {
                 const float f = is_dv ? 1.f : p.scale;
                 __nv_bfloat16 *dst = (is_dv ? p.dv : p.dk) + (static_cast<long long>(bh) * p.Tk + key) * HD + f0;
                 uint32_t w[16];

@@ -160,8 +160,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (kg >= STAGES && !(ok = mbar_wait(&sm.empty[st], ((kg / STAGES) - 1) & 1, ab)))
                         break;
                     mbar_arrive_expect_tx(&sm.full[st], kABytes + kBBytes);
-                    tma_load_2d(ta, &sm.full[st], sm.a[st], kb * BK, t.tm * BM);
-                    tma_load_3d(tb, &sm.full[st], sm.b[st], 0, kb * BK, t.tn * (BN / 64));
+                    const GemmProblem &pr = p.prob[t.pi];
+                    if (in_bounds(kb * BK < pr.K && t.tm * BM < pr.M && t.tn * BN < pr.N, p.status)) {
+                        tma_load_2d(ta, &sm.full[st], sm.a[st], kb * BK, t.tm * BM);
+                        tma_load_3d(tb, &sm.full[st], sm.b[st], 0, kb * BK, t.tn * (BN / 64));
+                    }
                 }
             }
             // Let every copy still in flight land before the CTA exits.
@@ -289,7 +292,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             *reinterpret_cast<uint4 *>(sm.ys[j >> 3] + rr * 128 + (((j & 7) ^ (rr & 7)) << 4)) =
                                 make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
                         }
-                    } else if (m < pr.M && n0 < pr.N) {
+                    } else if (m < pr.M && n0 < pr.N &&
+                               in_bounds(pr.out_mode != kOutHeadSplit || (n0 >> 6) < pr.H, p.status)) {
                         __nv_bfloat16 *dst;
                         if (pr.out_mode == kOutHeadSplit) {
                             const int head = n0 >> 6, c0 = n0 & 63;
@@ -313,6 +317,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int bx = 0; bx < 2; ++bx) {
                             const int nb = t.tn * BN + grp * 128 + 64 * bx;
                             if (nb >= pr.N) break;
+                            if (!in_bounds(t.tm * BM < pr.M && (pr.out_mode != kOutHeadSplit ||
+                                                                (nb >> 6) < pr.H), p.status))
+                                break;
                             if (pr.out_mode == kOutHeadSplit) {
                                 const int m0 = t.tm * BM, bb = m0 / pr.T;
                                 tma_store_3d(ty, sm.ys[bx], 0, m0 - bb * pr.T, bb * pr.H + (nb >> 6));

@@ -184,16 +184,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
             mbar_arrive_expect_tx(&sm.x_full, (BN / 64) * kXBox);
+            const bool tile_ok = in_bounds(tm * BM < p.M && n_base + BN <= p.D, p.status);
 #pragma unroll
             for (int bx = 0; bx < BN / 64; ++bx)
-                tma_load_2d(&tx, &sm.x_full, sm.xs[bx], n_base + 64 * bx, tm * BM);
+                if (tile_ok) tma_load_2d(&tx, &sm.x_full, sm.xs[bx], n_base + 64 * bx, tm * BM);
             int issued = 0;
             for (int kb = 0; kb < num_k; ++kb) {
                 const int st = kb % STAGES;
                 if (kb >= STAGES && !mbar_wait(&sm.empty[st], ((kb / STAGES) - 1) & 1, ab)) break;
                 mbar_arrive_expect_tx(&sm.full[st], kABytes + kBBytes);
-                tma_load_2d(&ta, &sm.full[st], sm.a[st], kb * BK, tm * BM);
-                tma_load_3d(&tb, &sm.full[st], sm.b[st], 0, kb * BK, n_base / 64);
+                if (tile_ok && in_bounds(kb * BK < p.K, p.status)) {
+                    tma_load_2d(&ta, &sm.full[st], sm.a[st], kb * BK, tm * BM);
+                    tma_load_3d(&tb, &sm.full[st], sm.b[st], 0, kb * BK, n_base / 64);
+                }
                 issued = kb + 1;
             }
             for (int x = max(0, issued - STAGES); x < issued; ++x)
@@ -336,7 +339,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (warp == 2 && lane == 0) {
             if (!*ab.cta_flag) {
 #pragma unroll
-                for (int bx = 0; bx < BN / 64; ++bx) tma_store_2d(&ty, sm.xs[bx], n_base + 64 * bx, tm * BM);
+                for (int bx = 0; bx < BN / 64; ++bx)
+                    if (in_bounds(tm * BM < p.M && n_base + 64 * bx < p.D, p.status))
+                        tma_store_2d(&ty, sm.xs[bx], n_base + 64 * bx, tm * BM);
                 bulk_commit_group();
             }
             bulk_wait_all();

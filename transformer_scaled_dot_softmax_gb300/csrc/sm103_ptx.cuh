@@ -15,6 +15,20 @@
 namespace mha {
 
 constexpr int kStatusTimeout = 6;  // == MHA_ERR_TIMEOUT
+constexpr int kStatusBounds = 7;   // == MHA_ERR_BOUNDS
+
+// Device-side bounds checks.  In a build compiled with MHA_BOUNDS_CHECK,
+// in_bounds(ok, status) records MHA_ERR_BOUNDS in the caller's status word
+// (first error wins) when `ok` is false, and the call site skips the access
+// it guards; in every other build it is `true` and the check compiles away.
+#ifdef MHA_BOUNDS_CHECK
+__device__ __forceinline__ bool in_bounds(bool ok, int *status) {
+    if (!ok && status) atomicCAS(status, 0, kStatusBounds);
+    return ok;
+}
+#else
+__device__ __forceinline__ constexpr bool in_bounds(bool, int *) { return true; }
+#endif
 // A wait that has not completed after this long is treated as a hang.
 constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
 // Longest single hardware suspension inside a wait (the thread resumes as soon
