@@ -188,6 +188,34 @@ def test_config5_every_element(lib):
     check_bf16(got, ref, "config 5, every element")
 
 
+LONG_SHAPES = [
+    # one head, a causal sequence 8x longer than the largest workload (131,328 score tiles)
+    (1, 1, 65536, 65536, si.MASK_CAUSAL),
+    # a short query block against a very long, padded key sequence (1,024 key tiles per item)
+    (2, 1, 200, 131072, si.MASK_KEY_PADDING),
+]
+
+
+@pytest.mark.parametrize("B,h,T_q,T_k,mask", LONG_SHAPES)
+def test_bf16_long_sequences_sampled_rows(lib, B, h, T_q, T_k, mask):
+    """Sequence lengths far past the workloads (the kernel has no length
+    limit below 2^31 / 128 query tiles): the rows the oracle can afford --
+    the first and last rows, every query-tile boundary region and a seeded
+    sample -- are compared element by element."""
+    w = si.WORKLOADS[4].replace(B=B, h=h, T_q=T_q, T_k=T_k, mask=mask, len_lo=T_k // 2,
+                                len_hi=T_k, seed=37)
+    x = si.make_inputs(w)
+    got = host(run_sdpa_bf16(lib, w, x))
+    rng = np.random.default_rng(37)
+    t = np.unique(np.concatenate([[0, 1, 127, 128, 129, T_q // 2, T_q - 2, T_q - 1],
+                                  rng.integers(0, T_q, 120)]))
+    t = t[t < T_q]
+    flat = (np.arange(B * h)[:, None] * T_q + t[None, :]).reshape(-1)
+    ref = oracle.sdpa_rows(x["q"], x["k"], x["v"], flat, scale=w.scale, mask=mask,
+                           key_lens=x["key_lens"])
+    check_bf16(got.reshape(-1, w.d_v)[flat], ref, "long B%d Tq%d Tk%d" % (B, T_q, T_k))
+
+
 def test_bf16_padding_rows_bitwise_independent_of_masked_keys(lib):
     w = si.WORKLOADS[4].replace(B=3, h=2, T_q=200, T_k=600, mask=si.MASK_KEY_PADDING,
                                 len_lo=100, len_hi=500, seed=31)
