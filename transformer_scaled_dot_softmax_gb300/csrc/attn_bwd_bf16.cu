@@ -156,12 +156,14 @@ __device__ __forceinline__ void softmax_terms(const uint32_t (&sv)[N], const uin
 //               Computing S and dP transposed puts the keys on the
 //               tensor-memory lanes, so P^T feeds (3) straight from tensor
 //               memory.  Issue order: (1) and (2) of block j+1 as soon as
-//               block j's softmax terms are written, then (4), (3) and (5) of
-//               block j -- the tensor pipe runs in issue order, so no product
-//               of block j stands between its softmax terms and block j+1's
-//               scores.  (4) reads dS^T from shared memory rather than tensor
-//               memory for that reason: in tensor memory it would have to sit
-//               over dP^T's columns, and (2) of block j+1 would wait for it.
+//               the softmax warps have loaded block j's S^T and dP^T into
+//               registers (they overwrite those columns while the terms of
+//               block j are still being computed), then (4), (3) and (5) of
+//               block j once its terms are written -- no product of block j
+//               stands between its softmax terms and block j+1's scores.
+//               (4) reads dS^T from shared memory rather than tensor memory
+//               for that reason: in tensor memory it would have to sit over
+//               dP^T's columns, and (2) of block j+1 would wait for it.
 //   warps 2-17  one thread per (key, chunk of 32 queries) -- warp w takes the
 //               keys of lane quadrant w%4 and chunk (w-2)/4:
 //               P^T = 2^(S^T c - lse_j) (masked: 0), dS^T = P^T (dP^T - D_j),
@@ -199,6 +201,7 @@ struct __align__(1024) SmemBwd {
     uint64_t q_empty[2];  // (1), (4) have read Q_j (and the softmax lse_j, D_j)
     uint64_t g_empty[2];  // (2), (3) have read dO_j
     uint64_t sdp_full;   // (1), (2) complete
+    uint64_t sdp_read;   // S^T, dP^T loaded into registers (16 warps)
     uint64_t pds_full;   // P^T (tensor memory), dS (shared memory) written (16 warps)
     uint64_t tmem_free;  // (4) of the block complete
     uint64_t p_free;     // (3) complete: the P^T columns reusable
@@ -241,6 +244,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         }
         mbar_init(&sm.p_free, 1);
         mbar_init(&sm.sdp_full, 1);
+        mbar_init(&sm.sdp_read, kSoftmaxWarps);
         mbar_init(&sm.pds_full, kSoftmaxWarps);
         mbar_init(&sm.tmem_free, 1);
         mbar_init(&sm.dq_full, 1);
@@ -351,17 +355,21 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             for (int t = 0; ok && t < n_j; ++t) {
                 const int st = t & 1;
                 const uint64_t so = static_cast<uint64_t>(st) * kT;  // q[st], g[st] stage offset
-                if (!(ok = warp_wait(&sm.pds_full, t & 1, ab))) break;
-                tc_fence_after_sync();
                 if (t + 1 < n_j) {
-                    // the next block's scores first: the softmax terms of
-                    // block t have read S^T and dP^T
+                    // The next block's scores as soon as the softmax warps
+                    // have loaded block t's S^T and dP^T into registers: they
+                    // run on the tensor pipe while the softmax terms of block t
+                    // are still being computed (the terms go to P^T's own
+                    // columns and to shared memory, not over S^T or dP^T).
+                    if (!(ok = warp_wait(&sm.sdp_read, t & 1, ab))) break;
                     if (!(ok = warp_wait(&sm.stage_full[st ^ 1], ((t + 1) >> 1) & 1, ab))) break;
                     tc_fence_after_sync();
                     score_s(st ^ 1);
                     score_dp(st ^ 1);
                     warp_commit(&sm.sdp_full);
                 }
+                if (!(ok = warp_wait(&sm.pds_full, t & 1, ab))) break;
+                tc_fence_after_sync();
                 // (4) from dS^T in shared memory
                 const uint64_t dso = static_cast<uint64_t>(st) * (2 * kT);
 #pragma unroll
@@ -446,6 +454,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 const int lim = key_ok ? (causal ? key - (q0 + 16 * h) : 0) : 16;
                 tmem_ld_wait(sv);
                 tmem_ld_wait(dp);
+                if (h == 1) {
+                    // this warp's S^T and dP^T columns are all in registers
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&sm.sdp_read);
+                }
                 uint32_t pk[8], dsk[8];
                 const float *l2 = sm.nlse2[st] + 32 * c + 16 * h, *dv = sm.dvec[st] + 32 * c + 16 * h;
                 if (__all_sync(0xffffffffu, lim <= 0))
