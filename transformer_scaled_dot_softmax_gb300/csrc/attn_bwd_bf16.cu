@@ -143,7 +143,7 @@ __device__ __forceinline__ void softmax_terms(const uint32_t (&sv)[N], const uin
 //
 //   warp 0      TMA: the K and V blocks once; per query block Q_j, dO_j (3-D
 //               tensor maps) and its 128 lse and D values (bulk copies) into
-//               a 2-stage ring.
+//               a 3-stage ring.
 //   warp 1      MMA issuer (whole warp, elected lane), per query block:
 //                 (1) S^T  = K Q_j^T     M=128 keys, N=128 queries, K=64
 //                 (2) dP^T = V dO_j^T    same shape
@@ -187,19 +187,20 @@ constexpr uint32_t kTile = BQ * HD * 2;  // 16 KiB
 constexpr uint32_t kColS = 0, kColDP = 128, kColP = 256, kColDV = 320, kColDK = 384, kColDQ = 448;
 constexpr int kBwdThreads = 576;
 constexpr int kSoftmaxWarps = 16;
+constexpr int kStages = 3;  // Q_j / dO_j / lse_j / D_j ring
 
 struct __align__(1024) SmemBwd {
     uint8_t k[kTile];
     uint8_t v[kTile];
-    uint8_t q[2][kTile];
-    uint8_t g[2][kTile];      // dO
+    uint8_t q[kStages][kTile];
+    uint8_t g[kStages][kTile];  // dO
     uint8_t ds[2][2 * kTile]; // dS, the A operand of (4) and (5): 2 blocks of 64 queries x 128 key rows
-    float nlse2[2][BQ];
-    float dvec[2][BQ];
+    float nlse2[kStages][BQ];
+    float dvec[kStages][BQ];
     uint64_t kv_full;
-    uint64_t stage_full[2];
-    uint64_t q_empty[2];  // (1), (4) have read Q_j (and the softmax lse_j, D_j)
-    uint64_t g_empty[2];  // (2), (3) have read dO_j
+    uint64_t stage_full[kStages];
+    uint64_t q_empty[kStages];  // (1), (4) have read Q_j (and the softmax lse_j, D_j)
+    uint64_t g_empty[kStages];  // (2), (3) have read dO_j
     uint64_t sdp_full;   // (1), (2) complete
     uint64_t sdp_read;   // S^T, dP^T loaded into registers (16 warps)
     uint64_t pds_full;   // P^T (tensor memory), dS (shared memory) written (16 warps)
@@ -237,7 +238,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(&sm.kv_full, 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kStages; ++i) {
             mbar_init(&sm.stage_full[i], 1);
             mbar_init(&sm.q_empty[i], 1);
             mbar_init(&sm.g_empty[i], 1);
@@ -285,8 +286,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             }
             int issued = 0;
             for (int t = 0; t < n_j; ++t) {
-                const int st = t & 1;
-                if (t >= 2 && !mbar_wait(&sm.q_empty[st], ((t >> 1) - 1) & 1, ab)) break;
+                const int st = t % kStages, use = t / kStages;
+                if (t >= kStages && !mbar_wait(&sm.q_empty[st], (use - 1) & 1, ab)) break;
                 const int j = j_begin + t;
                 const long long vrow = static_cast<long long>(bh) * p.Tq_pad + j * BQ;
                 mbar_arrive_expect_tx(&sm.stage_full[st], 2 * kTile + 2 * BQ * 4);
@@ -300,12 +301,12 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 }
                 issued = t + 1;
                 // dO_j last: its slot frees later (after (3))
-                if (t >= 2 && !mbar_wait(&sm.g_empty[st], ((t >> 1) - 1) & 1, ab)) break;
+                if (t >= kStages && !mbar_wait(&sm.g_empty[st], (use - 1) & 1, ab)) break;
                 if (j_ok) tma_load_3d(&tmap_g, &sm.stage_full[st], sm.g[st], 0, j * BQ, bh);
             }
             mbar_wait_drain(&sm.kv_full, 0);
-            for (int x = max(0, issued - 2); x < issued; ++x)
-                mbar_wait_drain(&sm.stage_full[x & 1], (x >> 1) & 1);
+            for (int x = max(0, issued - kStages); x < issued; ++x)
+                mbar_wait_drain(&sm.stage_full[x % kStages], (x / kStages) & 1);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------- MMA
@@ -326,8 +327,8 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
             constexpr uint64_t kDsMn = static_cast<uint64_t>((kTile >> 4) - 1) << 16;
             const uint64_t v_km = k_km + kT;
             const uint64_t q_km = k_km + 2 * kT;
-            const uint64_t g_km = k_km + 4 * kT;
-            const uint64_t ds_km0 = k_km + 6 * kT;
+            const uint64_t g_km = k_km + (2 + kStages) * kT;
+            const uint64_t ds_km0 = k_km + (2 + 2 * kStages) * kT;
             const uint64_t q_mn = q_km + kMn;
             const uint64_t g_mn = g_km + kMn;
             const uint64_t k_mn = k_km + kMn;
@@ -353,7 +354,7 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                 warp_commit(&sm.sdp_full);
             }
             for (int t = 0; ok && t < n_j; ++t) {
-                const int st = t & 1;
+                const int st = t % kStages, nst = (t + 1) % kStages;
                 const uint64_t so = static_cast<uint64_t>(st) * kT;  // q[st], g[st] stage offset
                 if (t + 1 < n_j) {
                     // The next block's scores as soon as the softmax warps
@@ -362,16 +363,16 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     // are still being computed (the terms go to P^T's own
                     // columns and to shared memory, not over S^T or dP^T).
                     if (!(ok = warp_wait(&sm.sdp_read, t & 1, ab))) break;
-                    if (!(ok = warp_wait(&sm.stage_full[st ^ 1], ((t + 1) >> 1) & 1, ab))) break;
+                    if (!(ok = warp_wait(&sm.stage_full[nst], ((t + 1) / kStages) & 1, ab))) break;
                     tc_fence_after_sync();
-                    score_s(st ^ 1);
-                    score_dp(st ^ 1);
+                    score_s(nst);
+                    score_dp(nst);
                     warp_commit(&sm.sdp_full);
                 }
                 if (!(ok = warp_wait(&sm.pds_full, t & 1, ab))) break;
                 tc_fence_after_sync();
                 // (4) from dS^T in shared memory
-                const uint64_t dso = static_cast<uint64_t>(st) * (2 * kT);
+                const uint64_t dso = static_cast<uint64_t>(t & 1) * (2 * kT);
 #pragma unroll
                 for (int kk = 0; kk < BQ / 16; ++kk)
                     warp_mma_bf16_ss(tmem + kColDK, ds_km0 + dso + (kk >> 2) * kT + 2 * (kk & 3),
@@ -393,10 +394,9 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
                     warp_mma_bf16_ss(tmem + kColDQ, ds_mn + dso + 128 * kk, k_mn + 128 * kk, id_q,
                                      kk > 0 ? 1u : 0u);
                 warp_commit(&sm.dq_full);
-                // (4) of this block complete before the next: it has long
-                // finished when the next block's softmax terms arrive, and
-                // the wait keeps the kernel within its 96 registers without
-                // spills (without it ptxas spills 12 bytes).
+                // (4) of this block complete before the next block's
+                // scores are issued: it has long finished by then, and the
+                // kernel measured slightly faster with the wait than without.
                 if (!(ok = warp_wait(&sm.tmem_free, t & 1, ab))) break;
             }
             if (ok) warp_commit(&sm.acc_done);
@@ -436,14 +436,14 @@ __global__ void __launch_bounds__(kBwdThreads, 1)
         };
         bool ok = true;
         for (int t = 0; t < n_j; ++t) {
-            const int st = t & 1;
+            const int st = t % kStages;
             const int q0 = (j_begin + t) * BQ + 32 * c;
             ok = __all_sync(0xffffffffu, mbar_wait(&sm.sdp_full, t & 1, ab)) &&
-                 __all_sync(0xffffffffu, mbar_wait(&sm.stage_full[st], (t >> 1) & 1, ab));
+                 __all_sync(0xffffffffu, mbar_wait(&sm.stage_full[st], (t / kStages) & 1, ab));
             if (!ok) break;
             tc_fence_after_sync();
             // two halves of 16 query columns, 32 registers in flight each
-            uint8_t *blk = sm.ds[st] + (c >> 1) * kTile + r * 128;
+            uint8_t *blk = sm.ds[t & 1] + (c >> 1) * kTile + r * 128;
 #pragma unroll 1
             for (int h = 0; h < 2; ++h) {
                 const uint32_t col = 32u * c + 16u * h;
