@@ -28,10 +28,15 @@ constexpr int kChunk = 32;             // keys per shared-memory chunk (one per 
 constexpr int kMaxD = 128;             // d_k, d_v <= 128
 constexpr int kMaxPerLane = kMaxD / 32;
 
+// DK = 64: head dimensions fixed at compile time (the common case: constant
+// loop bounds, no per-feature range checks); DK = 0: d_k, d_v <= 128 at run
+// time.
+template <int DK>
 __global__ void __launch_bounds__(kRows * 32)
     sdpa_f32_kernel(const float *__restrict__ q, const float *__restrict__ k,
                     const float *__restrict__ v, float *__restrict__ o, int H, int Tq, int Tk,
-                    int dk, int dv, float scale, int mask, const int32_t *__restrict__ key_lens) {
+                    int dk_rt, int dv_rt, float scale, int mask, const int32_t *__restrict__ key_lens) {
+    const int dk = DK ? DK : dk_rt, dv = DK ? DK : dv_rt;
     __shared__ float ks[kChunk][kMaxD + 1];
     __shared__ float vs[kChunk][kMaxD];
     __shared__ float qs[kRows][kMaxD];
@@ -134,8 +139,12 @@ cudaError_t launch_sdpa_f32(const float *q, const float *k, const float *v, floa
                             int H, int Tq, int Tk, int dk, int dv, float scale, int mask,
                             const int32_t *key_lens, cudaStream_t stream) {
     dim3 grid(static_cast<unsigned>(B * H), static_cast<unsigned>((Tq + kRows - 1) / kRows));
-    sdpa_f32_kernel<<<grid, kRows * 32, 0, stream>>>(q, k, v, o, H, Tq, Tk, dk, dv, scale, mask,
-                                                    key_lens);
+    if (dk == 64 && dv == 64)
+        sdpa_f32_kernel<64><<<grid, kRows * 32, 0, stream>>>(q, k, v, o, H, Tq, Tk, dk, dv, scale, mask,
+                                                            key_lens);
+    else
+        sdpa_f32_kernel<0><<<grid, kRows * 32, 0, stream>>>(q, k, v, o, H, Tq, Tk, dk, dv, scale, mask,
+                                                           key_lens);
     return cudaGetLastError();
 }
 
