@@ -39,7 +39,7 @@ __global__ void __launch_bounds__(kRows * 32)
     const int dk = DK ? DK : dk_rt, dv = DK ? DK : dv_rt;
     __shared__ float ks[kChunk][kMaxD + 1];
     __shared__ float vs[kChunk][kMaxD];
-    __shared__ float qs[kRows][kMaxD];
+    __shared__ __align__(16) float qs[kRows][kMaxD];
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -92,12 +92,23 @@ __global__ void __launch_bounds__(kRows * 32)
         float s = -INFINITY;
         if (c0 + lane < end) {
             float part[4] = {0.f, 0.f, 0.f, 0.f};  // four chains for ILP
-            int c = 0;
-            for (; c + 4 <= dk; c += 4) {
+            if constexpr (DK > 0) {
 #pragma unroll
-                for (int u = 0; u < 4; ++u) part[u] = fmaf(qs[warp][c + u], ks[lane][c + u], part[u]);
+                for (int c = 0; c < DK; c += 4) {
+                    const float4 q4 = *reinterpret_cast<const float4 *>(&qs[warp][c]);
+                    part[0] = fmaf(q4.x, ks[lane][c], part[0]);
+                    part[1] = fmaf(q4.y, ks[lane][c + 1], part[1]);
+                    part[2] = fmaf(q4.z, ks[lane][c + 2], part[2]);
+                    part[3] = fmaf(q4.w, ks[lane][c + 3], part[3]);
+                }
+            } else {
+                int c = 0;
+                for (; c + 4 <= dk; c += 4) {
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) part[u] = fmaf(qs[warp][c + u], ks[lane][c + u], part[u]);
+                }
+                for (; c < dk; ++c) part[0] = fmaf(qs[warp][c], ks[lane][c], part[0]);
             }
-            for (; c < dk; ++c) part[0] = fmaf(qs[warp][c], ks[lane][c], part[0]);
             s = ((part[0] + part[1]) + (part[2] + part[3])) * scale;
         }
         float mc = s;
