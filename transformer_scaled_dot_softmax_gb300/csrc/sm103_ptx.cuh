@@ -461,7 +461,7 @@ __device__ __forceinline__ void warp_commit(uint64_t *bar) {
         : "memory");
 }
 
-// All lanes wait; the warp leaves converged with one common verdict.
+// All lanes wait; the warp leaves converged with one common result.
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const AbortState &ab) {
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, ab));
 }
