@@ -47,6 +47,9 @@ def _load():
         lib.oracle_sdpa_backward.argtypes = [dp, dp, dp, dp, dp, dp, dp, ci, ci, ci, ci, ci, cd,
                                              ci, ip]
         lib.oracle_sdpa_backward.restype = ci
+        lib.oracle_sdpa_backward_tail.argtypes = [dp, dp, dp, dp, dp, dp, dp, ci, ci, ci, ci, ci,
+                                                  cd, ci, ip, ci]
+        lib.oracle_sdpa_backward_tail.restype = ci
         lib.oracle_positional_encoding.argtypes = [dp, ci, ci, ci]
         lib.oracle_positional_encoding.restype = ci
         lib.oracle_ffn.argtypes = [dp, dp, dp, dp, dp, dp, cl, ci, ci]
@@ -222,6 +225,30 @@ def sdpa_backward(q, k, v, dout, scale=None, mask=MASK_NONE, key_lens=None):
                                       Tq, Tk, d, float(scale), int(mask), _p(kl, ctypes.c_int32))
     if rc:
         raise RuntimeError("oracle_sdpa_backward failed")
+    return dq, dk, dv
+
+
+def sdpa_backward_tail(q, k, v, dout, i0, scale=None, mask=MASK_CAUSAL, key_lens=None):
+    """sdpa_backward summed over the query rows i >= i0 only: dq[..., i0:, :]
+    is the full gradient, and with a causal mask so are dk[..., i0:, :] and
+    dv[..., i0:, :] (no row before i0 sees those keys); dq rows before i0 are
+    0, dk and dv rows before i0 partial."""
+    q, k, v, dout = _d(q), _d(k), _d(v), _d(dout)
+    B, H, Tq, d = q.shape
+    Tk = k.shape[2]
+    if k.shape != (B, H, Tk, d) or v.shape != (B, H, Tk, d) or dout.shape != (B, H, Tq, d):
+        raise ValueError("shape mismatch (d_k must equal d_v)")
+    if not 0 <= i0 <= Tq:
+        raise ValueError("i0 out of range")
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    kl = _lens(key_lens, B)
+    dq, dk, dv = np.empty(q.shape), np.empty(k.shape), np.empty(v.shape)
+    rc = _load().oracle_sdpa_backward_tail(_p(q), _p(k), _p(v), _p(dout), _p(dq), _p(dk), _p(dv),
+                                           B, H, Tq, Tk, d, float(scale), int(mask),
+                                           _p(kl, ctypes.c_int32), int(i0))
+    if rc:
+        raise RuntimeError("oracle_sdpa_backward_tail failed")
     return dq, dk, dv
 
 

@@ -361,11 +361,11 @@ int oracle_sdpa_lse(const double *q, const double *k, double *lse, int B, int H,
  * P = 0 everywhere.  q, do (B,H,Tq,d); k, v (B,H,Tk,d); dq (B,H,Tq,d),
  * dk, dv (B,H,Tk,d).  The weights are recomputed here from q and k.
  */
-int oracle_sdpa_backward(const double *q, const double *k, const double *v, const double *dout,
-                         double *dq, double *dk, double *dv, int B, int H, int Tq, int Tk, int d,
-                         double scale, int mask_kind, const int32_t *key_lens)
+static int sdpa_backward_from(const double *q, const double *k, const double *v, const double *dout,
+                              double *dq, double *dk, double *dv, int B, int H, int Tq, int Tk,
+                              int d, double scale, int mask_kind, const int32_t *key_lens, int i0)
 {
-    if (B < 0 || H < 0 || Tq < 0 || Tk < 0 || d <= 0)
+    if (B < 0 || H < 0 || Tq < 0 || Tk < 0 || d <= 0 || i0 < 0 || i0 > Tq)
         return -1;
     const long BH = (long)B * H;
     int failed = 0;
@@ -389,7 +389,7 @@ int oracle_sdpa_backward(const double *q, const double *k, const double *v, cons
             dqb[x] = 0.0;
         for (size_t x = 0; x < (size_t)Tk * d; ++x)
             dkb[x] = dvb[x] = 0.0;
-        for (int i = 0; i < Tq; ++i) {
+        for (int i = i0; i < Tq; ++i) {
             const double *qi = qb + (size_t)i * d, *gi = gb + (size_t)i * d;
             /* P_i (the forward's weights) */
             double m = -INFINITY;
@@ -431,6 +431,30 @@ int oracle_sdpa_backward(const double *q, const double *k, const double *v, cons
         free(dp);
     }
     return failed ? -1 : 0;
+}
+
+int oracle_sdpa_backward(const double *q, const double *k, const double *v, const double *dout,
+                         double *dq, double *dk, double *dv, int B, int H, int Tq, int Tk, int d,
+                         double scale, int mask_kind, const int32_t *key_lens)
+{
+    return sdpa_backward_from(q, k, v, dout, dq, dk, dv, B, H, Tq, Tk, d, scale, mask_kind, key_lens,
+                              0);
+}
+
+/*
+ * The same sums taken over the query rows i >= i0 only (rows before i0 add
+ * nothing; their dq rows are left 0).  dq rows i >= i0 are then the full
+ * gradient, and under the causal mask (key j visible to row i iff j <= i)
+ * so are dk and dv rows j >= i0, which no earlier row sees: the tail of the
+ * gradient of a long sequence, at the cost of its last Tq - i0 rows.
+ */
+int oracle_sdpa_backward_tail(const double *q, const double *k, const double *v,
+                              const double *dout, double *dq, double *dk, double *dv, int B, int H,
+                              int Tq, int Tk, int d, double scale, int mask_kind,
+                              const int32_t *key_lens, int i0)
+{
+    return sdpa_backward_from(q, k, v, dout, dq, dk, dv, B, H, Tq, Tk, d, scale, mask_kind, key_lens,
+                              i0);
 }
 
 /*

@@ -105,3 +105,19 @@ def test_backward_masked_keys_get_no_gradient(lib):
     dq, dk, dv = run_backward(lib, w, x, si.f64_to_bf16_bits(dout))
     assert np.all(dk[0] == 0) and np.all(dv[0] == 0) and np.all(dq[0] == 0)
     assert np.all(dk[1, :, 77:] == 0) and np.all(dv[1, :, 77:] == 0)
+
+
+def test_backward_tail_rows_workload_full(lib):
+    """The backward at the benchmark's full size (causal, B=2, h=16,
+    T=8192, d=64), compared with the fp64 oracle where its tail sums are the
+    full gradient: dq of the last 256 query rows (each sums over up to every
+    key) and dk, dv of the last 256 keys (two key blocks, each summed over the
+    query rows that see it), every head, every element of those rows."""
+    w = si.WORKLOADS[4]
+    x = si.make_inputs(w)
+    dout = si.round_bf16(si.normal(w.seed, si.TENSOR_IDS["dout"], x["q"].shape))
+    got = run_backward(lib, w, x, si.f64_to_bf16_bits(dout))
+    i0 = w.T_q - 256
+    ref = oracle.sdpa_backward_tail(x["q"], x["k"], x["v"], dout, i0, scale=w.scale, mask=w.mask)
+    for name, g, r in zip(("dq", "dk", "dv"), got, ref):
+        check_grad(g[:, :, i0:], r[:, :, i0:], name + " (last 256 rows)")

@@ -564,6 +564,30 @@ def test_backward_key_gradients_sum_to_zero_and_masked_keys_get_none():
     np.testing.assert_allclose(dv[:, :, 0], g.sum(axis=2), atol=1e-13)
 
 
+@pytest.mark.parametrize("mask", [MASK_CAUSAL, MASK_CAUSAL_KEY_PADDING])
+def test_backward_tail_equals_the_full_gradient_where_it_claims_to(mask):
+    # Under the causal mask no query row before i0 sees a key at or after i0,
+    # so the tail sums give exactly the full dq rows >= i0 and dk, dv rows
+    # >= i0 (same terms, same order); the rows it does not claim differ.
+    rng = np.random.default_rng(104)
+    B, H, T, d = 2, 2, 37, 8
+    q, g = rng.normal(size=(B, H, T, d)), rng.normal(size=(B, H, T, d))
+    k, v = rng.normal(size=(B, H, T, d)), rng.normal(size=(B, H, T, d))
+    lens = np.array([T, 23], dtype=np.int32)
+    kl = lens if mask & MASK_KEY_PADDING else None
+    full = oracle.sdpa_backward(q, k, v, g, scale=0.3, mask=mask, key_lens=kl)
+    for i0 in (0, 1, 17, 36, 37):
+        dq, dk, dv = oracle.sdpa_backward_tail(q, k, v, g, i0, scale=0.3, mask=mask, key_lens=kl)
+        assert np.array_equal(dq[:, :, i0:], full[0][:, :, i0:])
+        assert np.all(dq[:, :, :i0] == 0)
+        assert np.array_equal(dk[:, :, i0:], full[1][:, :, i0:])
+        assert np.array_equal(dv[:, :, i0:], full[2][:, :, i0:])
+    dq, dk, dv = oracle.sdpa_backward_tail(q, k, v, g, 17, scale=0.3, mask=mask, key_lens=kl)
+    assert not np.allclose(dv[:, :, :17], full[2][:, :, :17])  # partial there
+    with pytest.raises(ValueError):
+        oracle.sdpa_backward_tail(q, k, v, g, T + 1, mask=mask, key_lens=kl)
+
+
 # ------------------------------------------ encoder layer: PE, FFN, composition
 def test_positional_encoding_toy_table_from_the_pages():
     g = GOLDEN["positional_encoding_toy"]
