@@ -1,6 +1,7 @@
 /*
  * mha.h -- C ABI of the GB300 (sm_103a) multi-head scaled dot-product
- * attention forward library (libmha.so).
+ * attention library (libmha.so): forward, backward, decode step and the
+ * surrounding encoder-layer pieces.
  *
  * The operation (cited by page title and section):
  *
