@@ -126,6 +126,9 @@ constexpr float kTileSumLimit = 65536.0f;  // 2^16: a tile sum above it takes th
 // Per-batch key lengths are read from the CTA's shared-memory copy when it
 // holds them all (B <= kLensCache), else from global memory.
 constexpr int kLensCache = 1024;
+// The geometry of a CTA's first kItemTable items is computed once, in the
+// prologue, into shared memory (every role looks each item up).
+constexpr int kItemTable = 64;
 
 struct __align__(1024) SmemAttn {
     uint8_t q[2][kTileBytes];
@@ -147,6 +150,8 @@ struct __align__(1024) SmemAttn {
     uint64_t o_free;             // accumulators read (4 output warps)
     uint64_t drain[3];           // one per MMA-issuing warp
     int lens[kLensCache];        // key_lens[0 .. B) when B <= kLensCache
+    int item_tab[kItemTable][6]; // this CTA's first items: bh, b, hh, q0, kv_len, n_kv
+    int n_items;                 // items this CTA walks
     uint32_t tmem_base;
     int abort_flag;
 };
@@ -181,6 +186,18 @@ __device__ __forceinline__ Item make_item(const AttnParams &p, int k, const int 
     it.kv_len = kv_len;
     const int kv_end = (p.mask & kMaskCausalBit) ? min(kv_len, min(it.q0 + BM, p.Tq)) : kv_len;
     it.n_kv = (kv_end + BN - 1) / BN;
+    return it;
+}
+
+__device__ __forceinline__ Item item_of(const SmemAttn &sm, const AttnParams &p, int t, int cta, int G) {
+    if (t >= kItemTable) return make_item(p, item_index(t, cta, G), sm.lens);
+    Item it;
+    it.bh = sm.item_tab[t][0];
+    it.b = sm.item_tab[t][1];
+    it.hh = sm.item_tab[t][2];
+    it.q0 = sm.item_tab[t][3];
+    it.kv_len = sm.item_tab[t][4];
+    it.n_kv = sm.item_tab[t][5];
     return it;
 }
 
@@ -242,6 +259,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
+    {
+        const int F = total / G, rem = total - F * G;
+        if (threadIdx.x == 0) sm.n_items = F + ((((F & 1) ? (G - 1 - cta) : cta) < rem) ? 1 : 0);
+        for (int t = threadIdx.x; t < kItemTable; t += kThreads) {
+            const int k = item_index(t, cta, G);
+            if (k < total) {
+                const Item it = make_item(p, k, sm.lens);
+                sm.item_tab[t][0] = it.bh;
+                sm.item_tab[t][1] = it.b;
+                sm.item_tab[t][2] = it.hh;
+                sm.item_tab[t][3] = it.q0;
+                sm.item_tab[t][4] = it.kv_len;
+                sm.item_tab[t][5] = it.n_kv;
+            }
+        }
+        __syncthreads();
+    }
     const uint32_t tmem = sm.tmem_base;
     const AbortState ab{&sm.abort_flag, p.status, p.wait_limit_ns};
     // Programmatic dependent launch: the next kernel may begin its prologue;
@@ -265,9 +299,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             int g = 0, v = 0;
             bool ok = true;
             for (int t = 0; ok; ++t) {
-                const int k = item_index(t, cta, G);
-                if (k >= total) break;
-                const Item it = make_item(p, k, sm.lens);
+                if (t >= sm.n_items) break;
+                const Item it = item_of(sm, p, t, cta, G);
                 if (it.n_kv == 0) continue;
                 const int qbuf = v & 1;
                 // Q buffer qbuf last served item v-2: wait until all of its
@@ -312,9 +345,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int g = 0, v = 0;
         bool ok = true;
         for (int t = 0; ok; ++t) {
-            const int k = item_index(t, cta, G);
-            if (k >= total) break;
-            const Item it = make_item(p, k, sm.lens);
+            if (t >= sm.n_items) break;
+            const Item it = item_of(sm, p, t, cta, G);
             if (it.n_kv == 0) continue;
             const int qbuf = v & 1;
             if (!(ok = warp_wait(&sm.q_full[qbuf], (v >> 1) & 1, ab))) break;
@@ -364,9 +396,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int g = 0, v = 0;
         bool ok = true;
         for (int t = 0; ok; ++t) {
-            const int k = item_index(t, cta, G);
-            if (k >= total) break;
-            const Item it = make_item(p, k, sm.lens);
+            if (t >= sm.n_items) break;
+            const Item it = item_of(sm, p, t, cta, G);
             if (it.n_kv == 0) continue;
             if (v >= 1 && !(ok = warp_wait(&sm.o_free, (v - 1) & 1, ab))) break;
             for (int j = 0; j < it.n_kv; ++j, ++g) {
@@ -485,9 +516,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int g = 0, v = 0;
         bool ok = true;
         for (int t = 0; ok; ++t) {
-            const int k = item_index(t, cta, G);
-            if (k >= total) break;
-            const Item it = make_item(p, k, sm.lens);
+            if (t >= sm.n_items) break;
+            const Item it = item_of(sm, p, t, cta, G);
             if (it.n_kv == 0) continue;
             const int row = it.q0 + r;  // query index
             const int row_lim = causal ? min(it.kv_len, row + 1) : it.kv_len;  // keys < row_lim visible
@@ -629,9 +659,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int v = 0;
         bool ok = true;
         for (int t = 0; ok; ++t) {
-            const int k = item_index(t, cta, G);
-            if (k >= total) break;
-            const Item it = make_item(p, k, sm.lens);
+            if (t >= sm.n_items) break;
+            const Item it = item_of(sm, p, t, cta, G);
             const int row = it.q0 + r;
             __nv_bfloat16 *dst = p.o + it.b * p.o_stride_b + it.hh * p.o_stride_h +
                                  static_cast<long long>(row) * p.o_stride_t;
