@@ -89,10 +89,13 @@
 // the group's current reference maximum (softmax is shift-invariant, so any
 // reference that keeps the exponentials finite gives the same result), and
 // only a row whose round sum exceeds 2^16 -- its maximum grew by 10 to 16
-// log2 units or more -- or that has no reference yet takes the exact step
-// (round maximum, O_h and l_h rescaled -- in round 1 after the round-0
-// product, taken against the old reference, has landed in O_h -- P
-// recomputed).  Decided per row.
+// log2 units or more -- takes the exact step (round maximum, O_h and l_h
+// rescaled -- in round 1 after the round-0 product, taken against the old
+// reference, has landed in O_h -- P recomputed).  Unless the log-sum-exp
+// is exported, a row's first round is taken against the reference 0 and
+// kept if its sum lies in [2^-64, 2^16] (0 then becomes the reference);
+// otherwise, or with no visible key, or with lse exported, it takes the
+// exact step.  Decided per row.
 //
 // Tensor memory (512 columns): S buffers [0,128), [128,256), [256,384);
 // O_A [384,448), O_B [448,512).  P (bf16, two keys per column) goes over
@@ -123,6 +126,9 @@ constexpr uint32_t kTileBytes = BM * HD * 2;  // 16 KiB, one 128 x 64 bf16 tile
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kOCol = 384;  // O_A [384,448), O_B [448,512)
 constexpr float kTileSumLimit = 65536.0f;  // 2^16: a tile sum above it takes the exact step
+// A row's first round is tried against the reference 0; a sum below 2^-64
+// (the scores far below 0, or none visible) takes the exact step instead.
+constexpr float kFirstSumMin = 5.421010862427522e-20f;  // 2^-64
 // Per-batch key lengths are read from the CTA's shared-memory copy when it
 // holds them all (B <= kLensCache), else from global memory.
 constexpr int kLensCache = 1024;
@@ -201,7 +207,7 @@ __device__ __forceinline__ Item item_of(const SmemAttn &sm, const AttnParams &p,
     return it;
 }
 
-template <bool kTiles>
+template <bool kTiles, bool kLse>
 __global__ void __launch_bounds__(kThreads, 1)
     attn_fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmap_q,
                          const __grid_constant__ CUtensorMap tmap_k,
@@ -447,12 +453,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         // therefore exponentiated straight against the current m_h (no
         // maximum pass), and the row checks its own round sum: only a row
         // whose sum exceeds 2^16 (its maximum grew by 10 to 16 log2 units or
-        // more, or overflowed) or that has not yet seen a visible key takes
-        // the exact step -- round maximum, new m_h, O_h and l_h scaled by
-        // 2^((m_old - m_new) c), P recomputed; in the second round O_h is
-        // scaled once the first round's product is in it.  Each decision
-        // uses only the row's own visible scores, so a row's result never
-        // depends on another row or on masked keys.
+        // more, or overflowed) takes the exact step -- round maximum, new
+        // m_h, O_h and l_h scaled by 2^((m_old - m_new) c), P recomputed; in
+        // the second round O_h is scaled once the first round's product is in
+        // it.  Before the row has a reference its round is taken against 0
+        // (any finite reference is valid) and kept when the sum lies in
+        // [2^-64, 2^16] -- scores within about 16 log2 units of 0, as scaled
+        // scores usually are; a sum outside (or no visible key, or an
+        // exported lse) takes the exact step.  Each decision uses only the row's own visible scores,
+        // so a row's result never depends on another row or on masked keys.
         const int half = warp >> 2;  // the group (by tiles) or key half (by halves)
         constexpr int kRounds = kTiles ? 2 : 1;  // 64-score rounds per tile
         const uint32_t lane_base = static_cast<uint32_t>(warp & 3) * 32;
@@ -460,6 +469,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tl = tmem_addr(tmem, lane_base, 0);
         const uint32_t to = tl + kOCol + 64u * half;         // O_h: 64 columns
         const float C = p.scale_log2;
+        // The first-round reference 0 only when no log-sum-exp is exported:
+        // with the exact first step the row's largest weight is exactly 1,
+        // so lse (and the weights a backward pass recomputes from it) carry
+        // no rounding of that term.
+        constexpr bool guess_first = !kLse;
 
         // Keys at or past `lim` (relative to the round's first key) get -inf:
         // weight exactly zero.
@@ -540,8 +554,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int lim = row_lim - (j * BN + c0);
                     uint32_t pk[32];
                     float lt = 0.f;
-                    bool need = true;  // the first round of the item: no reference yet
-                    if (kTiles ? (j >= 2 || rd == 1) : j > 0) {
+                    bool need = true;  // no reference yet: exact unless the guess holds
+                    if (guess_first || (kTiles ? (j >= 2 || rd == 1) : j > 0)) {
                         uint32_t s0[32], s1[32];
                         tmem_ld32(tr, s0);
                         tmem_ld32(tr + 32, s1);
@@ -549,7 +563,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         reg_fence32(s1);
                         if (edge) mask_scores(s0, s1, lim);
                         lt = exp_tile(s0, s1, m_run == -INFINITY ? 0.f : m_run * C, pk);
-                        need = m_run == -INFINITY || !(lt <= kTileSumLimit);
+                        // without a reference yet, the round was taken against 0:
+                        // kept if its sum lies in [2^-64, 2^16], which then
+                        // becomes the row's reference
+                        need = m_run == -INFINITY
+                                   ? !(guess_first && lt >= kFirstSumMin && lt <= kTileSumLimit)
+                                   : !(lt <= kTileSumLimit);
+                        if (!need && m_run == -INFINITY) m_run = 0.f;
                     }
                     if (__any_sync(0xffffffffu, need)) {
                         uint32_t s0[32], s1[32];
@@ -755,7 +775,9 @@ cudaError_t launch_attn_bf16(const CUtensorMap &tq, const CUtensorMap &tk,
                              const CUtensorMap &tv, const AttnParams &p, cudaStream_t stream,
                              bool pdl) {
     const bool by_tiles = attn_bf16_splits_by_tiles(p.Tq, p.Tk, p.mask);
-    auto kernel = by_tiles ? attn_fwd_bf16_kernel<true> : attn_fwd_bf16_kernel<false>;
+    // kLse: the log-sum-exp is exported (the first round always exact)
+    auto kernel = p.lse ? (by_tiles ? attn_fwd_bf16_kernel<true, true> : attn_fwd_bf16_kernel<false, true>)
+                        : (by_tiles ? attn_fwd_bf16_kernel<true, false> : attn_fwd_bf16_kernel<false, false>);
     const size_t smem = sizeof(SmemAttn) + 1024;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
