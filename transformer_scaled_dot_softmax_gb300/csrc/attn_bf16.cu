@@ -570,6 +570,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    ? !(guess_first && lt >= kFirstSumMin && lt <= kTileSumLimit)
                                    : !(lt <= kTileSumLimit);
                         if (!need && m_run == -INFINITY) m_run = 0.f;
+                        // by halves (short items) a round with no visible key
+                        // for this row -- the second key half of a diagonal
+                        // tile -- has P = 0 exactly and needs no exact step (a
+                        // missing reference stays missing)
+                        if (!kTiles && lim <= 0) need = false;
                     }
                     if (__any_sync(0xffffffffu, need)) {
                         uint32_t s0[32], s1[32];
