@@ -98,7 +98,10 @@ def test_config1_fp32_full(lib):
 
 
 @pytest.mark.parametrize("mask", list(MASK_NAMES))
-@pytest.mark.parametrize("T_q,T_k,d", [(37, 53, 64), (16, 16, 32), (5, 200, 128), (130, 7, 64)])
+# T_k <= 32 with d = 64 runs the short-key (register) kernel, the rest the
+# chunked one: (33, 32) and (9, 1) sit at its limits, (40, 33) just past.
+@pytest.mark.parametrize("T_q,T_k,d", [(37, 53, 64), (16, 16, 32), (5, 200, 128), (130, 7, 64),
+                                       (33, 32, 64), (9, 1, 64), (40, 33, 64)])
 def test_fp32_masks_and_ragged(lib, mask, T_q, T_k, d):
     w = si.WORKLOADS[0].replace(B=2, h=3, T_q=T_q, T_k=T_k, d_k=d, d_v=d, mask=mask, len_lo=1,
                                 len_hi=T_k, seed=11)
@@ -108,6 +111,49 @@ def test_fp32_masks_and_ragged(lib, mask, T_q, T_k, d):
     torch.cuda.synchronize()
     ref = oracle.sdpa(x["q"], x["k"], x["v"], scale=w.scale, mask=mask, key_lens=x["key_lens"])
     assert np.abs(host(out) - ref).max() <= F32_MAX
+
+
+@pytest.mark.parametrize("T_k", [20, 50])
+def test_fp32_rows_without_visible_keys(lib, T_k):
+    """Key lengths of 0 leave whole sequences without a visible key: their
+    rows are zeros in both fp32 kernels (short-key and chunked); the other
+    sequences match the oracle."""
+    w = si.WORKLOADS[0].replace(B=4, h=2, T_q=13, T_k=T_k, mask=si.MASK_CAUSAL_KEY_PADDING,
+                                len_lo=1, len_hi=T_k, seed=17)
+    x = si.make_inputs(w)
+    lens = np.array([0, T_k, 0, 3], dtype=np.int32)
+    out = lib.sdpa_forward(f32_dev(x["q"]), f32_dev(x["k"]), f32_dev(x["v"]), scale=w.scale,
+                           mask="causal_key_padding", key_lens=torch.from_numpy(lens).to(dev()))
+    torch.cuda.synchronize()
+    got = host(out)
+    assert np.all(got[lens == 0] == 0.0)
+    ref = oracle.sdpa(x["q"], x["k"], x["v"], scale=w.scale, mask=si.MASK_CAUSAL_KEY_PADDING,
+                      key_lens=lens)
+    assert np.abs(got[lens > 0] - ref[lens > 0]).max() <= F32_MAX
+
+
+def test_fp32_unaligned_rows_take_the_chunked_kernel(lib):
+    """q and k starting 4 bytes past a 16-byte boundary cannot be read as
+    float4: the short-key case then runs the chunked kernel, with the same
+    result bit for bit."""
+    w = si.WORKLOADS[0].replace(B=1, h=3, T_q=21, T_k=24, mask=si.MASK_CAUSAL, seed=19)
+    x = si.make_inputs(w)
+    q, k, v = (f32_dev(x[n]) for n in ("q", "k", "v"))
+    aligned = lib.sdpa_forward(q, k, v, scale=w.scale, mask="causal")
+
+    def shifted(t):
+        buf = torch.empty(t.numel() + 1, dtype=torch.float32, device=dev())
+        view = buf[1:].view(t.shape)
+        view.copy_(t)
+        return view
+
+    qs, ks = shifted(q), shifted(k)
+    assert qs.data_ptr() % 16 != 0 and ks.data_ptr() % 16 != 0
+    unaligned = lib.sdpa_forward(qs, ks, v, scale=w.scale, mask="causal")
+    torch.cuda.synchronize()
+    assert torch.equal(aligned, unaligned)
+    ref = oracle.sdpa(x["q"], x["k"], x["v"], scale=w.scale, mask=si.MASK_CAUSAL)
+    assert np.abs(host(unaligned) - ref).max() <= F32_MAX
 
 
 # ----------------------------------------------------------------- bf16 SDPA
