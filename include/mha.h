@@ -86,7 +86,10 @@ typedef enum { MHA_F32 = 0, MHA_BF16 = 1 } mha_dtype;
  *   o (B, h, T_q, d_v): element type `dt` (fp32 or bf16).
  *   scale: usually 1/sqrt(d_k) (aiany.app, Step 5: "divide by 8" for 64).
  *
- * MHA_F32: fp32 SIMT kernel (FFMA + expf), d_k, d_v <= 128.
+ * MHA_F32: fp32 SIMT kernel (FFMA + expf), d_k, d_v <= 128, 4-byte aligned
+ *   arrays (with T_k <= 32, d_k == d_v == 64 and 16-byte aligned q, k a
+ *   register kernel holding a row's whole key set runs instead, with the same
+ *   result bit for bit).
  * MHA_BF16: fused tcgen05 kernel (TMA tiles, QK^T and PV on the tensor cores
  *   with fp32 accumulators in tensor memory, online softmax in registers; the
  *   T_q x T_k score matrix never reaches global memory).  Requires
