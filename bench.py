@@ -398,7 +398,7 @@ def time_other_workloads(dev, stream, flush, iters=20):
     q, k, v = (torch.from_numpy(x[n].astype(np.float32)).to(dev) for n in ("q", "k", "v"))
     o = torch.empty_like(q)
     ms = timed(lambda: tsds.sdpa_forward(q, k, v, o, scale=w.scale, stream=stream))
-    res[w.name] = {"ms": ms, "us": 1e3 * ms, "kind": "fp32 SIMT SDPA, launch-bound"}
+    res[w.name] = {"ms": ms, "us": 1e3 * ms, "kind": "fp32 SIMT SDPA (register kernel for T_k <= 32): one memory round trip + launch latency"}
     for w in si.WORKLOADS[1:4]:
         x = si.make_inputs(w)
         xq = dv(x["x_q_bits"])
